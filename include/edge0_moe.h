@@ -1,0 +1,227 @@
+/*
+ * edge0_moe.h — C ABI of the latent-MoE layer library (libedge0_moe.so), B300 / sm_103a.
+ *
+ * The layer (one token; the pages' description):
+ *   z = D x                       down-projection 2560 -> l, one D per layer
+ *   l_e = R_e . z + b_e            router logits over the routed experts
+ *   top-k experts by (logit desc, index asc), weights = softmax renormalised over the k
+ *   o_e = W_d,e (silu(W_g,e z) * (W_up,e z))   each expert l -> 640 -> l, NVFP4 weights
+ *   c = o_shared + sum_k w_k o_(e_k)           the shared expert runs alongside, weight 1
+ *   y = U c                       up-projection l -> 2560, one U per layer
+ * Sources: "Edge0-145B hardware requirements", section "Edge0-145B latent MoE
+ * architecture: how 145B fits one GPU" (widths 2560 and 1792, 512 routed + 1
+ * shared expert, 10 picked per token, D and U shared by the experts);
+ * "Edge0-145B · Q3_K" model card, section "Architecture" (diagram caption:
+ * D, router, experts l -> 640 -> l, shared expert, U; one D/U per layer;
+ * config block: SwiGLU width 640); "Edge0 Squeezes a 145B Coding Agent...",
+ * table "Released model variants" (latent 1792 for 145B, 1280 for 120B);
+ * "Edge0-145B en local", introduction (experts in NVFP4, NVIDIA's 4-bit float).
+ * The softmax/top-k rule, tie-break, NVFP4 record layout and this interface
+ * are this library's readings; the pages print no formula or layout.
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" point to CUDA device memory of the current device;
+ *     "host" pointers to host memory.  The caller owns every buffer it passes.
+ *   - Device pointers must be 16-byte aligned; expert records 256-byte aligned.
+ *   - bf16 tensors are row-major arrays of IEEE bfloat16 (uint16 bit patterns).
+ *   - Calls taking a stream are asynchronous with respect to the host, enqueue
+ *     work on that stream (NULL = the legacy default stream) and do not
+ *     synchronise, except where stated.
+ *   - Errors are returned as edge0_status; nothing is printed and nothing exits.
+ *     Asynchronous device-side failures (a bounded wait that ran out) are
+ *     recorded in the handle's error word and reported by edge0_moe_get_error.
+ */
+#ifndef EDGE0_MOE_H
+#define EDGE0_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *edge0_stream_t;
+
+typedef enum {
+  EDGE0_OK = 0,
+  EDGE0_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or alignment */
+  EDGE0_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve */
+  EDGE0_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  EDGE0_ERR_OOM = 4,          /* workspace allocation failed */
+  EDGE0_ERR_TIMEOUT = 5       /* a device-side bounded wait ran out */
+} edge0_status;
+
+/*
+ * NVFP4 expert record (one per expert, this library's layout).
+ * Format (NVFP4 = E2M1 elements, one E4M3 scale per 16 consecutive weights
+ * along the input dimension K, one fp32 scale g per matrix):
+ *     w[r][k] = e2m1(code[r][k]) * e4m3(scale[r][k/16]) * g
+ * For latent L (a multiple of 256) and SwiGLU width F (a multiple of 64) a record holds, in
+ * order and without gaps:
+ *     gate codes  [F][L/2]   up codes  [F][L/2]   down codes  [L][F/2]
+ *     gate scales [F][L/16]  up scales [F][L/16]  down scales [L][F/16]
+ *     fp32 g: gate, up, down (little-endian)
+ * W_gate, W_up are [F x L] (K = L); W_down is [L x F] (K = F).  Two codes per
+ * byte, the even element in the low nibble.  E4M3 is OCP E4M3FN (bias 7,
+ * subnormals m * 2^-9, no infinities; the NaN bytes 0x7F/0xFF must not occur).
+ * For L=1792, F=640 the codes and scales take 1,935,360 bytes, the size that
+ * 48 layers x 512 experts of the 47.6 GB NVFP4 experts.bin imply ("Edge0-145B
+ * Review", table in section "Warum 29 GB nicht wirklich in 29 GB passen").
+ */
+
+/* Bytes of one record: codes + scales + 12 bytes of fp32 scales.  0 on bad shapes. */
+size_t edge0_expert_record_bytes(int latent, int ffn);
+
+/* Default distance between records in an array: record bytes rounded up to 256. */
+size_t edge0_expert_record_stride(int latent, int ffn);
+
+/*
+ * Pack one expert from its per-matrix arrays into a record (host memory).
+ *   codes   host, 3*F*L/2 bytes: gate [F][L/2], up [F][L/2], down [L][F/2]
+ *   scales  host, 3*F*L/16 bytes: gate [F][L/16], up [F][L/16], down [L][F/16]
+ *   globals host, 3 floats: gate, up, down
+ *   record_out host, edge0_expert_record_bytes(latent, ffn) bytes, caller-owned.
+ * Returns INVALID_ARG on NULL pointers or unsupported shapes.
+ */
+edge0_status edge0_pack_expert_host(const uint8_t *codes, const uint8_t *scales,
+                                    const float *globals, int latent, int ffn,
+                                    void *record_out);
+
+/*
+ * Pack n_experts experts on the device (same per-expert arrays, back to back).
+ *   codes    device, n_experts * 3*F*L/2 bytes
+ *   scales   device, n_experts * 3*F*L/16 bytes
+ *   globals  device, n_experts * 3 floats
+ *   records  device, n_experts * stride bytes, 256-byte aligned; stride >=
+ *            edge0_expert_record_bytes and a multiple of 16.
+ * Bytes between a record's end and the next stride boundary are left untouched.
+ */
+edge0_status edge0_pack_experts(const uint8_t *codes, const uint8_t *scales,
+                                const float *globals, int n_experts, int latent,
+                                int ffn, void *records, size_t stride,
+                                edge0_stream_t stream);
+
+/*
+ * Quantise an fp32 matrix to NVFP4 on the device (the format fixes the
+ * decoder, not the quantiser; this is the plain reading):
+ *   scale[r][b] = E4M3 round-to-nearest-even of amax(block) / (6 g), max 448;
+ *   code[r][k]  = nearest E2M1 value to w / (e4m3(scale) g), ties to the even
+ *                 code, saturating at +-6; an all-zero block gets scale 0.
+ *   w       device fp32 [rows][K], K a multiple of 16
+ *   codes   device uint8 [rows][K/2]; scales device uint8 [rows][K/16]
+ */
+edge0_status edge0_quantize_nvfp4(const float *w, int rows, int K, float g,
+                                  uint8_t *codes, uint8_t *scales,
+                                  edge0_stream_t stream);
+
+/* One layer's shapes and borrowed device weights. */
+typedef struct {
+  int hidden;     /* 2560 */
+  int latent;     /* l: 1792 (145B) or 1280 (120B); multiple of 256 */
+  int n_experts;  /* 512 routed experts */
+  int top_k;      /* 10 */
+  int ffn;        /* SwiGLU width 640; multiple of 64 */
+  int max_tokens; /* largest T forward will accept (workspace sizing) */
+  const void *D;            /* device bf16 [latent][hidden] */
+  const void *U;            /* device bf16 [hidden][latent] */
+  const void *router;       /* device bf16 [n_experts][latent] */
+  const float *router_bias; /* device fp32 [n_experts], or NULL for zeros */
+  const void *experts;      /* device, n_experts records, 256-byte aligned */
+  size_t expert_stride;     /* bytes between records; multiple of 256 */
+  const void *shared_expert;/* device, one record, 256-byte aligned */
+} edge0_moe_desc;
+
+/*
+ * Create a layer handle.  Validates shapes and alignment, records the
+ * borrowed pointers (which must stay valid for the handle's lifetime) and
+ * allocates the workspace for max_tokens (the handle owns only that).
+ * Supported shapes: hidden % 64 == 0, latent % 256 == 0, ffn % 64 == 0,
+ * 1 <= top_k <= 16, top_k <= n_experts <= 1024, n_experts % 32 == 0.  Launches no kernel.
+ * Returns INVALID_ARG, UNSUPPORTED, CUDA or OOM on failure (*handle_out = NULL).
+ */
+edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);
+
+/*
+ * y = Layer(x) for T tokens.  x device bf16 [T][hidden]; y device bf16
+ * [T][hidden] (round to nearest even); x and y must not overlap.
+ * T = 0 is a no-op; T > max_tokens returns INVALID_ARG.  T <= 16 runs the
+ * decode path (one persistent kernel); larger T the prefill path.
+ * Calls on one handle must be ordered (one stream, or synchronised): they
+ * share the handle's workspace.
+ */
+edge0_status edge0_moe_forward(void *handle, const void *x, void *y, int T,
+                               edge0_stream_t stream);
+
+/*
+ * Copy the routing of the last forward on this handle into caller buffers
+ * (any may be NULL), stream-ordered after it:
+ *   idx    device int32 [T][top_k], experts in rank order
+ *   w      device fp32  [T][top_k], renormalised weights
+ *   counts device int32 [n_experts], slots per expert
+ *   offsets device int32 [n_experts + 1], exclusive prefix sum of counts
+ *   perm   device int32 [T*top_k], slot (t*top_k + j) at each grouped position;
+ *          groups in expert order, slots ascending within a group
+ *   pos    device int32 [T*top_k], grouped position of each slot
+ */
+edge0_status edge0_moe_debug_routing(void *handle, int *idx, float *w, int *counts,
+                                     int *offsets, int *perm, int *pos,
+                                     edge0_stream_t stream);
+
+/*
+ * Copy an intermediate of the last forward (for stage-by-stage parity):
+ *   what = 0: z fp32 [T][latent]; 1: router logits fp32 [T][n_experts]
+ *   (2: combined latent c fp32 [T][latent]).  dst device, `bytes` >= size.
+ * Returns UNSUPPORTED if the last forward's path does not materialise it.
+ */
+edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t bytes,
+                                    edge0_stream_t stream);
+
+/*
+ * Post-norm residual between stacked layers (bf16 in, bf16 out):
+ *   out[t] = bf16( v / sqrt(mean(v^2) + eps) ),  v = x[t] + y[t]  (fp32 inside)
+ * x, y, out device bf16 [T][hidden]; out may alias x or y.
+ */
+edge0_status edge0_residual_rmsnorm(const void *x, const void *y, void *out, int T,
+                                    int hidden, float eps, edge0_stream_t stream);
+
+/*
+ * Run n_layers layers in sequence with the post-norm residual between them:
+ *   x_0 = x;  x_{i+1} = RMSNorm(x_i + Layer_i(x_i));  y = x_n
+ * handles: host array of n_layers handles of identical shapes; T <= 16
+ * (decode) runs all layers in one persistent kernel.  x, y device bf16
+ * [T][hidden], may be the same buffer.  Larger T chains forward and
+ * edge0_residual_rmsnorm per layer.
+ */
+edge0_status edge0_moe_stack_forward(void *const *handles, int n_layers, const void *x,
+                                     void *y, int T, float eps, edge0_stream_t stream);
+
+/*
+ * edge0_moe_stack_forward that also records every layer's input and output
+ * (for layer-by-layer checks): trace_x, trace_y device bf16 [n_layers][T][hidden]
+ * (either may be NULL).  Decode sizes only (T <= 16, n_layers <= 64); other
+ * sizes return UNSUPPORTED when a trace is requested.
+ */
+edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, const void *x,
+                                           void *y, int T, float eps, void *trace_x,
+                                           void *trace_y, edge0_stream_t stream);
+
+/*
+ * Synchronise with the device and return the handle's device error word
+ * (EDGE0_OK, or EDGE0_ERR_TIMEOUT if a bounded device wait ran out since the
+ * last call); clears the word.
+ */
+edge0_status edge0_moe_get_error(void *handle);
+
+/* Static text for a status code. */
+const char *edge0_status_string(edge0_status status);
+
+/* Free the handle's workspace (synchronises the device first).  NULL is a no-op. */
+void edge0_moe_destroy(void *handle);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EDGE0_MOE_H */

@@ -1,0 +1,525 @@
+// C ABI of the latent-MoE layer library (declared in include/edge0_moe.h).
+#include "../../include/edge0_moe.h"
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "decode.cuh"
+#include "prefill.cuh"
+
+namespace edge0 {
+int decode_bucket(int T);
+cudaError_t decode_prepare(int smem);
+cudaError_t decode_occupancy(int smem, int* blocks);
+cudaError_t decode_launch(const DecodeArgs& a, int grid, int smem, cudaStream_t s);
+}  // namespace edge0
+
+using namespace edge0;
+
+namespace {
+
+constexpr int kStackMax = 64;
+
+struct Handle {
+  edge0_moe_desc d;
+  int device = 0;
+  int num_sms = 0;
+  int smem_total = 0;         // dynamic shared memory of the decode kernel
+  int dec_max_t = 0;          // decode workspace tokens
+  char* ws = nullptr;         // one allocation for the whole workspace
+  size_t ws_bytes = 0;
+  float* z = nullptr; float* logits = nullptr; float* h = nullptr; unsigned* hmax = nullptr;
+  float* c = nullptr;
+  __nv_bfloat16* ybuf = nullptr; __nv_bfloat16* xbuf = nullptr;
+  int* idx = nullptr; float* w = nullptr; int* counts = nullptr; int* offsets = nullptr;
+  int* perm = nullptr; int* pos = nullptr;
+  GridBarrier* bar = nullptr; int* err = nullptr;
+  LayerW* d_layer = nullptr;  // this layer (1 entry)
+  LayerW* d_stack = nullptr;  // kStackMax entries for stack calls
+  PrefillWorkspace pf;        // prefill path buffers (T > 16)
+  int last_T = 0;
+  int last_path = 0;          // 0 none, 1 decode, 2 prefill
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool shapes_ok(int latent, int ffn) {
+  return latent > 0 && ffn > 0 && latent % 256 == 0 && ffn % 64 == 0;
+}
+
+// Shared-memory plan of the decode kernel for token bucket TB.
+void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
+  const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts;
+  size_t off = decode_tables_bytes();
+  size_t act = TB * (size_t)H * 2;
+  if (TB * (size_t)L * 4 > act) act = TB * (size_t)L * 4;
+  if (TB * (size_t)E * 4 > act) act = TB * (size_t)E * 4;
+  act = align_up(act, 128);
+  const size_t zh = align_up(TB * (size_t)L * 2, 128);
+  int res_rows = 2048 / TB;
+  if (res_rows > 256) res_rows = 256;
+  const size_t res = align_up(2 * (size_t)res_rows * TB * 4, 128);
+  a.off_act = (int)off;
+  a.act_bytes = (int)act;
+  a.off_zh = (int)(off + act);
+  a.off_slab = (int)(off + act + zh);
+  a.slab_bytes = (int)(hd->smem_total - (off + act + zh + res)) & ~127;
+  a.off_res = a.off_slab + a.slab_bytes;
+  a.res_rows = res_rows;
+}
+
+edge0_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA; }
+
+LayerW layer_of(const Handle* hd) {
+  LayerW l;
+  l.D = static_cast<const __nv_bfloat16*>(hd->d.D);
+  l.U = static_cast<const __nv_bfloat16*>(hd->d.U);
+  l.R = static_cast<const __nv_bfloat16*>(hd->d.router);
+  l.bias = hd->d.router_bias;
+  l.experts = static_cast<const uint8_t*>(hd->d.experts);
+  l.shared = static_cast<const uint8_t*>(hd->d.shared_expert);
+  l.stride = hd->d.expert_stride;
+  return l;
+}
+
+void fill_decode_args(const Handle* hd, DecodeArgs& a, const void* x, void* y, int T) {
+  memset(&a, 0, sizeof(a));
+  a.layers = hd->d_layer;
+  a.n_layers = 1;
+  a.eps = 1e-6f;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.T = T;
+  a.H = hd->d.hidden; a.L = hd->d.latent; a.E = hd->d.n_experts; a.K = hd->d.top_k; a.F = hd->d.ffn;
+  a.z = hd->z; a.logits = hd->logits; a.h = hd->h; a.hmax = hd->hmax; a.c = hd->c;
+  a.ybuf = hd->ybuf; a.xbuf = hd->xbuf;
+  a.idx = hd->idx; a.w = hd->w; a.counts = hd->counts; a.offsets = hd->offsets;
+  a.perm = hd->perm; a.pos = hd->pos;
+  a.bar = hd->bar; a.err = hd->err;
+  decode_plan(hd, decode_bucket(T), a);
+}
+
+// ------------------------------------------------------------------ small kernels
+__global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                            const float* __restrict__ globals, int n_codes, int n_scales,
+                            uint8_t* __restrict__ records, size_t stride) {
+  const int e = blockIdx.y;
+  uint8_t* rec = records + size_t(e) * stride;
+  const uint4* c4 = reinterpret_cast<const uint4*>(codes + size_t(e) * n_codes);
+  const uint4* s4 = reinterpret_cast<const uint4*>(scales + size_t(e) * n_scales);
+  const int nc4 = n_codes / 16, ns4 = n_scales / 16;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nc4 + ns4; i += gridDim.x * blockDim.x) {
+    if (i < nc4) reinterpret_cast<uint4*>(rec)[i] = c4[i];
+    else reinterpret_cast<uint4*>(rec + n_codes)[i - nc4] = s4[i - nc4];
+  }
+  if (blockIdx.x == 0 && threadIdx.x < 3) {
+    reinterpret_cast<float*>(rec + n_codes + n_scales)[threadIdx.x] = globals[size_t(e) * 3 + threadIdx.x];
+  }
+}
+
+// E4M3FN round-to-nearest-even of a non-negative double, saturating at 448.
+__device__ uint32_t e4m3_rne(double x) {
+  if (!(x > 0.0)) return 0u;
+  if (x >= 448.0) return 0x7Eu;
+  if (x < 0.015625) {                       // below 2^-6: subnormal grid m * 2^-9
+    return (uint32_t)rint(x * 512.0);       // m = 8 lands on 0x08 = 2^-6
+  }
+  int ex;
+  const double fr = frexp(x, &ex);          // x = fr * 2^ex, fr in [0.5, 1)
+  int e = ex - 1;
+  double mant = rint((2.0 * fr - 1.0) * 8.0);
+  if (mant == 8.0) { mant = 0.0; e += 1; }
+  uint32_t code = (uint32_t)((e + 7) << 3) + (uint32_t)mant;
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+__device__ double e4m3_value_d(uint32_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  return e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+}
+
+// Nearest E2M1 magnitude code (0..7) of |r|, ties to the even code.
+__device__ uint32_t e2m1_mag_rne(double a) {
+  if (a <= 0.25) return 0;
+  if (a < 0.75) return 1;
+  if (a <= 1.25) return 2;
+  if (a < 1.75) return 3;
+  if (a <= 2.5) return 4;
+  if (a < 3.5) return 5;
+  if (a <= 5.0) return 6;
+  return 7;
+}
+
+// One thread per 16-element block.
+__global__ void quantize_kernel(const float* __restrict__ w, int rows, int K, float g,
+                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const long nblk = long(rows) * (K / 16);
+  for (long bi = blockIdx.x * long(blockDim.x) + threadIdx.x; bi < nblk; bi += long(gridDim.x) * blockDim.x) {
+    const long r = bi / (K / 16), b = bi % (K / 16);
+    const float* src = w + r * K + b * 16;
+    double amax = 0.0;
+    for (int i = 0; i < 16; ++i) amax = fmax(amax, fabs((double)src[i]));
+    const double gd = (double)g;
+    const uint32_t sb = e4m3_rne(amax / (6.0 * gd));
+    const double denom = e4m3_value_d(sb) * gd;
+    uint8_t* cdst = codes + r * (K / 2) + b * 8;
+    for (int i = 0; i < 16; i += 2) {
+      uint32_t cc[2];
+      for (int j = 0; j < 2; ++j) {
+        const double rv = denom > 0.0 ? (double)src[i + j] / denom : 0.0;
+        const uint32_t m = e2m1_mag_rne(fabs(rv));
+        cc[j] = m | ((rv < 0.0 && m > 0) ? 8u : 0u);
+      }
+      cdst[i / 2] = (uint8_t)(cc[0] | (cc[1] << 4));
+    }
+    scales[r * (K / 16) + b] = (uint8_t)sb;
+  }
+}
+
+// out[t] = bf16(v / sqrt(mean(v^2) + eps)), v = x[t] + y[t]; one block per token.
+// Launched with the decode kernel's block size and summation order, so a stack run
+// as separate layer calls reproduces the fused stack bit for bit.
+__global__ void residual_rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* y,
+                                        __nv_bfloat16* out, int hidden, float eps) {
+  __shared__ float red[32];
+  const size_t base = size_t(blockIdx.x) * hidden;
+  float s = 0.f;
+  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
+    const float v = __bfloat162float(x[base + k]) + __bfloat162float(y[base + k]);
+    s = fmaf(v, v, s);
+  }
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+  const float inv = 1.0f / sqrtf(tot / float(hidden) + eps);
+  __syncthreads();
+  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
+    const float v = __bfloat162float(x[base + k]) + __bfloat162float(y[base + k]);
+    out[base + k] = __float2bfloat16_rn(v * inv);
+  }
+}
+
+edge0_status launch_status() { return cuda_status(cudaGetLastError()); }
+
+}  // namespace
+
+extern "C" {
+
+size_t edge0_expert_record_bytes(int latent, int ffn) {
+  if (!shapes_ok(latent, ffn)) return 0;
+  return size_t(3) * latent * ffn / 2 + size_t(3) * latent * ffn / 16 + 12;
+}
+
+size_t edge0_expert_record_stride(int latent, int ffn) {
+  const size_t b = edge0_expert_record_bytes(latent, ffn);
+  return b ? align_up(b, 256) : 0;
+}
+
+edge0_status edge0_pack_expert_host(const uint8_t* codes, const uint8_t* scales, const float* globals,
+                                    int latent, int ffn, void* record_out) {
+  if (!codes || !scales || !globals || !record_out || !shapes_ok(latent, ffn)) return EDGE0_ERR_INVALID_ARG;
+  const size_t nc = size_t(3) * latent * ffn / 2, ns = size_t(3) * latent * ffn / 16;
+  uint8_t* r = static_cast<uint8_t*>(record_out);
+  memcpy(r, codes, nc);
+  memcpy(r + nc, scales, ns);
+  memcpy(r + nc + ns, globals, 12);
+  return EDGE0_OK;
+}
+
+edge0_status edge0_pack_experts(const uint8_t* codes, const uint8_t* scales, const float* globals,
+                                int n_experts, int latent, int ffn, void* records, size_t stride,
+                                edge0_stream_t stream) {
+  if (!codes || !scales || !globals || !records || n_experts < 0 || !shapes_ok(latent, ffn))
+    return EDGE0_ERR_INVALID_ARG;
+  if (stride < edge0_expert_record_bytes(latent, ffn) || stride % 16 || !aligned(records, 256) ||
+      !aligned(codes, 16) || !aligned(scales, 16) || !aligned(globals, 4))
+    return EDGE0_ERR_INVALID_ARG;
+  if (n_experts == 0) return EDGE0_OK;
+  const int nc = 3 * latent * ffn / 2, ns = 3 * latent * ffn / 16;
+  if (n_experts > 65535) return EDGE0_ERR_UNSUPPORTED;
+  pack_kernel<<<dim3(64, n_experts), 256, 0, (cudaStream_t)stream>>>(
+      codes, scales, globals, nc, ns, static_cast<uint8_t*>(records), stride);
+  return launch_status();
+}
+
+edge0_status edge0_quantize_nvfp4(const float* w, int rows, int K, float g, uint8_t* codes,
+                                  uint8_t* scales, edge0_stream_t stream) {
+  if (!w || !codes || !scales || rows < 0 || K <= 0 || K % 16 || !(g > 0.f) || !isfinite(g))
+    return EDGE0_ERR_INVALID_ARG;
+  if (rows == 0) return EDGE0_OK;
+  const long nblk = long(rows) * (K / 16);
+  const int blocks = (int)((nblk + 255) / 256 < 4096 ? (nblk + 255) / 256 : 4096);
+  quantize_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(w, rows, K, g, codes, scales);
+  return launch_status();
+}
+
+edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
+  if (!handle_out) return EDGE0_ERR_INVALID_ARG;
+  *handle_out = nullptr;
+  if (!desc) return EDGE0_ERR_INVALID_ARG;
+  const edge0_moe_desc& d = *desc;
+  if (d.hidden <= 0 || d.hidden % 64 || !shapes_ok(d.latent, d.ffn) || d.top_k < 1 ||
+      d.top_k > kMaxTopK || d.n_experts < d.top_k || d.n_experts > 1024 || d.n_experts % 32 ||
+      d.max_tokens < 0)
+    return EDGE0_ERR_INVALID_ARG;
+  if (!d.D || !d.U || !d.router || !d.experts || !d.shared_expert) return EDGE0_ERR_INVALID_ARG;
+  if (!aligned(d.D, 16) || !aligned(d.U, 16) || !aligned(d.router, 16) ||
+      !aligned(d.experts, 256) || !aligned(d.shared_expert, 256) ||
+      (d.router_bias && !aligned(d.router_bias, 4)))
+    return EDGE0_ERR_INVALID_ARG;
+  if (d.expert_stride < edge0_expert_record_bytes(d.latent, d.ffn) || d.expert_stride % 256)
+    return EDGE0_ERR_INVALID_ARG;
+
+  Handle* hd = new Handle();
+  hd->d = d;
+  cudaError_t ce = cudaGetDevice(&hd->device);
+  cudaDeviceProp prop;
+  if (ce == cudaSuccess) ce = cudaGetDeviceProperties(&prop, hd->device);
+  if (ce != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
+  if (prop.major < 10 || !prop.cooperativeLaunch) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
+  hd->num_sms = prop.multiProcessorCount;
+  hd->smem_total = (int)prop.sharedMemPerBlockOptin - 1024;
+  // every decode bucket must leave room for at least one staged row and one P3 group
+  for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
+    DecodeArgs a;
+    decode_plan(hd, TB, a);
+    const int need = 2 * (d.hidden > d.latent ? d.hidden : d.latent) + 4096;
+    if (a.slab_bytes < need) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
+  }
+  if ((ce = decode_prepare(hd->smem_total)) != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
+  int occ = 0;
+  if ((ce = decode_occupancy(hd->smem_total, &occ)) != cudaSuccess || occ < 1) {
+    delete hd;
+    return ce != cudaSuccess ? EDGE0_ERR_CUDA : EDGE0_ERR_UNSUPPORTED;
+  }
+
+  // workspace
+  const int H = d.hidden, L = d.latent, E = d.n_experts, K = d.top_k, F = d.ffn;
+  const int TD = kDecodeMaxT;
+  hd->dec_max_t = TD;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  const size_t o_z = take(size_t(TD) * L * 4), o_lg = take(size_t(TD) * E * 4);
+  const size_t o_h = take(size_t(TD * K + TD) * F * 4), o_hm = take(size_t(TD * K + TD) * 4);
+  const size_t o_c = take(size_t(TD) * L * 4);
+  const size_t o_y = take(size_t(2) * TD * H * 2), o_x = take(size_t(2) * TD * H * 2);
+  const int TKmax = (d.max_tokens > TD ? d.max_tokens : TD) * K;
+  const size_t o_idx = take(size_t(TKmax) * 4), o_w = take(size_t(TKmax) * 4);
+  const size_t o_cnt = take(size_t(E) * 4), o_off = take(size_t(E + 1) * 4);
+  const size_t o_perm = take(size_t(TKmax) * 4), o_pos = take(size_t(TKmax) * 4);
+  const size_t o_bar = take(sizeof(GridBarrier)), o_err = take(sizeof(int));
+  const size_t o_lw = take(sizeof(LayerW)), o_st = take(sizeof(LayerW) * kStackMax);
+  const size_t o_pf = take(prefill_workspace_bytes(d, d.max_tokens));
+  hd->ws_bytes = off;
+  if (cudaMalloc(&hd->ws, hd->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete hd;
+    return EDGE0_ERR_OOM;
+  }
+  char* b = hd->ws;
+  hd->z = (float*)(b + o_z); hd->logits = (float*)(b + o_lg); hd->h = (float*)(b + o_h);
+  hd->hmax = (unsigned*)(b + o_hm); hd->c = (float*)(b + o_c);
+  hd->ybuf = (__nv_bfloat16*)(b + o_y); hd->xbuf = (__nv_bfloat16*)(b + o_x);
+  hd->idx = (int*)(b + o_idx); hd->w = (float*)(b + o_w); hd->counts = (int*)(b + o_cnt);
+  hd->offsets = (int*)(b + o_off); hd->perm = (int*)(b + o_perm); hd->pos = (int*)(b + o_pos);
+  hd->bar = (GridBarrier*)(b + o_bar); hd->err = (int*)(b + o_err);
+  hd->d_layer = (LayerW*)(b + o_lw); hd->d_stack = (LayerW*)(b + o_st);
+  prefill_workspace_carve(d, d.max_tokens, b + o_pf, &hd->pf);
+  hd->pf.idx = hd->idx; hd->pf.w = hd->w; hd->pf.counts = hd->counts; hd->pf.offsets = hd->offsets;
+  hd->pf.perm = hd->perm; hd->pf.pos = hd->pos;
+  hd->pf.err = hd->err;
+  const LayerW lw = layer_of(hd);
+  ce = cudaMemset(hd->ws, 0, o_lw);
+  if (ce == cudaSuccess) ce = cudaMemcpy(hd->d_layer, &lw, sizeof(lw), cudaMemcpyHostToDevice);
+  if (ce == cudaSuccess) ce = prefill_init(d, &hd->pf, hd->num_sms);
+  if (ce != cudaSuccess) {
+    cudaFree(hd->ws);
+    delete hd;
+    return EDGE0_ERR_CUDA;
+  }
+  *handle_out = hd;
+  return EDGE0_OK;
+}
+
+edge0_status edge0_moe_forward(void* handle, const void* x, void* y, int T, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || T < 0) return EDGE0_ERR_INVALID_ARG;
+  if (T == 0) return EDGE0_OK;
+  if (!x || !y || !aligned(x, 16) || !aligned(y, 16) || T > (hd->d.max_tokens > kDecodeMaxT ? hd->d.max_tokens : kDecodeMaxT))
+    return EDGE0_ERR_INVALID_ARG;
+  if (T > hd->d.max_tokens && T > kDecodeMaxT) return EDGE0_ERR_INVALID_ARG;
+  const size_t xy = size_t(T) * hd->d.hidden * 2;
+  const char* xc = static_cast<const char*>(x);
+  const char* yc = static_cast<const char*>(y);
+  if (xc < yc + xy && yc < xc + xy) return EDGE0_ERR_INVALID_ARG;
+  if (T <= kDecodeMaxT) {
+    DecodeArgs a;
+    fill_decode_args(hd, a, x, y, T);
+    const cudaError_t e = decode_launch(a, hd->num_sms, hd->smem_total, (cudaStream_t)stream);
+    if (e != cudaSuccess) return EDGE0_ERR_CUDA;
+    hd->last_T = T;
+    hd->last_path = 1;
+    return EDGE0_OK;
+  }
+  if (T > hd->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
+  const edge0_status st = prefill_forward(hd->d, &hd->pf, hd->num_sms,
+                                          static_cast<const __nv_bfloat16*>(x),
+                                          static_cast<__nv_bfloat16*>(y), T, (cudaStream_t)stream);
+  if (st == EDGE0_OK) { hd->last_T = T; hd->last_path = 2; }
+  return st;
+}
+
+edge0_status edge0_moe_debug_routing(void* handle, int* idx, float* w, int* counts, int* offsets,
+                                     int* perm, int* pos, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->last_path) return EDGE0_ERR_UNSUPPORTED;
+  const size_t tk = size_t(hd->last_T) * hd->d.top_k;
+  const int E = hd->d.n_experts;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  if (idx && e == cudaSuccess) e = cudaMemcpyAsync(idx, hd->idx, tk * 4, cudaMemcpyDeviceToDevice, s);
+  if (w && e == cudaSuccess) e = cudaMemcpyAsync(w, hd->w, tk * 4, cudaMemcpyDeviceToDevice, s);
+  if (counts && e == cudaSuccess) e = cudaMemcpyAsync(counts, hd->counts, size_t(E) * 4, cudaMemcpyDeviceToDevice, s);
+  if (offsets && e == cudaSuccess) e = cudaMemcpyAsync(offsets, hd->offsets, size_t(E + 1) * 4, cudaMemcpyDeviceToDevice, s);
+  if (perm && e == cudaSuccess) e = cudaMemcpyAsync(perm, hd->perm, tk * 4, cudaMemcpyDeviceToDevice, s);
+  if (pos && e == cudaSuccess) e = cudaMemcpyAsync(pos, hd->pos, tk * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+edge0_status edge0_moe_debug_tensor(void* handle, int what, void* dst, size_t bytes, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !dst) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->last_path) return EDGE0_ERR_UNSUPPORTED;
+  const size_t T = hd->last_T;
+  const void* src = nullptr;
+  size_t n = 0;
+  if (hd->last_path == 1) {
+    if (what == 0) { src = hd->z; n = T * hd->d.latent * 4; }
+    else if (what == 1) { src = hd->logits; n = T * hd->d.n_experts * 4; }
+    else if (what == 2) { src = hd->c; n = T * hd->d.latent * 4; }
+  } else {
+    src = prefill_debug_tensor(&hd->pf, what, hd->d, (int)T, &n);
+  }
+  if (!src) return what >= 0 && what <= 2 ? EDGE0_ERR_UNSUPPORTED : EDGE0_ERR_INVALID_ARG;
+  if (bytes < n) return EDGE0_ERR_INVALID_ARG;
+  return cuda_status(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+}
+
+edge0_status edge0_residual_rmsnorm(const void* x, const void* y, void* out, int T, int hidden, float eps,
+                                    edge0_stream_t stream) {
+  if (T < 0 || hidden <= 0 || hidden % 8 || !(eps >= 0.f)) return EDGE0_ERR_INVALID_ARG;
+  if (T == 0) return EDGE0_OK;
+  if (!x || !y || !out) return EDGE0_ERR_INVALID_ARG;
+  residual_rmsnorm_kernel<<<T, kDecThreads, 0, (cudaStream_t)stream>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(y),
+      static_cast<__nv_bfloat16*>(out), hidden, eps);
+  return launch_status();
+}
+
+static edge0_status stack_impl(void* const* handles, int n_layers, const void* x, void* y, int T, float eps,
+                               void* trace_x, void* trace_y, edge0_stream_t stream) {
+  if (!handles || n_layers < 1 || T < 0 || !(eps >= 0.f)) return EDGE0_ERR_INVALID_ARG;
+  if (T == 0) return EDGE0_OK;
+  Handle* h0 = static_cast<Handle*>(handles[0]);
+  if (!h0 || !x || !y || !aligned(x, 16) || !aligned(y, 16)) return EDGE0_ERR_INVALID_ARG;
+  for (int i = 0; i < n_layers; ++i) {
+    const Handle* hi = static_cast<const Handle*>(handles[i]);
+    if (!hi || hi->d.hidden != h0->d.hidden || hi->d.latent != h0->d.latent ||
+        hi->d.n_experts != h0->d.n_experts || hi->d.top_k != h0->d.top_k || hi->d.ffn != h0->d.ffn ||
+        hi->device != h0->device)
+      return EDGE0_ERR_INVALID_ARG;
+  }
+  if (T > kDecodeMaxT || n_layers > kStackMax) {
+    if (trace_x || trace_y) return EDGE0_ERR_UNSUPPORTED;
+    // chain: layer forward into the prefill scratch of handle 0, then the residual norm
+    if (T > h0->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
+    __nv_bfloat16* tmp = prefill_stack_scratch(&h0->pf);
+    if (!tmp) return EDGE0_ERR_UNSUPPORTED;
+    const void* cur = x;
+    for (int i = 0; i < n_layers; ++i) {
+      edge0_status st = edge0_moe_forward(handles[i], cur, tmp, T, stream);
+      if (st != EDGE0_OK) return st;
+      st = edge0_residual_rmsnorm(cur, tmp, y, T, h0->d.hidden, eps, stream);
+      if (st != EDGE0_OK) return st;
+      cur = y;
+    }
+    return EDGE0_OK;
+  }
+  std::vector<LayerW> lws(n_layers);
+  for (int i = 0; i < n_layers; ++i) lws[i] = layer_of(static_cast<const Handle*>(handles[i]));
+  cudaStream_t s = (cudaStream_t)stream;
+  // pageable source: the copy is staged before the call returns
+  cudaError_t e = cudaMemcpyAsync(h0->d_stack, lws.data(), sizeof(LayerW) * n_layers, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return EDGE0_ERR_CUDA;
+  DecodeArgs a;
+  fill_decode_args(h0, a, x, y, T);
+  a.layers = h0->d_stack;
+  a.n_layers = n_layers;
+  a.eps = eps;
+  a.trace_x = static_cast<__nv_bfloat16*>(trace_x);
+  a.trace_y = static_cast<__nv_bfloat16*>(trace_y);
+  e = decode_launch(a, h0->num_sms, h0->smem_total, s);
+  if (e != cudaSuccess) return EDGE0_ERR_CUDA;
+  h0->last_T = T;
+  h0->last_path = 1;
+  return EDGE0_OK;
+}
+
+edge0_status edge0_moe_stack_forward(void* const* handles, int n_layers, const void* x, void* y, int T,
+                                     float eps, edge0_stream_t stream) {
+  return stack_impl(handles, n_layers, x, y, T, eps, nullptr, nullptr, stream);
+}
+
+edge0_status edge0_moe_stack_forward_trace(void* const* handles, int n_layers, const void* x, void* y,
+                                           int T, float eps, void* trace_x, void* trace_y,
+                                           edge0_stream_t stream) {
+  return stack_impl(handles, n_layers, x, y, T, eps, trace_x, trace_y, stream);
+}
+
+edge0_status edge0_moe_get_error(void* handle) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return EDGE0_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, hd->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EDGE0_ERR_CUDA;
+  if (err) {
+    // clear the word and reset the grid barrier an aborted launch may have left behind
+    if (cudaMemset(hd->err, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(hd->bar, 0, sizeof(GridBarrier)) != cudaSuccess)
+      return EDGE0_ERR_CUDA;
+    return EDGE0_ERR_TIMEOUT;
+  }
+  return EDGE0_OK;
+}
+
+const char* edge0_status_string(edge0_status s) {
+  switch (s) {
+    case EDGE0_OK: return "ok";
+    case EDGE0_ERR_INVALID_ARG: return "invalid argument";
+    case EDGE0_ERR_UNSUPPORTED: return "unsupported";
+    case EDGE0_ERR_CUDA: return "CUDA error";
+    case EDGE0_ERR_OOM: return "out of device memory";
+    case EDGE0_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+void edge0_moe_destroy(void* handle) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return;
+  cudaDeviceSynchronize();
+  prefill_destroy(&hd->pf);
+  cudaFree(hd->ws);
+  delete hd;
+}
+
+}  // extern "C"

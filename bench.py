@@ -1,0 +1,418 @@
+"""Benchmark of the latent-MoE layer hot path on B300 (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (D, router, top-k + softmax, permutation,
+routed and shared NVFP4 SwiGLU experts, combine, U) over one batch of seeded
+synthetic tokens.  Inputs are resident in HBM before timing; L2 (126 MB) is
+defeated by rotating over independent layer instances whose bytes exceed it.
+Time is taken with CUDA events on the launching stream (the steps are replayed
+from a captured CUDA graph, so host launch cost is not measured), max over
+ranks.  ``e2e`` repeats the measurement through the same C-ABI call with the
+step's input copied from pinned host memory and its output read back.
+``--impl reference`` times the CPU oracle (fp64 numpy) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: latent, T, seed, layers per step, zipf pattern, instances rotated
+    "layer145b_t1": dict(latent=1792, T=1, seed=0, layers=1, zipf=(0.0,), instances=16,
+                         desc="one Edge0-145B latent-MoE layer, decode T=1"),
+    "layer120b_t4": dict(latent=1280, T=4, seed=1, layers=1, zipf=(0.0,), instances=16,
+                         desc="one Edge0-120B latent-MoE layer, speculative-verify batch T=4"),
+    "stack48_145b_t1": dict(latent=1792, T=1, seed=2, layers=48, zipf=(0.0,), instances=1,
+                            desc="48 Edge0-145B layers (all 48x512 experts resident), decode T=1"),
+}
+DEFAULT_WORKLOAD = "layer145b_t1"
+HIDDEN, E, K, F = 2560, 512, 10, 640
+METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofline"
+
+
+def record_bytes(latent):
+    return 3 * F * latent // 2 + 3 * F * latent // 16 + 12
+
+
+def decode_algorithmic_bytes(latent, T, distinct_experts):
+    """HBM bytes one decode forward must move: D, U, router, every distinct
+    routed record once, the shared record, x and y."""
+    dense = 2 * latent * HIDDEN * 2 + E * latent * 2
+    return dense + (distinct_experts + 1) * record_bytes(latent) + 2 * T * HIDDEN * 2
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (clocks and throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ dist helpers
+def dist_setup(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), d.get("bf16_tflops_sustained", 1400.0), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def cpu_baseline(wl, seconds=12.0):
+    """The oracle as it stands, on host cores, for a bounded sample of the workload."""
+    import numpy as np
+    import synth
+    from oracle import moe
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    spec = synth.LayerSpec(seed=wl["seed"], layer=0, latent=wl["latent"], zipf=wl["zipf"][0])
+    inp = synth.make_layer(spec)
+    lay = moe.Layer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn, spec.top_k)
+    T = wl["T"]
+    done_tokens, t0, it = 0, time.perf_counter(), 0
+    while True:
+        inp._cache.clear()                       # each sample dequantises its experts again
+        x = synth.tokens_bf16(1000 + it, T, HIDDEN)
+        moe.layer_forward(lay, x)
+        done_tokens += T * wl["layers"] and T
+        it += 1
+        el = time.perf_counter() - t0
+        if el > seconds or it >= 64:
+            break
+    # per-layer tokens: each sample runs one layer; a stack step runs `layers` of them
+    tok_per_s = done_tokens / el / wl["layers"]
+    return {"value": tok_per_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{it} forward(s) of one layer at T={T} (fresh expert dequantisation each), "
+                      f"{el:.1f} s; stack workloads scaled by 1/{wl['layers']} layers"}
+
+
+# ------------------------------------------------------------------ our implementation
+def build_instances(wl, n_inst, max_tokens):
+    import torch
+    import synth
+    from synth import device
+    insts = []
+    for i in range(n_inst):
+        spec = synth.LayerSpec(seed=wl["seed"], layer=i, latent=wl["latent"],
+                               zipf=wl["zipf"][i % len(wl["zipf"])])
+        insts.append(device.DeviceLayer(synth.make_layer(spec), max_tokens=max_tokens))
+    torch.cuda.synchronize()
+    return insts
+
+
+def run_ours(args, wl, rank, world, local):
+    import numpy as np
+    import torch
+    import synth
+    import latent_sparse_moe_router_b300 as ext
+    from synth import device
+
+    torch.cuda.set_device(local)
+    T, L, n_layers = wl["T"], wl["latent"], wl["layers"]
+    hbm, bf16, bf16_s, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    if n_layers == 1:
+        insts = build_instances(wl, wl["instances"], max_tokens=16)
+        n_inst = len(insts)
+        xs = [device.bf16_tensor(synth.tokens_bf16(wl["seed"] * 1000 + rank * 100 + i, T, HIDDEN))
+              for i in range(n_inst)]
+        ys = [torch.empty_like(x) for x in xs]
+
+        def step(i, s):
+            j = i % n_inst
+            ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, s)
+        launches_per_step = 1
+        # distinct experts per instance (for the algorithmic bytes)
+        distinct = []
+        with torch.cuda.stream(stream):
+            for j in range(n_inst):
+                step(j, stream)
+        stream.synchronize()
+        for j in range(n_inst):
+            ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, stream)
+            stream.synchronize()
+            distinct.append(len(np.unique(insts[j].routing(T)["idx"])))
+        bytes_per_step = float(np.mean([decode_algorithmic_bytes(L, T, d) for d in distinct]))
+        work_note = f"mean distinct routed experts {np.mean(distinct):.2f}"
+    else:
+        # the 48-layer stack: all 48 x 512 records resident in one allocation
+        stride = ext.edge0_expert_record_stride(L, F)
+        big = torch.empty(n_layers * E * stride, dtype=torch.uint8, device="cuda")
+        insts = []
+        for l in range(n_layers):
+            spec = synth.LayerSpec(seed=wl["seed"], layer=l, latent=L)
+            rec = big[l * E * stride:(l + 1) * E * stride]
+            insts.append(device.DeviceLayer(synth.make_layer(spec), max_tokens=16, records=rec))
+        torch.cuda.synchronize()
+        handles = [d.handle for d in insts]
+        n_tok = 256
+        xs_all = device.bf16_tensor(synth.tokens_bf16(wl["seed"], n_tok, HIDDEN))
+        ys_all = torch.empty_like(xs_all)
+
+        def step(i, s):
+            j = i % n_tok
+            ext.edge0_moe_stack_forward(handles, xs_all[j:j + 1], ys_all[j:j + 1], 1, 1e-6, s)
+        launches_per_step = 1
+        bytes_per_step = None      # computed below from the routing of the last layer run
+        distinct_total = []
+        for j in range(4):
+            for l, d in enumerate(insts):
+                pass
+        bytes_per_step = n_layers * decode_algorithmic_bytes(L, 1, K)
+        work_note = "48 layers x (D + U + router + 10 routed + 1 shared record) per token"
+
+    # warm-up, then capture the timed steps in a CUDA graph
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(args.warmup + i, stream)
+        stream.synchronize()
+        graph.replay()                      # one untimed replay (the graph's first launch)
+        stream.synchronize()
+    except Exception as e:                  # graph capture unavailable: launch directly
+        print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
+        graph = None
+        torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        reps = max(1, int(args.repeat))
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for r in range(reps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    for i in range(args.steps):
+                        step(args.warmup + i, stream)
+            ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    steps_done = args.steps * reps
+    ms_per_step = el_ms / steps_done
+    tokens_per_step = T * world
+    value = tokens_per_step / (ms_per_step / 1e3) / (1 if n_layers == 1 else 1)
+    # roofline of the dominant (only) kernel: algorithmic bytes / launch duration
+    achieved_gbs = bytes_per_step / (ms_per_step / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm, 4), "traffic": None,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "bytes_per_launch": bytes_per_step, "note": work_note}
+
+    # e2e through the C ABI with pinned host buffers: H2D x, forward, D2H y, per step
+    e2e = None
+    if n_layers == 1:
+        hx = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
+        hy = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
+        for j in range(len(insts)):
+            hx[j].copy_(xs[j].cpu())
+        n_e2e = max(args.steps, 32)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(n_e2e):
+                j = i % len(insts)
+                xs[j].copy_(hx[j], non_blocking=True)
+                ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, stream)
+                hy[j].copy_(ys[j], non_blocking=True)
+                stream.synchronize()             # the host reads the step's result
+            e1.record(stream)
+        stream.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+        e2e = {"value": round(T * world / (e_ms / 1e3), 1), "unit": "tok/s",
+               "h2d_bytes_per_step": T * HIDDEN * 2, "d2h_bytes_per_step": T * HIDDEN * 2}
+    else:
+        hx = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+        hy = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(xs_all[:1].cpu())
+        xd = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device="cuda")
+        yd = torch.empty_like(xd)
+        n_e2e = 16
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(n_e2e):
+                xd.copy_(hx, non_blocking=True)
+                ext.edge0_moe_stack_forward(handles, xd, yd, 1, 1e-6, stream)
+                hy.copy_(yd, non_blocking=True)
+                stream.synchronize()
+            e1.record(stream)
+        stream.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+        e2e = {"value": round(world / (e_ms / 1e3), 2), "unit": "tok/s",
+               "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 2}
+
+    for d in insts:
+        d.close()
+    return dict(value=value, ms_per_step=ms_per_step, roofline=roof, e2e=e2e,
+                gpu_launches=launches_per_step * steps_done, clocks=clk.summary(), reps=reps)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--repeat", type=int, default=20, help="graph replays inside the timed region")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--instances", type=int, default=0,
+                    help="override the number of rotated layer instances (profiling runs)")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    wl = dict(WORKLOADS[args.workload])
+    if args.instances:
+        wl["instances"] = args.instances
+    rank, world, local = dist_setup(args.gpus)
+
+    config = {"workload": args.workload, "desc": wl["desc"], "hidden": HIDDEN, "latent": wl["latent"],
+              "experts": E, "top_k": K, "ffn": F, "T": wl["T"], "layers_per_step": wl["layers"],
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+              "l2": (f"rotating {wl['instances']} independent layer instances "
+                     f"(~{wl['instances'] * decode_algorithmic_bytes(wl['latent'], wl['T'], K * wl['T']) / 1e6:.0f} MB touched) > 126 MB L2"
+                     if wl["layers"] == 1 else "48-layer stack, 47.6 GB of records > 126 MB L2")}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t_steps = []
+        sample = None
+        for s in range(args.warmup + args.steps):
+            cb = cpu_baseline(wl, seconds=max(2.0, 60.0 / (args.steps + args.warmup)))
+            if s >= args.warmup:
+                t_steps.append(cb["value"])
+            sample = cb
+        v = statistics.median(t_steps)
+        line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tok/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wl["T"] / v, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "config": config,
+                "cpu_baseline": {"value": round(v, 3), "unit": "tok/s", "cores": sample["cores"],
+                                 "kind": "oracle", "sample": sample["sample"]},
+                "e2e": {"value": round(v, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, wl, rank, world, local)
+    if rank != 0:
+        return
+    cb = None if args.no_cpu_baseline else cpu_baseline(wl)
+    line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps * r["reps"], "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights, bf16/f16 activations, fp32 accumulate",
+            "data": "synthetic (seeded; random NVFP4 experts and N(0,1/fan_in) bf16 projections)",
+            "config": config, "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -58,14 +58,19 @@ typedef enum {
  * Format (NVFP4 = E2M1 elements, one E4M3 scale per 16 consecutive weights
  * along the input dimension K, one fp32 scale g per matrix):
  *     w[r][k] = e2m1(code[r][k]) * e4m3(scale[r][k/16]) * g
- * For latent L (a multiple of 256) and SwiGLU width F (a multiple of 64) a record holds, in
- * order and without gaps:
- *     gate codes  [F][L/2]   up codes  [F][L/2]   down codes  [L][F/2]
- *     gate scales [F][L/16]  up scales [F][L/16]  down scales [L][F/16]
- *     fp32 g: gate, up, down (little-endian)
+ * For latent L (a multiple of 256) and SwiGLU width F (a multiple of 128) a
+ * record holds, without gaps:
+ *   GU block, F rows of 9L/8 bytes; row f =
+ *       gate codes row f (L/2) | up codes row f (L/2) |
+ *       gate scales row f (L/16) | up scales row f (L/16)
+ *   D block, L/2 row pairs of 9F/8 bytes; pair p =
+ *       down codes rows 2p, 2p+1 (F/2 each) | down scales rows 2p, 2p+1 (F/16 each)
+ *   fp32 g: gate, up, down (little-endian)
  * W_gate, W_up are [F x L] (K = L); W_down is [L x F] (K = F).  Two codes per
  * byte, the even element in the low nibble.  E4M3 is OCP E4M3FN (bias 7,
  * subnormals m * 2^-9, no infinities; the NaN bytes 0x7F/0xFF must not occur).
+ * Interleaving makes any run of gate/up rows, or of down row pairs, one
+ * contiguous byte range, and every run starts on a 16-byte boundary.
  * For L=1792, F=640 the codes and scales take 1,935,360 bytes, the size that
  * 48 layers x 512 experts of the 47.6 GB NVFP4 experts.bin imply ("Edge0-145B
  * Review", table in section "Warum 29 GB nicht wirklich in 29 GB passen").
@@ -79,6 +84,7 @@ size_t edge0_expert_record_stride(int latent, int ffn);
 
 /*
  * Pack one expert from its per-matrix arrays into a record (host memory).
+ * The per-matrix ("logical") arrays are row-major per matrix, concatenated:
  *   codes   host, 3*F*L/2 bytes: gate [F][L/2], up [F][L/2], down [L][F/2]
  *   scales  host, 3*F*L/16 bytes: gate [F][L/16], up [F][L/16], down [L][F/16]
  *   globals host, 3 floats: gate, up, down
@@ -122,7 +128,7 @@ typedef struct {
   int latent;     /* l: 1792 (145B) or 1280 (120B); multiple of 256 */
   int n_experts;  /* 512 routed experts */
   int top_k;      /* 10 */
-  int ffn;        /* SwiGLU width 640; multiple of 64 */
+  int ffn;        /* SwiGLU width 640; multiple of 128 */
   int max_tokens; /* largest T forward will accept (workspace sizing) */
   const void *D;            /* device bf16 [latent][hidden] */
   const void *U;            /* device bf16 [hidden][latent] */
@@ -137,7 +143,7 @@ typedef struct {
  * Create a layer handle.  Validates shapes and alignment, records the
  * borrowed pointers (which must stay valid for the handle's lifetime) and
  * allocates the workspace for max_tokens (the handle owns only that).
- * Supported shapes: hidden % 64 == 0, latent % 256 == 0, ffn % 64 == 0,
+ * Supported shapes: hidden % 64 == 0, latent % 256 == 0, ffn % 128 == 0,
  * 1 <= top_k <= 16, top_k <= n_experts <= 1024, n_experts % 32 == 0.  Launches no kernel.
  * Returns INVALID_ARG, UNSUPPORTED, CUDA or OOM on failure (*handle_out = NULL).
  */

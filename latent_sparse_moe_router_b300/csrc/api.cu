@@ -32,12 +32,15 @@ struct Handle {
   int dec_max_t = 0;          // decode workspace tokens
   char* ws = nullptr;         // one allocation for the whole workspace
   size_t ws_bytes = 0;
-  float* z = nullptr; float* logits = nullptr; float* h = nullptr; unsigned* hmax = nullptr;
+  float* z = nullptr; float* logits = nullptr; float* h = nullptr;
   float* c = nullptr;
   __nv_bfloat16* ybuf = nullptr; __nv_bfloat16* xbuf = nullptr;
   int* idx = nullptr; float* w = nullptr; int* counts = nullptr; int* offsets = nullptr;
   int* perm = nullptr; int* pos = nullptr;
   GridBarrier* bar = nullptr; int* err = nullptr;
+  float* rd = nullptr;        // R D, fp32 [n_experts][hidden]
+  float dnorm = 0.f;          // max_r sum_h |D[r][h]|
+  __half* zh = nullptr;       // f16 copy of z for the decode experts
   LayerW* d_layer = nullptr;  // this layer (1 entry)
   LayerW* d_stack = nullptr;  // kStackMax entries for stack calls
   PrefillWorkspace pf;        // prefill path buffers (T > 16)
@@ -50,28 +53,51 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool shapes_ok(int latent, int ffn) {
-  return latent > 0 && ffn > 0 && latent % 256 == 0 && ffn % 64 == 0;
+  return latent > 0 && ffn > 0 && latent % 256 == 0 && ffn % 128 == 0;
+}
+
+// Source byte offset, in the per-matrix arrays, of the 16-byte chunk at byte `o`
+// of a record body (see the record layout in edge0_moe.h).  Sets *from_scales.
+__host__ __device__ inline size_t record_src(size_t o, size_t L, size_t F, bool* from_scales) {
+  const size_t gu_row = 9 * L / 8, d_pair = 9 * F / 8;
+  if (o < F * gu_row) {
+    const size_t f = o / gu_row, w = o % gu_row;
+    if (w < L / 2) { *from_scales = false; return f * (L / 2) + w; }
+    if (w < L) { *from_scales = false; return F * (L / 2) + f * (L / 2) + (w - L / 2); }
+    if (w < L + L / 16) { *from_scales = true; return f * (L / 16) + (w - L); }
+    *from_scales = true;
+    return F * (L / 16) + f * (L / 16) + (w - L - L / 16);
+  }
+  const size_t od = o - F * gu_row, pr = od / d_pair, w = od % d_pair;
+  if (w < F) { *from_scales = false; return F * L + pr * F + w; }
+  *from_scales = true;
+  return 2 * F * (L / 16) + pr * (F / 8) + (w - F);
 }
 
 // Shared-memory plan of the decode kernel for token bucket TB.
 void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
-  const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts;
+  const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts, F = hd->d.ffn;
   size_t off = decode_tables_bytes();
-  size_t act = TB * (size_t)H * 2;
-  if (TB * (size_t)L * 4 > act) act = TB * (size_t)L * 4;
-  if (TB * (size_t)E * 4 > act) act = TB * (size_t)E * 4;
-  act = align_up(act, 128);
-  const size_t zh = align_up(TB * (size_t)L * 2, 128);
-  int res_rows = 2048 / TB;
-  if (res_rows > 256) res_rows = 256;
-  const size_t res = align_up(2 * (size_t)res_rows * TB * 4, 128);
+  // x (P0 only) and the fp32 activations (P1, P3) are never live together
+  size_t act = TB * (size_t)(L > E ? L : E) * 4;
+  if (TB * (size_t)H * 2 > act) act = TB * (size_t)H * 2;
+  const size_t cand = TB * (size_t)((E + 31) / 32) * 16 * 8 * 3 / 2 + 16 * 8;   // top-k lists
+  if (cand > act) act = cand;
+  a.off_xs = (int)off;
   a.off_act = (int)off;
-  a.act_bytes = (int)act;
-  a.off_zh = (int)(off + act);
-  a.off_slab = (int)(off + act + zh);
-  a.slab_bytes = (int)(hd->smem_total - (off + act + zh + res)) & ~127;
-  a.off_res = a.off_slab + a.slab_bytes;
-  a.res_rows = res_rows;
+  a.act_bytes = (int)align_up(act, 128);
+  off += a.act_bytes;
+  a.off_zh = (int)off;
+  off += align_up(TB * (size_t)L * 2, 128);
+  const int shared_rows = (F + hd->num_sms - 1) / hd->num_sms;
+  a.off_sh = (int)off;
+  a.sh_bytes = (int)align_up((size_t)shared_rows * 2 * (L / 2 + L / 16), 128);
+  off += a.sh_bytes;
+  a.off_res = (int)off;
+  a.res_rows = 0;
+  off = align_up(off, 1024);
+  a.off_dyn = (int)off;
+  a.dyn_bytes = (int)((hd->smem_total - off) & ~size_t(1023));
 }
 
 edge0_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA; }
@@ -80,16 +106,18 @@ LayerW layer_of(const Handle* hd) {
   LayerW l;
   l.D = static_cast<const __nv_bfloat16*>(hd->d.D);
   l.U = static_cast<const __nv_bfloat16*>(hd->d.U);
-  l.R = static_cast<const __nv_bfloat16*>(hd->d.router);
+  l.RD = hd->rd;
   l.bias = hd->d.router_bias;
   l.experts = static_cast<const uint8_t*>(hd->d.experts);
   l.shared = static_cast<const uint8_t*>(hd->d.shared_expert);
   l.stride = hd->d.expert_stride;
+  l.dnorm = hd->dnorm;
   return l;
 }
 
 void fill_decode_args(const Handle* hd, DecodeArgs& a, const void* x, void* y, int T) {
   memset(&a, 0, sizeof(a));
+  a.l0 = layer_of(hd);
   a.layers = hd->d_layer;
   a.n_layers = 1;
   a.eps = 1e-6f;
@@ -97,7 +125,7 @@ void fill_decode_args(const Handle* hd, DecodeArgs& a, const void* x, void* y, i
   a.y = static_cast<__nv_bfloat16*>(y);
   a.T = T;
   a.H = hd->d.hidden; a.L = hd->d.latent; a.E = hd->d.n_experts; a.K = hd->d.top_k; a.F = hd->d.ffn;
-  a.z = hd->z; a.logits = hd->logits; a.h = hd->h; a.hmax = hd->hmax; a.c = hd->c;
+  a.z = hd->z; a.zh = hd->zh; a.logits = hd->logits; a.h = hd->h; a.c = hd->c;
   a.ybuf = hd->ybuf; a.xbuf = hd->xbuf;
   a.idx = hd->idx; a.w = hd->w; a.counts = hd->counts; a.offsets = hd->offsets;
   a.perm = hd->perm; a.pos = hd->pos;
@@ -107,19 +135,69 @@ void fill_decode_args(const Handle* hd, DecodeArgs& a, const void* x, void* y, i
 
 // ------------------------------------------------------------------ small kernels
 __global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                            const float* __restrict__ globals, int n_codes, int n_scales,
+                            const float* __restrict__ globals, int L, int F, int n_codes, int n_scales,
                             uint8_t* __restrict__ records, size_t stride) {
   const int e = blockIdx.y;
   uint8_t* rec = records + size_t(e) * stride;
-  const uint4* c4 = reinterpret_cast<const uint4*>(codes + size_t(e) * n_codes);
-  const uint4* s4 = reinterpret_cast<const uint4*>(scales + size_t(e) * n_scales);
-  const int nc4 = n_codes / 16, ns4 = n_scales / 16;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nc4 + ns4; i += gridDim.x * blockDim.x) {
-    if (i < nc4) reinterpret_cast<uint4*>(rec)[i] = c4[i];
-    else reinterpret_cast<uint4*>(rec + n_codes)[i - nc4] = s4[i - nc4];
+  const uint8_t* ce = codes + size_t(e) * n_codes;
+  const uint8_t* se = scales + size_t(e) * n_scales;
+  const int nchunk = (n_codes + n_scales) / 16;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunk; i += gridDim.x * blockDim.x) {
+    bool sc = false;
+    const size_t src = record_src(size_t(i) * 16, L, F, &sc);
+    reinterpret_cast<uint4*>(rec)[i] = *reinterpret_cast<const uint4*>((sc ? se : ce) + src);
   }
   if (blockIdx.x == 0 && threadIdx.x < 3) {
     reinterpret_cast<float*>(rec + n_codes + n_scales)[threadIdx.x] = globals[size_t(e) * 3 + threadIdx.x];
+  }
+}
+
+// RD[e][h] = sum_l R[e][l] * D[l][h] in fp32 (the router folded with the
+// down-projection, so decode computes the logits from x directly).  32x32 output
+// tiles, K staged through shared memory in fixed order.
+__global__ void fold_router_kernel(const __nv_bfloat16* __restrict__ R, const __nv_bfloat16* __restrict__ D,
+                                   float* __restrict__ RD, int E, int L, int H) {
+  __shared__ float rs[32][33];
+  __shared__ float ds[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+  const int e0 = blockIdx.y * 32, h0 = blockIdx.x * 32;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int l0 = 0; l0 < L; l0 += 32) {
+    for (int i = ty; i < 32; i += 8) {
+      rs[i][tx] = (e0 + i < E) ? __bfloat162float(R[size_t(e0 + i) * L + l0 + tx]) : 0.f;
+      ds[i][tx] = (h0 + tx < H) ? __bfloat162float(D[size_t(l0 + i) * H + h0 + tx]) : 0.f;
+    }
+    __syncthreads();
+    for (int k = 0; k < 32; ++k) {
+      const float dv = ds[k][tx];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = fmaf(rs[ty + 8 * j][k], dv, acc[j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = e0 + ty + 8 * j;
+    if (e < E && h0 + tx < H) RD[size_t(e) * H + h0 + tx] = acc[j];
+  }
+}
+
+// out = max_r sum_h |D[r][h]| (one block; fixed reduction order)
+__global__ void row_l1_max_kernel(const __nv_bfloat16* __restrict__ D, int rows, int cols, float* out) {
+  __shared__ float red[32];
+  float m = 0.f;
+  for (int r = threadIdx.x >> 5; r < rows; r += blockDim.x >> 5) {
+    float s = 0.f;
+    for (int c = threadIdx.x & 31; c < cols; c += 32) s += fabsf(__bfloat162float(D[size_t(r) * cols + c]));
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    m = fmaxf(m, s);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mm = fmaxf(mm, red[i]);
+    *out = mm;
   }
 }
 
@@ -228,8 +306,11 @@ edge0_status edge0_pack_expert_host(const uint8_t* codes, const uint8_t* scales,
   if (!codes || !scales || !globals || !record_out || !shapes_ok(latent, ffn)) return EDGE0_ERR_INVALID_ARG;
   const size_t nc = size_t(3) * latent * ffn / 2, ns = size_t(3) * latent * ffn / 16;
   uint8_t* r = static_cast<uint8_t*>(record_out);
-  memcpy(r, codes, nc);
-  memcpy(r + nc, scales, ns);
+  for (size_t o = 0; o < nc + ns; o += 16) {
+    bool sc = false;
+    const size_t src = record_src(o, size_t(latent), size_t(ffn), &sc);
+    memcpy(r + o, (sc ? scales : codes) + src, 16);
+  }
   memcpy(r + nc + ns, globals, 12);
   return EDGE0_OK;
 }
@@ -246,7 +327,7 @@ edge0_status edge0_pack_experts(const uint8_t* codes, const uint8_t* scales, con
   const int nc = 3 * latent * ffn / 2, ns = 3 * latent * ffn / 16;
   if (n_experts > 65535) return EDGE0_ERR_UNSUPPORTED;
   pack_kernel<<<dim3(64, n_experts), 256, 0, (cudaStream_t)stream>>>(
-      codes, scales, globals, nc, ns, static_cast<uint8_t*>(records), stride);
+      codes, scales, globals, latent, ffn, nc, ns, static_cast<uint8_t*>(records), stride);
   return launch_status();
 }
 
@@ -291,8 +372,8 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
     DecodeArgs a;
     decode_plan(hd, TB, a);
-    const int need = 2 * (d.hidden > d.latent ? d.hidden : d.latent) + 4096;
-    if (a.slab_bytes < need) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
+    const int need = 4 * d.hidden * 2 + 8192;   // an fp32 R D row pair, a gate/up row pair
+    if (a.dyn_bytes < need) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
   }
   if ((ce = decode_prepare(hd->smem_total)) != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
   int occ = 0;
@@ -308,7 +389,8 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t o_z = take(size_t(TD) * L * 4), o_lg = take(size_t(TD) * E * 4);
-  const size_t o_h = take(size_t(TD * K + TD) * F * 4), o_hm = take(size_t(TD * K + TD) * 4);
+  const size_t o_zh = take(size_t(TD) * L * 2), o_dn = take(sizeof(float));
+  const size_t o_h = take(size_t(TD * K + TD) * F * 4);
   const size_t o_c = take(size_t(TD) * L * 4);
   const size_t o_y = take(size_t(2) * TD * H * 2), o_x = take(size_t(2) * TD * H * 2);
   const int TKmax = (d.max_tokens > TD ? d.max_tokens : TD) * K;
@@ -317,6 +399,7 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   const size_t o_perm = take(size_t(TKmax) * 4), o_pos = take(size_t(TKmax) * 4);
   const size_t o_bar = take(sizeof(GridBarrier)), o_err = take(sizeof(int));
   const size_t o_lw = take(sizeof(LayerW)), o_st = take(sizeof(LayerW) * kStackMax);
+  const size_t o_rd = take(size_t(E) * H * 4);
   const size_t o_pf = take(prefill_workspace_bytes(d, d.max_tokens));
   hd->ws_bytes = off;
   if (cudaMalloc(&hd->ws, hd->ws_bytes) != cudaSuccess) {
@@ -326,20 +409,36 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   }
   char* b = hd->ws;
   hd->z = (float*)(b + o_z); hd->logits = (float*)(b + o_lg); hd->h = (float*)(b + o_h);
-  hd->hmax = (unsigned*)(b + o_hm); hd->c = (float*)(b + o_c);
+  hd->zh = (__half*)(b + o_zh);
+  float* d_dnorm = (float*)(b + o_dn);
+  hd->c = (float*)(b + o_c);
   hd->ybuf = (__nv_bfloat16*)(b + o_y); hd->xbuf = (__nv_bfloat16*)(b + o_x);
   hd->idx = (int*)(b + o_idx); hd->w = (float*)(b + o_w); hd->counts = (int*)(b + o_cnt);
   hd->offsets = (int*)(b + o_off); hd->perm = (int*)(b + o_perm); hd->pos = (int*)(b + o_pos);
   hd->bar = (GridBarrier*)(b + o_bar); hd->err = (int*)(b + o_err);
   hd->d_layer = (LayerW*)(b + o_lw); hd->d_stack = (LayerW*)(b + o_st);
+  hd->rd = (float*)(b + o_rd);
   prefill_workspace_carve(d, d.max_tokens, b + o_pf, &hd->pf);
   hd->pf.idx = hd->idx; hd->pf.w = hd->w; hd->pf.counts = hd->counts; hd->pf.offsets = hd->offsets;
   hd->pf.perm = hd->perm; hd->pf.pos = hd->pos;
   hd->pf.err = hd->err;
-  const LayerW lw = layer_of(hd);
   ce = cudaMemset(hd->ws, 0, o_lw);
+  if (ce == cudaSuccess) {
+    row_l1_max_kernel<<<1, 1024>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, d_dnorm);
+    ce = cudaGetLastError();
+  }
+  if (ce == cudaSuccess) ce = cudaMemcpy(&hd->dnorm, d_dnorm, sizeof(float), cudaMemcpyDeviceToHost);
+  const LayerW lw = layer_of(hd);
+  if (ce == cudaSuccess) {
+    fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256>>>(
+        static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), hd->rd, E, L, H);
+    ce = cudaGetLastError();
+  }
   if (ce == cudaSuccess) ce = cudaMemcpy(hd->d_layer, &lw, sizeof(lw), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess) ce = prefill_init(d, &hd->pf, hd->num_sms);
+  // the fold and the initialisation above ran on the legacy stream: finish them
+  // before the handle is used from any stream
+  if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
   if (ce != cudaSuccess) {
     cudaFree(hd->ws);
     delete hd;
@@ -465,6 +564,7 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
   a.layers = h0->d_stack;
   a.n_layers = n_layers;
   a.eps = eps;
+  a.final_norm = 1;
   a.trace_x = static_cast<__nv_bfloat16*>(trace_x);
   a.trace_y = static_cast<__nv_bfloat16*>(trace_y);
   e = decode_launch(a, h0->num_sms, h0->smem_total, s);

@@ -117,51 +117,56 @@ __device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes
 }
 
 // ---------------------------------------------------------------- grid barrier
-// Sense-reversing barrier over all CTAs of a co-resident (cooperative) grid.
+// Ticket barrier over all CTAs of a co-resident (cooperative) grid.  Every
+// barrier adds exactly gridDim.x to `ticket`; a CTA's arrival returns its ticket
+// and it waits until the counter reaches the end of that round.  The counter
+// never resets between launches (it stays a multiple of the grid size), so
+// nothing needs clearing before a launch.  An aborted launch leaves it in the
+// middle of a round: the host must zero the struct before the next launch.
 struct GridBarrier {
-  unsigned int count;
-  unsigned int gen;
+  unsigned long long ticket;
   unsigned int abort;
-  unsigned int pad;
+  unsigned int pad[13];
 };
 
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // All threads of every CTA call this.  Returns false if the barrier was
-// aborted (some CTA timed out); the error word then holds kErrTimeout.
+// aborted (some CTA's wait ran out); the error word then holds kErrTimeout.
 __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    __threadfence();
-    const unsigned int gen = ld_acquire_u32(&bar->gen);
-    const unsigned int arrived = atomicAdd(&bar->count, 1u);
-    if (arrived == gridDim.x - 1) {
-      bar->count = 0;
-      st_release_u32(&bar->gen, gen + 1);
-    } else {
+    unsigned long long tk;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(tk) : "l"(&bar->ticket) : "memory");
+    const unsigned long long target = (tk / gridDim.x + 1) * gridDim.x;
+    if (ld_relaxed_u64(&bar->ticket) < target) {
       const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_u32(&bar->gen) == gen) {
-        if (ld_acquire_u32(&bar->abort)) { ok = 0; break; }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(err, kErrTimeout);
-          atomicExch(&bar->abort, 1u);
-          ok = 0;
-          break;
+      unsigned int spins = 0;
+      while (ld_relaxed_u64(&bar->ticket) < target) {
+        if ((++spins & 31u) == 0) {
+          if (ld_relaxed_u32(&bar->abort)) { ok = 0; break; }
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            atomicExch(&bar->abort, 1u);
+            ok = 0;
+            break;
+          }
         }
-        __nanosleep(32);
       }
     }
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     s_ok = ok;
   }
   __syncthreads();

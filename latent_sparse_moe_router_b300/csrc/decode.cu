@@ -10,73 +10,90 @@ size_t decode_tables_bytes() { return (sizeof(DecTables) + 127) & ~size_t(127); 
 
 namespace {
 
+constexpr unsigned kFull = 0xffffffffu;
+
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
-// ------------------------------------------------------------------ batch waits
+// ------------------------------------------------------------------ mbarrier bookkeeping
 struct Ctx {
   DecTables* tb;
-  uint8_t* base;     // dynamic shared memory base
   int* err;
-  uint32_t mbp;      // parity bits of tb->mbar (identical in every thread)
+  uint32_t mbp;  // parity bits of tb->mbar (identical in every thread)
 };
 
-__device__ __forceinline__ void wait_batch(Ctx& cx, int b) {
+// Wait for the current phase of mbarrier b (idempotent until the phase is released).
+__device__ __forceinline__ void wait_mb(Ctx& cx, int b) {
   if (!mbar_wait(&cx.tb->mbar[b], (cx.mbp >> b) & 1u, cx.err)) atomicOr(&cx.tb->stuck, 1 << b);
 }
-
-// After a round that used batches [0, nb): flip their parity (all threads).
-__device__ __forceinline__ void end_round(Ctx& cx, int nb) { cx.mbp ^= (1u << nb) - 1u; }
+// Release the barriers in `mask` after their use (all threads, uniformly).
+__device__ __forceinline__ void release_mb(Ctx& cx, uint32_t mask) { cx.mbp ^= mask; }
 
 // ------------------------------------------------------------------ dot products
-// Sum over the lanes of an aligned group of `nl` lanes.
 template <int TB>
 __device__ __forceinline__ void group_reduce(float* acc, int nl) {
 #pragma unroll
   for (int i = 0; i < TB; ++i)
-    for (int o = nl >> 1; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    for (int o = nl >> 1; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(kFull, acc[i], o);
 }
 
-// acc[t] += W_row . act[t] over K (bf16 weights in shared memory; activations
-// bf16 or fp32 [T][K] in shared memory); lanes l, l+nl, ... of a group of nl.
-template <int TB, bool ACT_BF16>
-__device__ __forceinline__ void bf16_dot(const uint8_t* wrow, int K, const void* act, int T,
-                                         int l, int nl, float* acc) {
-  const uint4* w4 = reinterpret_cast<const uint4*>(wrow);
+// 8 consecutive activation values of row t as fp32 (bf16 or fp32 storage).
+template <bool ACT_F32>
+__device__ __forceinline__ void act8(const void* act, int K, int t, int c, float* af) {
+  if (ACT_F32) {
+    const float4* ap = reinterpret_cast<const float4*>(static_cast<const float*>(act) + size_t(t) * K);
+    const float4 a0 = ap[2 * c], a1 = ap[2 * c + 1];
+    af[0] = a0.x; af[1] = a0.y; af[2] = a0.z; af[3] = a0.w;
+    af[4] = a1.x; af[5] = a1.y; af[6] = a1.z; af[7] = a1.w;
+  } else {
+    const uint4 av = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(act) + size_t(t) * K)[c];
+    af[0] = bf16_lo(av.x); af[1] = bf16_hi(av.x); af[2] = bf16_lo(av.y); af[3] = bf16_hi(av.y);
+    af[4] = bf16_lo(av.z); af[5] = bf16_hi(av.z); af[6] = bf16_lo(av.w); af[7] = bf16_hi(av.w);
+  }
+}
+
+// acc[t] += W_row . act[t] over K; weights bf16 (W_F32 = false) or fp32, in shared
+// memory; lanes l, l+nl, ... of an aligned group of nl lanes, 8 elements per step.
+template <int TB, bool W_F32, bool ACT_F32>
+__device__ __forceinline__ void row_dot(const uint8_t* wrow, int K, const void* act, int T, int l,
+                                        int nl, float* acc) {
   for (int c = l; c < K / 8; c += nl) {
-    const uint4 wv = w4[c];
-    const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                         bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+    float wf[8];
+    if (W_F32) {
+      const float4* wp = reinterpret_cast<const float4*>(wrow);
+      const float4 w0 = wp[2 * c], w1 = wp[2 * c + 1];
+      wf[0] = w0.x; wf[1] = w0.y; wf[2] = w0.z; wf[3] = w0.w;
+      wf[4] = w1.x; wf[5] = w1.y; wf[6] = w1.z; wf[7] = w1.w;
+    } else {
+      const uint4 wv = reinterpret_cast<const uint4*>(wrow)[c];
+      wf[0] = bf16_lo(wv.x); wf[1] = bf16_hi(wv.x); wf[2] = bf16_lo(wv.y); wf[3] = bf16_hi(wv.y);
+      wf[4] = bf16_lo(wv.z); wf[5] = bf16_hi(wv.z); wf[6] = bf16_lo(wv.w); wf[7] = bf16_hi(wv.w);
+    }
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
       if (t < T) {
         float af[8];
-        if (ACT_BF16) {
-          const uint4 av = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(act) + size_t(t) * K)[c];
-          af[0] = bf16_lo(av.x); af[1] = bf16_hi(av.x); af[2] = bf16_lo(av.y); af[3] = bf16_hi(av.y);
-          af[4] = bf16_lo(av.z); af[5] = bf16_hi(av.z); af[6] = bf16_lo(av.w); af[7] = bf16_hi(av.w);
-        } else {
-          const float4* ap = reinterpret_cast<const float4*>(static_cast<const float*>(act) + size_t(t) * K);
-          const float4 a0 = ap[2 * c], a1 = ap[2 * c + 1];
-          af[0] = a0.x; af[1] = a0.y; af[2] = a0.z; af[3] = a0.w;
-          af[4] = a1.x; af[5] = a1.y; af[6] = a1.z; af[7] = a1.w;
-        }
-        float s = acc[t];
+        act8<ACT_F32>(act, K, t, c, af);
+        float s0 = wf[0] * af[0], s1 = wf[1] * af[1];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s = fmaf(wf[i], af[i], s);
-        acc[t] = s;
+        for (int i = 2; i < 8; i += 2) {
+          s0 = fmaf(wf[i], af[i], s0);
+          s1 = fmaf(wf[i + 1], af[i + 1], s1);
+        }
+        acc[t] += s0 + s1;
       }
     }
   }
 }
 
 // acc[i] += sum_k e2m1(code[k]) * e4m3(scale[k/16]) * act_i[k] for n activation
-// rows (f16, pre-scaled), K = 16 * nblk.  Products of one 16-block are summed in
-// f16x2 (8 per half), the block sum is scaled and accumulated in fp32.
+// rows (f16, pre-scaled).  Lane l of a group of nl lanes takes blocks l, l+nl, ...
+// Products of one 16-block are summed in f16x2 (two chains of 4 per half); the
+// block sum is scaled and accumulated in fp32.
 template <int TB>
 __device__ __forceinline__ void fp4_dot(const uint8_t* codes, const uint8_t* scales, int nblk,
                                         const __half* const* arow, int n, int l, int nl,
                                         float* acc) {
+#pragma unroll 2
   for (int b = l; b < nblk; b += nl) {
     const uint2 cw = reinterpret_cast<const uint2*>(codes)[b];
     const float s = e4m3_to_f32(scales[b]);
@@ -95,177 +112,175 @@ __device__ __forceinline__ void fp4_dot(const uint8_t* codes, const uint8_t* sca
         const uint4* ap = reinterpret_cast<const uint4*>(arow[i] + b * 16);
         const uint4 a0 = ap[0], a1 = ap[1];
         __half2 p = __hmul2(wv[0], u32_as_h2(a0.x));
+        __half2 q = __hmul2(wv[4], u32_as_h2(a1.x));
         p = __hfma2(wv[1], u32_as_h2(a0.y), p);
+        q = __hfma2(wv[5], u32_as_h2(a1.y), q);
         p = __hfma2(wv[2], u32_as_h2(a0.z), p);
+        q = __hfma2(wv[6], u32_as_h2(a1.z), q);
         p = __hfma2(wv[3], u32_as_h2(a0.w), p);
-        p = __hfma2(wv[4], u32_as_h2(a1.x), p);
-        p = __hfma2(wv[5], u32_as_h2(a1.y), p);
-        p = __hfma2(wv[6], u32_as_h2(a1.z), p);
-        p = __hfma2(wv[7], u32_as_h2(a1.w), p);
+        q = __hfma2(wv[7], u32_as_h2(a1.w), q);
         const float2 f = __half22float2(p);
-        acc[i] = fmaf(s, f.x + f.y, acc[i]);
+        const float2 g = __half22float2(q);
+        acc[i] = fmaf(s, (f.x + f.y) + (g.x + g.y), acc[i]);
       }
     }
   }
 }
 
-// ------------------------------------------------------------------ bf16 GEMV over row ranges
-// out_fn(t, row, value) for rows [r0, r1) of W (bf16 [rows][K], global), one warp
-// per row, rows staged in the slab by bulk copies in <= kMaxBatches batches per round.
-template <int TB, bool ACT_BF16, class OutFn>
-__device__ void bf16_gemv_rows(Ctx& cx, const __nv_bfloat16* W, int r0, int r1, int K,
-                               const void* act, int T, uint8_t* slab, int slab_bytes,
-                               OutFn out_fn) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_bytes = K * 2;
-  const int cap = slab_bytes / row_bytes;
-  for (int ra = r0; ra < r1; ra += cap) {
-    const int nrow = min(cap, r1 - ra);
-    const int nb = min(kMaxBatches, nrow);
-    if (threadIdx.x == 0) {
-      for (int b = 0; b < nb; ++b) {
-        const int b0 = nrow * b / nb, b1 = nrow * (b + 1) / nb;
-        const uint32_t bytes = uint32_t(b1 - b0) * row_bytes;
-        mbar_arrive_expect_tx(&cx.tb->mbar[b], bytes);
-        bulk_g2s(slab + size_t(b0) * row_bytes, W + size_t(ra + b0) * K, bytes, &cx.tb->mbar[b]);
-      }
+// ------------------------------------------------------------------ dense rows (bf16 / fp32)
+// Up to two row ranges of row-major matrices, staged in the dynamic region by bulk
+// copies (<= kMbRounds batches per round) and reduced by one half-warp per row:
+// out_fn(m, t, row, value) with m the matrix index.
+struct RowSet {
+  const uint8_t* base;   // matrix m, row-major
+  int r0, r1;            // rows of this CTA
+  int row_bytes;         // K * element size
+  int f32;               // 1: fp32 weights, 0: bf16
+};
+
+// Rows of a round [from, from + n) of the concatenated row list: set-0 rows first.
+struct RoundRows {
+  int c0;      // rows of set 0 in the round
+  int rb0, rb1;
+  int from, n, nb;
+  __device__ __forceinline__ uint32_t offset(int i) const {
+    return i < c0 ? uint32_t(i) * rb0 : uint32_t(c0) * rb0 + uint32_t(i - c0) * rb1;
+  }
+  __device__ __forceinline__ int batch(int i) const {
+    int b = 0;
+    while (i >= n * (b + 1) / nb) ++b;
+    return b;
+  }
+};
+
+__device__ __forceinline__ RoundRows round_rows(const RowSet* rs, int nset, int from, int n) {
+  RoundRows rr;
+  const int n0 = rs[0].r1 - rs[0].r0;
+  rr.c0 = max(0, min(from + n, n0) - from);
+  rr.rb0 = rs[0].row_bytes;
+  rr.rb1 = nset > 1 ? rs[1].row_bytes : rs[0].row_bytes;
+  rr.from = from;
+  rr.n = n;
+  rr.nb = min(kMbRounds, n);
+  return rr;
+}
+
+// Lanes of warp 0: bulk copies of a round, lane b one batch (<= 2 copies: one
+// per set piece).  Call from all 32 lanes of warp 0.
+__device__ void stage_rows(Ctx& cx, const RowSet* rs, int nset, int from, int n, uint8_t* dst) {
+  const RoundRows rr = round_rows(rs, nset, from, n);
+  const int n0 = rs[0].r1 - rs[0].r0;
+  const int b = threadIdx.x & 31;
+  if (b < rr.nb) {
+    const int i0 = n * b / rr.nb, i1 = n * (b + 1) / rr.nb;
+    mbar_arrive_expect_tx(&cx.tb->mbar[kMbRound + b], rr.offset(i1) - rr.offset(i0));
+    // set 0 piece [i0, min(i1, c0)), set 1 piece [max(i0, c0), i1)
+    if (i0 < rr.c0) {
+      const int ie = min(i1, rr.c0);
+      const int row = rs[0].r0 + from + i0;
+      bulk_g2s(dst + rr.offset(i0), rs[0].base + size_t(row) * rr.rb0, uint32_t(ie - i0) * rr.rb0,
+               &cx.tb->mbar[kMbRound + b]);
     }
-    for (int i = warp; i < nrow; i += kDecWarps) {
-      int b = 0;
-      while (i >= nrow * (b + 1) / nb) ++b;
-      wait_batch(cx, b);
+    if (i1 > rr.c0) {
+      const int ia = max(i0, rr.c0);
+      const int row = rs[1].r0 + (from + ia - n0);
+      bulk_g2s(dst + rr.offset(ia), rs[1].base + size_t(row) * rr.rb1, uint32_t(i1 - ia) * rr.rb1,
+               &cx.tb->mbar[kMbRound + b]);
+    }
+  }
+}
+
+__device__ __forceinline__ int dense_cap(const RowSet* rs, int nset, int dyn_bytes) {
+  int maxrb = 0;
+  for (int m = 0; m < nset; ++m) maxrb = max(maxrb, rs[m].row_bytes);
+  return min(512, dyn_bytes / maxrb);
+}
+
+// Rows of the sets, round by round, one half-warp per row; out_fn(m, t, row, v).
+// With `prestaged`, warp 0 already ran stage_rows for the first round
+// (rows [0, min(cap, total))) before the CTA's last __syncthreads.
+template <int TB, bool ACT_F32, class OutFn>
+__device__ void dense_rows(Ctx& cx, const RowSet* rs, int nset, const void* act, int K, int T,
+                           uint8_t* dyn, int dyn_bytes, bool prestaged, OutFn out_fn) {
+  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
+  int total = 0;
+  for (int m = 0; m < nset; ++m) total += rs[m].r1 - rs[m].r0;
+  const int n0 = rs[0].r1 - rs[0].r0;
+  const int cap = dense_cap(rs, nset, dyn_bytes);
+  for (int from = 0; from < total; from += cap) {
+    const int n = min(cap, total - from);
+    if (!(prestaged && from == 0)) {
+      if (threadIdx.x < 32) stage_rows(cx, rs, nset, from, n, dyn);
+    }
+    const RoundRows rr = round_rows(rs, nset, from, n);
+    // both halves of a warp run the same trip count (shuffles in group_reduce)
+    for (int base = (hw & ~1); base < n; base += kDecThreads / 16) {
+      const int i = base + (hw & 1);
+      const bool valid = i < n;
+      const int m = (valid && i >= rr.c0) ? 1 : 0;
+      if (valid) wait_mb(cx, kMbRound + rr.batch(i));
       float acc[TB];
 #pragma unroll
       for (int t = 0; t < TB; ++t) acc[t] = 0.f;
-      bf16_dot<TB, ACT_BF16>(slab + size_t(i) * row_bytes, K, act, T, lane, 32, acc);
-      group_reduce<TB>(acc, 32);
-      if (lane == 0) {
+      if (valid) {
+        const uint8_t* wrow = dyn + rr.offset(i);
+        if (rs[m].f32) row_dot<TB, true, ACT_F32>(wrow, K, act, T, hl, 16, acc);
+        else row_dot<TB, false, ACT_F32>(wrow, K, act, T, hl, 16, acc);
+      }
+      group_reduce<TB>(acc, 16);
+      if (valid && hl == 0) {
+        const int q = from + i;
+        const int row = q < n0 ? rs[0].r0 + q : rs[1].r0 + (q - n0);
 #pragma unroll
         for (int t = 0; t < TB; ++t)
-          if (t < T) out_fn(t, ra + i, acc[t]);
+          if (t < T) out_fn(m, t, row, acc[t]);
       }
     }
-    // every thread waits on every batch so the parity bits stay uniform
-    for (int b = 0; b < nb; ++b) wait_batch(cx, b);
+    for (int b = 0; b < rr.nb; ++b) wait_mb(cx, kMbRound + b);
     __syncthreads();
-    end_round(cx, nb);
+    release_mb(cx, (1u << rr.nb) - 1u);
   }
 }
 
-// ------------------------------------------------------------------ NVFP4 gate/up rows
-// Gate and up rows of SwiGLU experts.  A "row" is q in [q0, q1) of the
-// group-major row space (group g = q / F, f = q % F).  For group g the
-// activation rows are zh[tok_of(g, i)] (i < n_of(g)); results go through
-// h_fn(g, i, f, gate_dot, up_dot).  res holds 2 x rcap x TB floats.
-template <int TB, class RecFn, class NFn, class TokFn, class HFn>
-__device__ void fp4_gateup_rows(Ctx& cx, int q0, int q1, int L, int F, const __half* zh,
-                                uint8_t* slab, int slab_bytes, float* res, int rcap,
-                                RecFn rec_of, NFn n_of, TokFn tok_of, HFn h_fn) {
-  const int tid = threadIdx.x;
-  const int hw = tid >> 4, hl = tid & 15;           // half-warp id and lane
-  const int crow = L / 2, srow = L / 16;            // code / scale bytes per row
-  const int per_row = 2 * (crow + srow);
-  const int cap = min(slab_bytes / per_row, rcap);
-  DecTables* tb = cx.tb;
-  int qa = q0;
-  while (qa < q1) {
-    // the round: at most `cap` rows and at most kMaxBatches group runs
-    int nrow = 0, runs = 0;
-    while (qa + nrow < q1 && nrow < cap && runs < kMaxBatches) {
-      const int q = qa + nrow;
-      const int qe = min(min((q / F + 1) * F, q1), qa + cap);
-      nrow += qe - q;
-      ++runs;
-    }
-    if (tid == 0) {
-      // one batch per run, then split the longest runs until kMaxBatches
-      int rs[kMaxBatches], rl[kMaxBatches], parts[kMaxBatches];
-      {
-        int q = qa;
-        for (int r = 0; r < runs; ++r) {
-          const int qe = min((q / F + 1) * F, qa + nrow);
-          rs[r] = q; rl[r] = qe - q; parts[r] = 1;
-          q = qe;
-        }
-      }
-      for (int extra = kMaxBatches - runs; extra > 0; --extra) {
-        int best = -1;
-        for (int r = 0; r < runs; ++r)
-          if (parts[r] < rl[r] && (best < 0 || rl[r] * parts[best] > rl[best] * parts[r])) best = r;
-        if (best < 0) break;
-        ++parts[best];
-      }
-      int nb = 0;
-      uint32_t off = 0;
-      for (int r = 0; r < runs; ++r) {
-        for (int pi = 0; pi < parts[r]; ++pi) {
-          const int s0 = rs[r] + rl[r] * pi / parts[r], s1 = rs[r] + rl[r] * (pi + 1) / parts[r];
-          const int b = nb++;
-          const int g = s0 / F, f0 = s0 % F, n = s1 - s0;
-          const uint8_t* rec = rec_of(g);
-          const uint32_t cb = uint32_t(n) * crow, sb = uint32_t(n) * srow;
-          const size_t up_c = size_t(F) * crow, sc0 = size_t(3) * F * L / 2;
-          const size_t up_s = size_t(F) * srow;
-          mbar_arrive_expect_tx(&tb->mbar[b], 2 * (cb + sb));
-          bulk_g2s(slab + off, rec + size_t(f0) * crow, cb, &tb->mbar[b]);
-          bulk_g2s(slab + off + cb, rec + up_c + size_t(f0) * crow, cb, &tb->mbar[b]);
-          bulk_g2s(slab + off + 2 * cb, rec + sc0 + size_t(f0) * srow, sb, &tb->mbar[b]);
-          bulk_g2s(slab + off + 2 * cb + sb, rec + sc0 + up_s + size_t(f0) * srow, sb, &tb->mbar[b]);
-          for (int i = 0; i < n; ++i) {
-            const int rr = s0 - qa + i;
-            tb->task_row[rr] = s0 + i;                            // q
-            tb->task_aux[rr] = (b << 16) | n;                     // batch, rows in batch
-            tb->task_off[rr] = off + uint32_t(i) * crow;          // gate codes row
-            tb->task_off2[rr] = off + 2 * cb + uint32_t(i) * srow;  // gate scales row
-          }
-          off += 2 * (cb + sb);
-        }
-      }
-      tb->round_nb = nb;
-    }
-    __syncthreads();
-    const int nb = tb->round_nb;
-    // tasks: (row, gate|up), one half-warp each
-    for (int task = hw; task < 2 * nrow; task += kDecThreads / 16) {
-      const int r = task >> 1, mat = task & 1;
-      const int q = tb->task_row[r];
-      const int b = tb->task_aux[r] >> 16, n_in_b = tb->task_aux[r] & 0xFFFF;
-      const int g = q / F;
-      wait_batch(cx, b);
-      const uint8_t* codes = slab + tb->task_off[r] + (mat ? uint32_t(n_in_b) * crow : 0u);
-      const uint8_t* scl = slab + tb->task_off2[r] + (mat ? uint32_t(n_in_b) * srow : 0u);
-      const int n = n_of(g);
-      const __half* arow[TB];
+// ------------------------------------------------------------------ top-k (tree of warp sorts)
+// The k largest of E logits by (value descending, index ascending).  Chunks of 32
+// experts are sorted across the lanes of a warp (bitonic network over shuffles);
+// sorted top-16 lists are then merged pairwise (bitonic merge) level by level.
+struct Cand {
+  float v;
+  int i;
+};
+
+__device__ __forceinline__ bool cand_first(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Bitonic sort of one (v, i) per lane across the warp, descending.
+__device__ __forceinline__ void warp_sort_desc(float& v, int& i, int lane) {
 #pragma unroll
-      for (int i = 0; i < TB; ++i) arow[i] = zh + size_t(i < n ? tok_of(g, i) : 0) * L;
-      float acc[TB];
+  for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
-      for (int i = 0; i < TB; ++i) acc[i] = 0.f;
-      fp4_dot<TB>(codes, scl, L / 16, arow, n, hl, 16, acc);
-      group_reduce<TB>(acc, 16);
-      if (hl == 0) {
-#pragma unroll
-        for (int i = 0; i < TB; ++i)
-          if (i < n) res[(size_t(mat) * rcap + r) * TB + i] = acc[i];
-      }
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, v, j);
+      const int oi = __shfl_xor_sync(kFull, i, j);
+      const bool desc = (lane & k) == 0 || k == 32;
+      const bool lower = (lane & j) == 0;
+      const bool o_first = cand_first(ov, oi, v, i);
+      if ((lower == desc) ? o_first : !o_first) { v = ov; i = oi; }
     }
-    for (int b = 0; b < nb; ++b) wait_batch(cx, b);
-    __syncthreads();
-    end_round(cx, nb);
-    // SwiGLU per (row, activation)
-    for (int p = tid; p < nrow * TB; p += kDecThreads) {
-      const int r = p / TB, i = p % TB;
-      const int q = tb->task_row[r];
-      const int g = q / F;
-      if (i < n_of(g)) h_fn(g, i, q % F, res[size_t(r) * TB + i], res[(size_t(rcap) + r) * TB + i]);
-    }
-    __syncthreads();
-    qa += nrow;
   }
 }
 
-__device__ __forceinline__ void atomic_max_abs(unsigned int* p, float v) {
-  atomicMax(p, __float_as_uint(fabsf(v)));
+// Merge of a bitonic sequence across the warp into descending order.
+__device__ __forceinline__ void warp_merge_desc(float& v, int& i, int lane) {
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const float ov = __shfl_xor_sync(kFull, v, j);
+    const int oi = __shfl_xor_sync(kFull, i, j);
+    const bool lower = (lane & j) == 0;
+    const bool o_first = cand_first(ov, oi, v, i);
+    if (lower ? o_first : !o_first) { v = ov; i = oi; }
+  }
 }
 
 // power-of-two scale that brings max |v| into [0.5, 1)
@@ -276,6 +291,60 @@ __device__ __forceinline__ void pow2_scale(float maxabs, float* sc, float* inv) 
   *inv = ldexpf(1.0f, e);
 }
 
+// x_out = bf16(v / sqrt(mean(v^2) + eps)), v = x + y, for T rows of H (all threads of
+// the CTA; the summation order matches edge0_residual_rmsnorm's kernel).
+__device__ void residual_norm(DecTables* tb, const __nv_bfloat16* xp, const __nv_bfloat16* yp,
+                              __nv_bfloat16* xs, int T, int H, float eps) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int t = 0; t < T; ++t) {
+    float s = 0.f;
+    for (int k = tid; k < H; k += kDecThreads) {
+      const float v = __bfloat162float(xp[size_t(t) * H + k]) + __bfloat162float(yp[size_t(t) * H + k]);
+      s = fmaf(v, v, s);
+    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) tb->red[warp * kDecodeMaxT + t] = s;
+  }
+  __syncthreads();
+  if (tid < T) {
+    float s = 0.f;
+    for (int wv = 0; wv < kDecWarps; ++wv) s += tb->red[wv * kDecodeMaxT + tid];
+    tb->inv_rms[tid] = 1.0f / sqrtf(s / float(H) + eps);
+  }
+  __syncthreads();
+  for (int i = tid; i < T * H; i += kDecThreads) {
+    const int t = i / H;
+    const float v = __bfloat162float(xp[i]) + __bfloat162float(yp[i]);
+    xs[i] = __float2bfloat16_rn(v * tb->inv_rms[t]);
+  }
+  __syncthreads();
+}
+
+// SwiGLU of one gate/up row pair by one warp: lanes 0-15 reduce the gate row,
+// lanes 16-31 the up row, for n activation rows; h_fn(i, h) per activation i.
+template <int TB, class HFn>
+__device__ __forceinline__ void gateup_row(const uint8_t* gc, const uint8_t* gs, const uint8_t* uc,
+                                           const uint8_t* us, int L, const __half* const* arow, int n,
+                                           float gg, float gu, const float* ainv, HFn h_fn) {
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const bool up = lane >= 16;
+  float acc[TB];
+#pragma unroll
+  for (int i = 0; i < TB; ++i) acc[i] = 0.f;
+  fp4_dot<TB>(up ? uc : gc, up ? us : gs, L / 16, arow, n, hl, 16, acc);
+  group_reduce<TB>(acc, 16);
+#pragma unroll
+  for (int i = 0; i < TB; ++i) {
+    const float other = __shfl_xor_sync(kFull, acc[i], 16);
+    if (i < n && lane == i) {
+      // lane i < 16 holds the gate sum in acc[i] and the up sum in `other`
+      const float gv = gg * acc[i] * ainv[i];
+      const float uv = gu * other * ainv[i];
+      h_fn(i, silu_f(gv) * uv);
+    }
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ the kernel
@@ -283,154 +352,152 @@ template <int TB>
 __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];
   DecTables* tb = reinterpret_cast<DecTables*>(dsm);
-  Ctx cx{tb, dsm, a.err, 0u};
+  Ctx cx{tb, a.err, 0u};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, bid = blockIdx.x;
   const int T = a.T, H = a.H, L = a.L, E = a.E, K = a.K, F = a.F;
-  const int TK = T * K;
-  uint8_t* act = dsm + a.off_act;
+  const int TK = T * K, nslot = TK + T;
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dsm + a.off_xs);
+  float* act = reinterpret_cast<float*>(dsm + a.off_act);
   __half* zh = reinterpret_cast<__half*>(dsm + a.off_zh);
-  uint8_t* slab = dsm + a.off_slab;
-  const size_t rec_codes = size_t(3) * F * L / 2;
-  const size_t rec_body = rec_codes + size_t(3) * F * L / 16;
+  uint8_t* shr = dsm + a.off_sh;
+  uint8_t* dyn = dsm + a.off_dyn;
+  // record layout: GU block of F rows (gate codes | up codes | gate scales | up
+  // scales, 9L/8 bytes), D block of L/2 row pairs (codes 2p | codes 2p+1 |
+  // scales 2p | scales 2p+1, 9F/8 bytes), then the three fp32 scales
+  const int gu_row = 9 * L / 8, d_pair = 9 * F / 8;
+  const size_t rec_dblk = size_t(F) * gu_row;
+  const size_t rec_body = rec_dblk + size_t(L / 2) * d_pair;
+  const int cofs_up = L / 2, sofs_g = L, sofs_u = L + L / 16;   // offsets inside a GU row
+  // this CTA's row ranges (latent rows in whole pairs)
+  const int r0 = 2 * int(long(bid) * (L / 2) / G), r1 = 2 * int(long(bid + 1) * (L / 2) / G);
+  const int e0 = int(long(bid) * E / G), e1 = int(long(bid + 1) * E / G);      // router rows
+  const int f0 = int(long(bid) * F / G), f1 = int(long(bid + 1) * F / G);      // shared rows
+  const int j0 = int(long(bid) * H / G), j1 = int(long(bid + 1) * H / G);      // hidden rows
+  const int nr = r1 - r0, nsr = f1 - f0;
 
   if (tid == 0) {
-    for (int b = 0; b < kMaxBatches; ++b) mbar_init(&tb->mbar[b], 1);
+    for (int b = 0; b < kNumMbar; ++b) mbar_init(&tb->mbar[b], 1);
     fence_mbar_init();
     tb->stuck = 0;
   }
   __syncthreads();
 
+  LayerW lw = a.l0;
   for (int li = 0; li < a.n_layers; ++li) {
-    const LayerW lw = a.layers[li];
     const bool last = (li == a.n_layers - 1);
     __nv_bfloat16* xcur = a.xbuf + size_t(li & 1) * T * H;
-    // ================================================================ P0: x, z = D x
+    // ================================================================ P0: z = D x, l = (R D) x + b
     {
-      // L2 prefetch of the routing-independent bytes of this layer
-      l2_prefetch_share(lw.R, size_t(E) * L * 2, bid, G);
-      l2_prefetch_share(lw.U, size_t(H) * L * 2, bid, G);
-      l2_prefetch_share(lw.shared, rec_body, bid, G);
-      __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(act);
+      // shared-expert gate/up rows of this CTA, consumed in P1
+      if (tid == 0 && nsr > 0) {
+        mbar_arrive_expect_tx(&tb->mbar[kMbShared], uint32_t(nsr) * gu_row);
+        bulk_g2s(shr, lw.shared + size_t(f0) * gu_row, uint32_t(nsr) * gu_row, &tb->mbar[kMbShared]);
+      }
+      RowSet rs[2] = {{reinterpret_cast<const uint8_t*>(lw.D), r0, r1, H * 2, 0},
+                      {reinterpret_cast<const uint8_t*>(lw.RD), e0, e1, H * 4, 1}};
+      // the weight rows are in flight before x is even read
+      if (warp == 0 && nr + (e1 - e0) > 0)
+        stage_rows(cx, rs, 2, 0, min(dense_cap(rs, 2, a.dyn_bytes), nr + (e1 - e0)), dyn);
       if (li == 0) {
         for (int i = tid; i < T * H / 8; i += kDecThreads)
           reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
+        __syncthreads();
       } else {
         // x_l = bf16(RMSNorm(x_{l-1} + y_{l-1})), computed by every CTA
-        const __nv_bfloat16* xp = a.xbuf + size_t((li - 1) & 1) * T * H;
-        const __nv_bfloat16* yp = a.ybuf + size_t((li - 1) & 1) * T * H;
-        for (int t = 0; t < T; ++t) {
-          float s = 0.f;
-          for (int k = tid; k < H; k += kDecThreads) {
-            const float v = __bfloat162float(xp[size_t(t) * H + k]) + __bfloat162float(yp[size_t(t) * H + k]);
-            s = fmaf(v, v, s);
-          }
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lane == 0) tb->red[warp * kDecodeMaxT + t] = s;
-        }
-        __syncthreads();
-        if (tid < T) {
-          float s = 0.f;
-          for (int wv = 0; wv < kDecWarps; ++wv) s += tb->red[wv * kDecodeMaxT + tid];
-          tb->inv_rms[tid] = 1.0f / sqrtf(s / float(H) + a.eps);
-        }
-        __syncthreads();
-        for (int i = tid; i < T * H; i += kDecThreads) {
-          const int t = i / H;
-          const float v = __bfloat162float(xp[i]) + __bfloat162float(yp[i]);
-          xs[i] = __float2bfloat16_rn(v * tb->inv_rms[t]);
-        }
+        residual_norm(tb, a.xbuf + size_t((li - 1) & 1) * T * H, a.ybuf + size_t((li - 1) & 1) * T * H,
+                      xs, T, H, a.eps);
       }
-      __syncthreads();
       if (bid == 0) {
         for (int i = tid; i < T * H / 8; i += kDecThreads)
           reinterpret_cast<uint4*>(xcur)[i] = reinterpret_cast<const uint4*>(xs)[i];
         if (a.trace_x)
           for (int i = tid; i < T * H / 8; i += kDecThreads)
             reinterpret_cast<uint4*>(a.trace_x + size_t(li) * T * H)[i] = reinterpret_cast<const uint4*>(xs)[i];
-        for (int i = tid; i < TK + T; i += kDecThreads) a.hmax[i] = 0u;
       }
-      const int r0 = int(long(bid) * L / G), r1 = int(long(bid + 1) * L / G);
-      float* z = a.z;
-      bf16_gemv_rows<TB, true>(cx, lw.D, r0, r1, H, xs, T, slab, a.slab_bytes,
-                               [&](int t, int r, float v) { z[size_t(t) * L + r] = v; });
-    }
-    if (!grid_sync(a.bar, a.err)) return;
-    // ================================================================ P1: router logits, shared gate/up
-    {
-      float* zs = reinterpret_cast<float*>(act);
-      for (int i = tid; i < T * L / 4; i += kDecThreads)
-        reinterpret_cast<float4*>(zs)[i] = reinterpret_cast<const float4*>(a.z)[i];
-      __syncthreads();
-      for (int t = warp; t < T; t += kDecWarps) {
+      // per-token power-of-two scale of z for its f16 copy, from the bound
+      // |z_r| <= max_r sum_h |D_rh| * max_h |x_h|, identical in every CTA
+      for (int t = 0; t < T; ++t) {
         float m = 0.f;
-        for (int k = lane; k < L; k += 32) m = fmaxf(m, fabsf(zs[size_t(t) * L + k]));
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) pow2_scale(m, &tb->zsc[t], &tb->zinv[t]);
+        for (int k = tid; k < H; k += kDecThreads) m = fmaxf(m, fabsf(__bfloat162float(xs[size_t(t) * H + k])));
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        if (lane == 0) tb->red[warp * kDecodeMaxT + t] = m;
       }
       __syncthreads();
-      for (int i = tid; i < T * L; i += kDecThreads) zh[i] = __float2half_rn(zs[i] * tb->zsc[i / L]);
+      if (tid < T) {
+        float m = 0.f;
+        for (int wv = 0; wv < kDecWarps; ++wv) m = fmaxf(m, tb->red[wv * kDecodeMaxT + tid]);
+        pow2_scale(m * lw.dnorm, &tb->zsc[tid], &tb->zinv[tid]);
+      }
       __syncthreads();
-      // router rows of this CTA
-      const int e0 = int(long(bid) * E / G), e1 = int(long(bid + 1) * E / G);
+      float* z = a.z;
+      __half* zg = a.zh;
       float* logits = a.logits;
       const float* bias = lw.bias;
-      bf16_gemv_rows<TB, false>(cx, lw.R, e0, e1, L, zs, T, slab, a.slab_bytes,
-                                [&](int t, int e, float v) {
-                                  logits[size_t(t) * E + e] = v + (bias ? bias[e] : 0.f);
-                                });
-      // shared expert gate/up rows [f0, f1) for every token; results -> h slots TK + t
-      const int f0 = int(long(bid) * F / G), f1 = int(long(bid + 1) * F / G);
-      const float* gsh = reinterpret_cast<const float*>(lw.shared + rec_body);
-      const float gg = gsh[0], gu = gsh[1];
-      float* res = reinterpret_cast<float*>(dsm + a.off_res);
-      float* hbuf = a.h;
-      unsigned int* hmax = a.hmax;
-      const float* zinv = tb->zinv;
-      fp4_gateup_rows<TB>(
-          cx, f0, f1, L, F, zh, slab, a.slab_bytes, res, a.res_rows,
-          [&](int) { return lw.shared; }, [&](int) { return T; }, [&](int, int i) { return i; },
-          [&](int, int i, int f, float gd, float ud) {
-            const float hv = silu_f(gg * gd * zinv[i]) * (gu * ud * zinv[i]);
-            hbuf[size_t(TK + i) * F + f] = hv;
-            atomic_max_abs(&hmax[TK + i], hv);
-          });
+      const float* zsc = tb->zsc;
+      dense_rows<TB, false>(cx, rs, 2, xs, H, T, dyn, a.dyn_bytes, true, [&](int m, int t, int row, float v) {
+        if (m == 0) {
+          z[size_t(t) * L + row] = v;
+          zg[size_t(t) * L + row] = __float2half_rn(v * zsc[t]);
+        } else {
+          logits[size_t(t) * E + row] = v + (bias ? bias[row] : 0.f);
+        }
+      });
     }
     if (!grid_sync(a.bar, a.err)) return;
-    // ================================================================ P2: routing, routed gate/up
+    // ================================================================ P1: routing, gate/up -> h
     {
-      float* ls = reinterpret_cast<float*>(act);
-      for (int i = tid; i < T * E / 4; i += kDecThreads)
-        reinterpret_cast<float4*>(ls)[i] = reinterpret_cast<const float4*>(a.logits)[i];
+      // U rows of this CTA into L2 for P3 (routing-independent)
+      if (tid == 0 && j1 > j0) l2_prefetch_share(lw.U + size_t(j0) * L, size_t(j1 - j0) * L * 2, 0, 1);
+      if (tid == 0) tb->task_ctr = 0;
+      // zh = f16(z * 2^-e) per token (warp t), and the chunk sorts of the top-k
+      const int nc = (E + 31) / 32;
+      Cand* cx0 = reinterpret_cast<Cand*>(act);                       // [T][nc][16]
+      Cand* cx1 = cx0 + size_t(T) * nc * 16;                          // [T][(nc+1)/2][16]
+      for (int i = tid; i < T * L / 8; i += kDecThreads)
+        reinterpret_cast<uint4*>(zh)[i] = reinterpret_cast<const uint4*>(a.zh)[i];
+      for (int task = warp; task < T * nc; task += kDecWarps) {
+        const int t = task / nc, c = task % nc;
+        const int e = c * 32 + lane;
+        float v = e < E ? a.logits[size_t(t) * E + e] : -INFINITY;
+        if (isnan(v)) v = -INFINITY;        // any pick stays a valid expert
+        int ix = e < E ? e : 0x7fffffff;
+        warp_sort_desc(v, ix, lane);
+        if (lane < 16) cx0[(size_t(t) * nc + c) * 16 + lane] = Cand{v, ix};
+      }
       __syncthreads();
-      // top-K per token: one warp per token, lane owns experts lane + 32 j
-      for (int t = warp; t < T; t += kDecWarps) {
-        const float* lt = ls + size_t(t) * E;
-        uint32_t taken = 0u;
-        float top0 = 0.f, den = 0.f;
-        float sel[kMaxTopK];
-        for (int j = 0; j < K; ++j) {
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
-          for (int q = 0; lane + 32 * q < E; ++q) {
-            const int e = lane + 32 * q;
-            const float raw = lt[e];
-            const float v = isnan(raw) ? -INFINITY : raw;   // any pick stays a valid expert
-            if (!((taken >> q) & 1u) && (v > bv || (v == bv && e < bi))) { bv = v; bi = e; }
+      // merge levels: lists 2p, 2p+1 -> p (an odd last list passes through)
+      {
+        Cand* src = cx0;
+        Cand* dst = cx1;
+        for (int width = nc; width > 1; width = (width + 1) / 2) {
+          const int outw = (width + 1) / 2;
+          for (int task = warp; task < T * outw; task += kDecWarps) {
+            const int t = task / outw, p = task % outw;
+            const Cand* la = src + (size_t(t) * width + 2 * p) * 16;
+            Cand* lo = dst + (size_t(t) * outw + p) * 16;
+            if (2 * p + 1 < width) {
+              const Cand cv = lane < 16 ? la[lane] : la[16 + (31 - lane)];
+              float v = cv.v;
+              int ix = cv.i;
+              warp_merge_desc(v, ix, lane);
+              if (lane < 16) lo[lane] = Cand{v, ix};
+            } else if (lane < 16) {
+              lo[lane] = la[lane];
+            }
           }
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-          }
-          if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-          if (j == 0) top0 = bv;
-          sel[j] = expf(bv - top0);
-          den += sel[j];
-          if (lane == 0) tb->idx[t * K + j] = bi;
+          __syncthreads();
+          Cand* tmp = src; src = dst; dst = tmp;
         }
-        if (lane == 0)
-          for (int j = 0; j < K; ++j) tb->w[t * K + j] = sel[j] / den;
+        // src holds [T][1][16]: the ranked candidates; weights = softmax over the k
+        for (int t = warp; t < T; t += kDecWarps) {
+          const Cand cv = src[size_t(t) * 16 + (lane < 16 ? lane : 0)];
+          const float top0 = __shfl_sync(kFull, cv.v, 0);
+          const float ev = lane < K ? expf(cv.v - top0) : 0.f;
+          float den = ev;
+          for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+          if (lane < K) { tb->idx[t * K + lane] = cv.i; tb->w[t * K + lane] = ev / den; }
+        }
       }
       __syncthreads();
       // permutation: stable order by (expert, slot)
@@ -450,7 +517,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         for (int p0 = 0; p0 < TK; p0 += 32) {
           const int p = p0 + lane;
           const bool start = p < TK && (p == 0 || tb->idx[tb->perm[p]] != tb->idx[tb->perm[p - 1]]);
-          const unsigned bal = __ballot_sync(0xffffffffu, start);
+          const unsigned bal = __ballot_sync(kFull, start);
           if (start) {
             const int gi = base + __popc(bal & ((1u << lane) - 1u));
             tb->gexp[gi] = tb->idx[tb->perm[p]];
@@ -462,12 +529,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       __syncthreads();
       const int nu = tb->nu;
+      // routed gate/up rows: q in [q0, q1) of nu * F (group-major)
+      const long nq = long(nu) * F;
+      const int q0 = int(nq * bid / G), q1 = int(nq * (bid + 1) / G);
+      const int per_row = gu_row;
+      // stage P2's down rows now when the whole P1 slab and the down slab both fit
+      const int ngr = nu + 1;                          // routed groups + the shared expert
+      const int down_grp = (nr / 2) * d_pair;
+      const int down_bytes = ngr * down_grp;
+      const int gu_bytes = (q1 - q0) * per_row;
+      const int hrows_bytes = nslot * F * 2;
+      const int ob_bytes = (nslot * nr * 4 + 127) & ~127;
+      const int gu_alloc = (gu_bytes + 1023) & ~1023;
+      const bool stage_down = nr > 0 && (q1 - q0) <= 256 &&
+                              gu_alloc + down_bytes + hrows_bytes + ob_bytes <= a.dyn_bytes;
+      if (tid == 0) {
+        tb->down_staged = stage_down ? 1 : 0;
+        tb->down_off = gu_alloc;
+      }
+      // bid 0 publishes the routing of the last layer
       if (bid == 0 && last) {
         for (int s = tid; s < TK; s += kDecThreads) {
           a.idx[s] = tb->idx[s]; a.w[s] = tb->w[s]; a.perm[s] = tb->perm[s]; a.pos[s] = tb->posn[s];
         }
         for (int e = tid; e <= E; e += kDecThreads) {
-          // offsets[e] = slots routed to experts < e; counts[e] = slots routed to e
           int off = TK, cnt = 0;
           for (int g = 0; g < nu; ++g) {
             if (tb->gexp[g] >= e) { off = tb->goff[g]; if (tb->gexp[g] == e) cnt = tb->goff[g + 1] - tb->goff[g]; break; }
@@ -476,151 +561,277 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           if (e < E) a.counts[e] = cnt;
         }
       }
-      // L2 prefetch of the selected experts' down matrices (codes and scales)
-      {
-        const int parts = max(1, G / max(nu, 1));
-        for (int u = bid; u < nu * parts; u += G) {
-          const int g = u / parts, part = u % parts;
-          const uint8_t* rec = lw.experts + size_t(tb->gexp[g]) * lw.stride;
-          if (tid == 0) {
-            l2_prefetch_share(rec + size_t(F) * L, size_t(L) * F / 2, part, parts);
-            l2_prefetch_share(rec + rec_codes + size_t(F) * L / 8, (size_t(L) * F / 16 + 15) & ~size_t(15), part, parts);
-          }
-        }
-      }
-      // routed gate/up rows: q in [q0, q1) of nu * F
-      const long nq = long(nu) * F;
-      const int q0 = int(nq * bid / G), q1 = int(nq * (bid + 1) / G);
-      float* res = reinterpret_cast<float*>(dsm + a.off_res);
-      float* hbuf = a.h;
-      unsigned int* hmax = a.hmax;
-      const float* zinv = tb->zinv;
+      const uint8_t* experts = lw.experts;
+      const size_t stride = lw.stride;
+      const float* gsh = reinterpret_cast<const float*>(lw.shared + rec_body);
+      const float sgg = gsh[0], sgu = gsh[1];
+      const __half* arow_all[TB];
+#pragma unroll
+      for (int i = 0; i < TB; ++i) arow_all[i] = zh + size_t(i < T ? i : 0) * L;
       const int* gexp = tb->gexp;
       const int* goff = tb->goff;
       const int* perm = tb->perm;
-      const uint8_t* experts = lw.experts;
-      const size_t stride = lw.stride;
-      fp4_gateup_rows<TB>(
-          cx, q0, q1, L, F, zh, slab, a.slab_bytes, res, a.res_rows,
-          [&](int g) { return experts + size_t(gexp[g]) * stride; },
-          [&](int g) { return goff[g + 1] - goff[g]; },
-          [&](int g, int i) { return perm[goff[g] + i] / K; },
-          [&](int g, int i, int f, float gd, float ud) {
+      int qa = q0;
+      bool first_round = true;
+      while (qa < q1) {
+        // with the down rows staged behind it, every round stays inside gu_alloc
+        const int cap = min(256, (stage_down ? gu_alloc : a.dyn_bytes) / per_row);
+        const int nrow = min(cap, q1 - qa);
+        // batches of BR rows, one lane of warp 0 each (a batch may span a group boundary)
+        const int BR = (nrow + kMbRounds - 1) / kMbRounds;
+        const int nb = (nrow + BR - 1) / BR;          // every batch non-empty
+        if (warp == 0 && lane < nb) {
+          const int s0 = qa + lane * BR, s1 = min(s0 + BR, qa + nrow);
+          if (s1 > s0) {
+            const int b = lane;
+            mbar_arrive_expect_tx(&tb->mbar[kMbRound + b], uint32_t(s1 - s0) * per_row);
+            uint32_t off = uint32_t(lane) * BR * per_row;
+            for (int q = s0; q < s1;) {
+              // rows of one expert are one byte range of its GU block
+              const int g = q / F, fa = q % F;
+              const int n = min(s1, (g + 1) * F) - q;
+              const uint8_t* rec = experts + size_t(gexp[g]) * stride;
+              bulk_g2s(dyn + off, rec + size_t(fa) * gu_row, uint32_t(n) * gu_row, &tb->mbar[kMbRound + b]);
+              off += uint32_t(n) * gu_row;
+              q += n;
+            }
+          }
+        }
+        if (stage_down && first_round && warp == 1) {
+          // down rows [r0, r1) of every used expert (shared first), for P2: the batch
+          // leader arms the barrier, then one lane per expert issues its two copies
+          uint8_t* dd = dyn + gu_alloc;
+          const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
+          for (int gbase = 0; gbase < ngr; gbase += 32) {
+            const int gi = gbase + lane;
+            if (gi < ngr && gi % per_b == 0) {
+              const int n_in = min(per_b, ngr - gi);
+              mbar_arrive_expect_tx(&tb->mbar[kMbDown + gi / per_b], uint32_t(n_in) * down_grp);
+            }
+            __syncwarp();
+            if (gi < ngr) {
+              // this CTA's row pairs of one expert's D block: one byte range
+              const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
+              bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
+                       uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
+            }
+          }
+        }
+        __syncthreads();
+        if (first_round && nsr > 0) {
+          // shared-expert rows (staged in P0) while the routed rows land
+          wait_mb(cx, kMbShared);
+          for (;;) {
+            int r = 0;
+            if (lane == 0) r = atomicAdd(&tb->task_ctr, 1);
+            r = __shfl_sync(kFull, r, 0);
+            if (r >= nsr) break;
+            const uint8_t* row = shr + size_t(r) * gu_row;
+            gateup_row<TB>(row, row + sofs_g, row + cofs_up, row + sofs_u, L, arow_all, T, sgg, sgu, tb->zinv,
+                           [&](int i, float hv) { a.h[size_t(TK + i) * F + f0 + r] = hv; });
+          }
+        }
+        // one warp per row pair: lanes 0-15 gate, lanes 16-31 up
+        for (int r = warp; r < nrow; r += kDecWarps) {
+          // row r of the round sits at r * gu_row (pieces are packed back to back)
+          const int q = qa + r;
+          const int g = q / F, f = q % F;
+          wait_mb(cx, kMbRound + r / BR);
+          const uint8_t* gc = dyn + size_t(r) * gu_row;
+          const uint8_t* gs = gc + sofs_g;
+          const uint8_t* uc = gc + cofs_up;
+          const uint8_t* us = gc + sofs_u;
+          const int n = goff[g + 1] - goff[g];
+          const __half* arow[TB];
+          float ainv[TB];
+#pragma unroll
+          for (int i = 0; i < TB; ++i) {
+            const int t = perm[goff[g] + (i < n ? i : 0)] / K;
+            arow[i] = zh + size_t(t) * L;
+            ainv[i] = tb->zinv[t];
+          }
+          const float* gl = reinterpret_cast<const float*>(experts + size_t(gexp[g]) * stride + rec_body);
+          gateup_row<TB>(gc, gs, uc, us, L, arow, n, gl[0], gl[1], ainv, [&](int i, float hv) {
             const int slot = perm[goff[g] + i];
-            const float* gl = reinterpret_cast<const float*>(experts + size_t(gexp[g]) * stride + rec_body);
-            const int t = slot / K;
-            const float hv = silu_f(gl[0] * gd * zinv[t]) * (gl[1] * ud * zinv[t]);
-            hbuf[size_t(slot) * F + f] = hv;
-            atomic_max_abs(&hmax[slot], hv);
+            a.h[size_t(slot) * F + f] = hv;
           });
+        }
+        for (int b = 0; b < nb; ++b) wait_mb(cx, kMbRound + b);
+        __syncthreads();
+        release_mb(cx, (1u << nb) - 1u);
+        if (first_round && nsr > 0) release_mb(cx, 1u << kMbShared);
+        qa += nrow;
+        first_round = false;
+      }
+      if (first_round && nsr > 0) {
+        // no routed rows for this CTA: the shared rows still run
+        wait_mb(cx, kMbShared);
+        for (;;) {
+          int r = 0;
+          if (lane == 0) r = atomicAdd(&tb->task_ctr, 1);
+          r = __shfl_sync(kFull, r, 0);
+          if (r >= nsr) break;
+          const uint8_t* row = shr + size_t(r) * gu_row;
+          gateup_row<TB>(row, row + sofs_g, row + cofs_up, row + sofs_u, L, arow_all, T, sgg, sgu, tb->zinv,
+                         [&](int i, float hv) { a.h[size_t(TK + i) * F + f0 + r] = hv; });
+        }
+        __syncthreads();
+        release_mb(cx, 1u << kMbShared);
+      }
+      if (tid == 0 && li + 1 < a.n_layers) {
+        // next layer's D and R D into L2 while this layer finishes
+        const LayerW nx = a.layers[li + 1];
+        l2_prefetch_share(nx.D, size_t(L) * H * 2, bid, G);
+        l2_prefetch_share(nx.RD, size_t(E) * H * 4, bid, G);
+      }
     }
     if (!grid_sync(a.bar, a.err)) return;
-    // ================================================================ P3: down + combine -> c
+    // ================================================================ P2: down + combine -> c
+    LayerW nxt = lw;
+    if (li + 1 < a.n_layers) nxt = a.layers[li + 1];
     {
       const int nu = tb->nu;
-      const int nslot = TK + T;
-      for (int s = tid; s < nslot; s += kDecThreads) {
-        pow2_scale(__uint_as_float(a.hmax[s]), &tb->hsc[s], &tb->hinv[s]);
-      }
-      if (li + 1 < a.n_layers) {
-        const LayerW nx = a.layers[li + 1];
-        if (tid == 0) l2_prefetch_share(nx.D, size_t(L) * H * 2, bid, G);
-      }
-      __syncthreads();
-      const int r0 = int(long(bid) * L / G), r1 = int(long(bid + 1) * L / G);
-      const int nr = r1 - r0;
-      // region: [ob (nslot x nr fp32) | h f16 rows | staged down rows]
-      uint8_t* region = act;
-      const int region_bytes = a.act_bytes + (a.off_slab - a.off_zh) + a.slab_bytes;
-      float* ob = reinterpret_cast<float*>(region);
-      const int ob_bytes = ((nslot * nr * 4) + 127) & ~127;
-      const int hrow = F * 2;
-      const int crow = F / 2, srow = F / 16;
-      const size_t down_c = size_t(F) * L, down_s = rec_codes + size_t(F) * L / 8;
-      // groups: j = 0 shared, j >= 1 routed group j-1
-      const int ngroups = nu + 1;
-      int j0 = 0;
-      while (nr > 0 && j0 < ngroups) {
-        // plan the round on every thread (deterministic, identical)
-        int j1 = j0, nslots_r = 0;
-        int wbytes = 0;
-        while (j1 < ngroups) {
-          const int ns = (j1 == 0) ? T : (tb->goff[j1] - tb->goff[j1 - 1]);
-          const int wb = ((nr * crow + 15) & ~15) + ((nr * srow + 32 + 15) & ~15);
-          const int need = ob_bytes + (nslots_r + ns) * hrow + wbytes + wb;
-          if (need > region_bytes || (j1 - j0) >= 2 * 256) break;
-          nslots_r += ns; wbytes += wb; ++j1;
+      const bool down_staged = tb->down_staged != 0;
+      const int ngr = nu + 1;
+      const int down_grp = (nr / 2) * d_pair;
+      const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
+      const int n_down_b = (ngr + per_b - 1) / per_b;
+      // stage P3's U rows (L2-resident by now) where P1's gate/up slab was
+      const int nur = j1 - j0;
+      const int u_bytes = nur * L * 2;
+      const bool stage_u = down_staged && u_bytes <= tb->down_off;
+      if (tid == 0) {
+        tb->u_staged = stage_u ? 1 : 0;
+        if (stage_u && nur > 0) {
+          const int nc = (u_bytes + 16383) / 16384;
+          mbar_arrive_expect_tx(&tb->mbar[kMbU], uint32_t(u_bytes));
+          for (int c = 0; c < nc; ++c) {
+            const int ra = nur * c / nc, rb = nur * (c + 1) / nc;
+            if (rb > ra)
+              bulk_g2s(dyn + size_t(ra) * L * 2, lw.U + size_t(j0 + ra) * L, uint32_t(rb - ra) * L * 2,
+                       &tb->mbar[kMbU]);
+          }
         }
-        const int ng = j1 - j0;
+      }
+      // region for h rows and per-slot outputs: after the staged down rows, or the
+      // whole dynamic region when the down rows go in rounds
+      uint8_t* region;
+      int region_bytes;
+      if (down_staged) {
+        region = dyn + tb->down_off + ngr * down_grp;
+        region_bytes = a.dyn_bytes - (tb->down_off + ngr * down_grp);
+      } else {
+        region = dyn;
+        region_bytes = a.dyn_bytes;
+      }
+      float* ob = reinterpret_cast<float*>(region);
+      const int ob_bytes = (nslot * nr * 4 + 127) & ~127;
+      const int hrow = F * 2;
+      int j0g = 0;
+      while (nr > 0 && j0g < ngr) {
+        // groups [j0g, j1g) this round: h rows (and, without staging, down rows) must fit
+        int j1g = j0g, nslots_r = 0, wbytes = 0;
+        while (j1g < ngr) {
+          const int ns = (j1g == 0) ? T : (tb->goff[j1g] - tb->goff[j1g - 1]);
+          const int wb = down_staged ? 0 : down_grp;
+          if (ob_bytes + (nslots_r + ns) * hrow + wbytes + wb > region_bytes || (j1g - j0g) >= 512) break;
+          nslots_r += ns; wbytes += wb; ++j1g;
+        }
+        const int ng = j1g - j0g;
         if (ng == 0) {  // cannot happen for validated shapes; stop instead of spinning
           if (tid == 0) atomicOr(a.err, kErrTimeout);
           break;
         }
-        const int nb = min(kMaxBatches, ng);
-        uint8_t* wbase = region + ob_bytes + nslots_r * hrow;
-        if (tid == 0) {
-          uint32_t off = 0;
+        const int nb = down_staged ? 0 : min(kMbRounds, ng);
+        uint8_t* wbase = down_staged ? dyn + tb->down_off : region + ob_bytes + nslots_r * hrow;
+        if (tid == 0 && !down_staged) {
           for (int b = 0; b < nb; ++b) {
-            const int ga = j0 + ng * b / nb, gb = j0 + ng * (b + 1) / nb;
-            uint32_t tot = 0;
-            for (int j = ga; j < gb; ++j) {
-              const uint32_t cb = ((nr * crow + 15) & ~15);
-              const size_t s_off = down_s + size_t(r0) * srow;
-              const size_t s_a = s_off & ~size_t(15);
-              const size_t s_b = (s_off + size_t(nr) * srow + 15) & ~size_t(15);
-              tot += cb + uint32_t(s_b - s_a);
-            }
-            mbar_arrive_expect_tx(&tb->mbar[b], tot);
+            const int ga = j0g + ng * b / nb, gb = j0g + ng * (b + 1) / nb;
+            mbar_arrive_expect_tx(&tb->mbar[kMbRound + b], uint32_t(gb - ga) * down_grp);
             for (int j = ga; j < gb; ++j) {
               const uint8_t* rec = (j == 0) ? lw.shared : lw.experts + size_t(tb->gexp[j - 1]) * lw.stride;
-              const uint32_t cb = ((nr * crow + 15) & ~15);
-              const size_t s_off = down_s + size_t(r0) * srow;
-              const size_t s_a = s_off & ~size_t(15);
-              const size_t s_b = (s_off + size_t(nr) * srow + 15) & ~size_t(15);
-              // codes rows [r0, r1): nr * F/2 bytes (a multiple of 16 as F % 64 == 0)
-              bulk_g2s(wbase + off, rec + down_c + size_t(r0) * crow, uint32_t(nr) * crow, &tb->mbar[b]);
-              bulk_g2s(wbase + off + cb, rec + s_a, uint32_t(s_b - s_a), &tb->mbar[b]);
-              tb->task_off[j - j0] = off;
-              tb->task_off2[j - j0] = off + cb + uint32_t(s_off - s_a);
-              tb->task_aux[j - j0] = b;
-              off += cb + uint32_t(s_b - s_a);
+              bulk_g2s(wbase + size_t(j - j0g) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
+                       uint32_t(down_grp), &tb->mbar[kMbRound + b]);
+              tb->task_aux[j - j0g] = b;
             }
           }
         }
-        // h rows of the round's slots, scaled to f16 (shared slots first, then routed by position)
+        // h rows of the round's slots, scaled to f16: shared slots first, then routed by position
         __half* hs = reinterpret_cast<__half*>(region + ob_bytes);
-        {
-          int ls = 0;
-          for (int j = j0; j < j1; ++j) {
-            const int ns = (j == 0) ? T : (tb->goff[j] - tb->goff[j - 1]);
-            for (int i = warp; i < ns; i += kDecWarps) {
-              const int slot = (j == 0) ? TK + i : tb->perm[tb->goff[j - 1] + i];
-              const float sc = tb->hsc[slot];
-              const float4* src = reinterpret_cast<const float4*>(a.h + size_t(slot) * F);
-              __half2* dst = reinterpret_cast<__half2*>(hs + size_t(ls + i) * F);
-              for (int k = lane; k < F / 4; k += 32) {
-                const float4 v = src[k];
-                dst[2 * k] = __floats2half2_rn(v.x * sc, v.y * sc);
-                dst[2 * k + 1] = __floats2half2_rn(v.z * sc, v.w * sc);
-              }
+        const int sh = (j0g == 0) ? T : 0;
+        const int p0 = (j0g == 0) ? 0 : tb->goff[j0g - 1];
+        if (tid < ng) {
+          const int j = j0g + tid;
+          tb->task_row[tid] = (j == 0) ? 0 : sh + (tb->goff[j - 1] - p0);
+        }
+        for (int i = warp; i < nslots_r; i += kDecWarps) {
+          // one warp per slot: the row in registers (one round trip), max |h|, scaled f16 copy
+          const int slot = (i < sh) ? TK + i : tb->perm[p0 + (i - sh)];
+          const float4* src = reinterpret_cast<const float4*>(a.h + size_t(slot) * F);
+          __half2* dst = reinterpret_cast<__half2*>(hs + size_t(i) * F);
+          for (int k0 = 0; k0 < F / 4; k0 += 32 * 8) {
+            float4 v[8];
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int k = k0 + lane + 32 * j;
+              v[j] = k < F / 4 ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            if (tid == 0) tb->task_row[j - j0] = ls;
-            ls += ns;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              m = fmaxf(fmaxf(m, fmaxf(fabsf(v[j].x), fabsf(v[j].y))), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+            if (k0 == 0 && F / 4 <= 32 * 8) {
+              float sc, inv;
+              pow2_scale(m, &sc, &inv);
+              if (lane == 0) tb->hinv[slot] = inv;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int k = k0 + lane + 32 * j;
+                if (k < F / 4) {
+                  dst[2 * k] = __floats2half2_rn(v[j].x * sc, v[j].y * sc);
+                  dst[2 * k + 1] = __floats2half2_rn(v[j].z * sc, v[j].w * sc);
+                }
+              }
+            } else {
+              // rows longer than 1024: a second pass (max first over all chunks)
+              float mm = m;
+              for (int k1 = k0 + 32 * 8; k1 < F / 4; k1 += 32) {
+                for (int k = k1 + lane; k < min(k1 + 32, F / 4); k += 32) {
+                  const float4 w4 = src[k];
+                  mm = fmaxf(fmaxf(mm, fmaxf(fabsf(w4.x), fabsf(w4.y))), fmaxf(fabsf(w4.z), fabsf(w4.w)));
+                }
+              }
+              for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
+              float sc, inv;
+              pow2_scale(mm, &sc, &inv);
+              if (lane == 0) tb->hinv[slot] = inv;
+              for (int k = lane; k < F / 4; k += 32) {
+                const float4 w4 = src[k];
+                dst[2 * k] = __floats2half2_rn(w4.x * sc, w4.y * sc);
+                dst[2 * k + 1] = __floats2half2_rn(w4.z * sc, w4.w * sc);
+              }
+              break;
+            }
           }
         }
         __syncthreads();
-        // tasks (group, row): 8 lanes each, 4 per warp; the loop bound is uniform
-        // per warp so the shuffles in group_reduce see all 32 lanes
+        // tasks (group, row): 8 lanes each, 4 per warp; the loop bound is uniform per warp
         const int l8 = tid & 7;
         for (int tbase = warp * 4; tbase < ng * nr; tbase += kDecThreads / 8) {
           const int task = tbase + (lane >> 3);
           const bool valid = task < ng * nr;
           const int jj = valid ? task / nr : 0, r = valid ? task % nr : 0;
-          const int j = j0 + jj;
+          const int j = j0g + jj;
           const int ns = !valid ? 0 : (j == 0) ? T : (tb->goff[j] - tb->goff[j - 1]);
-          if (valid) wait_batch(cx, tb->task_aux[jj]);
-          const uint8_t* codes = wbase + tb->task_off[jj] + size_t(r) * crow;
-          const uint8_t* scl = wbase + tb->task_off2[jj] + size_t(r) * srow;
+          if (valid) {
+            if (down_staged) wait_mb(cx, kMbDown + j / per_b);
+            else wait_mb(cx, kMbRound + tb->task_aux[jj]);
+          }
+          const uint8_t* gbase = wbase + size_t(down_staged ? j : jj) * down_grp;
+          const uint8_t* pr = gbase + size_t(r / 2) * d_pair;
+          const uint8_t* codes = pr + (r & 1) * (F / 2);
+          const uint8_t* scl = pr + F + (r & 1) * (F / 16);
           const __half* arow[TB];
 #pragma unroll
           for (int i = 0; i < TB; ++i) arow[i] = hs + size_t(tb->task_row[jj] + (i < ns ? i : 0)) * F;
@@ -641,10 +852,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             }
           }
         }
-        for (int b = 0; b < nb; ++b) wait_batch(cx, b);
+        if (!down_staged) {
+          for (int b = 0; b < nb; ++b) wait_mb(cx, kMbRound + b);
+        }
         __syncthreads();
-        end_round(cx, nb);
-        j0 = j1;
+        if (!down_staged) release_mb(cx, (1u << nb) - 1u);
+        j0g = j1g;
+      }
+      if (down_staged) {
+        for (int b = 0; b < n_down_b; ++b) wait_mb(cx, kMbDown + b);
+        __syncthreads();
+        release_mb(cx, ((1u << n_down_b) - 1u) << kMbDown);
       }
       // combine: c[t][r] = o_shared + sum_j w[t][j] o[t*K + j], j ascending
       for (int p = tid; p < T * nr; p += kDecThreads) {
@@ -655,30 +873,61 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
     }
     if (!grid_sync(a.bar, a.err)) return;
-    // ================================================================ P4: y = U c
+    // ================================================================ P3: y = U c
     {
-      float* cs = reinterpret_cast<float*>(act);
       for (int i = tid; i < T * L / 4; i += kDecThreads)
-        reinterpret_cast<float4*>(cs)[i] = reinterpret_cast<const float4*>(a.c)[i];
+        reinterpret_cast<float4*>(act)[i] = reinterpret_cast<const float4*>(a.c)[i];
       __syncthreads();
-      const int j0 = int(long(bid) * H / G), j1 = int(long(bid + 1) * H / G);
-      __nv_bfloat16* yo = last ? a.y : a.ybuf + size_t(li & 1) * T * H;
+      __nv_bfloat16* yo = (last && !a.final_norm) ? a.y : a.ybuf + size_t(li & 1) * T * H;
       __nv_bfloat16* ty = a.trace_y ? a.trace_y + size_t(li) * T * H : nullptr;
-      bf16_gemv_rows<TB, false>(cx, lw.U, j0, j1, L, cs, T, slab, a.slab_bytes,
-                                [&](int t, int j, float v) {
-                                  const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                                  yo[size_t(t) * H + j] = b;
-                                  if (ty) ty[size_t(t) * H + j] = b;
-                                });
+      auto emit = [&](int t, int j, float v) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        yo[size_t(t) * H + j] = b;
+        if (ty) ty[size_t(t) * H + j] = b;
+      };
+      const int nur = j1 - j0;
+      if (tb->u_staged) {
+        if (nur > 0) wait_mb(cx, kMbU);
+        const int hw = tid >> 4, hl = tid & 15;
+        for (int base = (hw & ~1); base < nur; base += kDecThreads / 16) {
+          const int i = base + (hw & 1);
+          const bool valid = i < nur;
+          float acc[TB];
+#pragma unroll
+          for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+          if (valid) row_dot<TB, false, true>(dyn + size_t(i) * L * 2, L, act, T, hl, 16, acc);
+          group_reduce<TB>(acc, 16);
+          if (valid && hl == 0) {
+#pragma unroll
+            for (int t = 0; t < TB; ++t)
+              if (t < T) emit(t, j0 + i, acc[t]);
+          }
+        }
+        __syncthreads();
+        if (nur > 0) release_mb(cx, 1u << kMbU);
+      } else {
+        RowSet rs[1] = {{reinterpret_cast<const uint8_t*>(lw.U), j0, j1, L * 2, 0}};
+        dense_rows<TB, true>(cx, rs, 1, act, L, T, dyn, a.dyn_bytes, false,
+                             [&](int, int t, int j, float v) { emit(t, j, v); });
+      }
     }
-    if (!last) {
+    if (!last || a.final_norm) {
       if (!grid_sync(a.bar, a.err)) return;
     }
+    if (last && a.final_norm) {
+      // stack output: RMSNorm(x_last + y_last); every CTA normalises, each writes its slice
+      residual_norm(tb, xcur, a.ybuf + size_t(li & 1) * T * H, xs, T, H, a.eps);
+      const int n8 = T * H / 8;
+      const int i0 = int(long(bid) * n8 / G), i1 = int(long(bid + 1) * n8 / G);
+      for (int i = i0 + tid; i < i1; i += kDecThreads)
+        reinterpret_cast<uint4*>(a.y)[i] = reinterpret_cast<const uint4*>(xs)[i];
+    }
+    lw = nxt;
   }
   // a wait that ran out may leave a copy in flight: wait for it once more (bounded)
   __syncthreads();
   if (tid == 0 && tb->stuck) {
-    for (int b = 0; b < kMaxBatches; ++b)
+    for (int b = 0; b < kNumMbar; ++b)
       if ((tb->stuck >> b) & 1) mbar_wait(&tb->mbar[b], (cx.mbp >> b) & 1u, a.err);
   }
 }

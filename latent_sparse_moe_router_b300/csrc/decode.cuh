@@ -4,20 +4,21 @@
 // hardware requirements", section "Edge0-145B latent MoE architecture"):
 //   z = D x;  l = R z + b;  top-k + renormalised softmax;  o_e = W_d (silu(W_g z) * W_up z);
 //   c = o_shared + sum_k w_k o_k;  y = U c.
-// At T <= 16 every step is a GEMV bound by HBM bandwidth, and each step needs all
-// of the previous one (z before the router, the routing before the routed
-// experts, every h before the down projection, all of c before U).  So one CTA
-// per SM runs five phases separated by software grid barriers:
-//   P0  z = D x            (D rows of this CTA; L2 prefetch of R, U, shared record)
-//   P1  logits = R z + b;  shared expert gate/up -> h_shared
-//   P2  top-k + weights + permutation (redundantly per CTA, in shared memory);
-//       routed gate/up -> h (rows of the union of selected experts);
-//       L2 prefetch of the selected experts' down matrices
-//   P3  down projections of every used expert for this CTA's latent rows; combine -> c
-//   P4  y = U c
-// Each CTA stages its slab of weights in shared memory with bulk copies
-// (cp.async.bulk, completion on mbarriers) and dequantises NVFP4 in registers.
-// A stack of layers (residual + RMSNorm between them) runs in the same launch.
+// At T <= 16 every step is a GEMV bound by HBM bandwidth and each step needs all of
+// the previous one.  One CTA per SM runs four phases separated by software grid
+// barriers (the minimum for this dependency chain):
+//   P0  z = D x and l = (R D) x + b     R D is folded once, in fp32, when the handle
+//                                        is created, so the router needs no phase of its own
+//   P1  top-k + weights + permutation   redundantly per CTA, in shared memory, while
+//       shared-expert gate/up           other warps run the shared expert (staged in P0)
+//       routed gate/up -> h             rows of the union of the selected experts;
+//                                        the down rows of P2 are staged at the same time
+//   P2  down projections + combine -> c (U rows of P3 staged at the start)
+//   P3  y = U c
+// Weights move with bulk copies (cp.async.bulk) into shared memory, completion on
+// mbarriers, one phase ahead where shared memory allows; NVFP4 is dequantised in
+// registers.  A stack of layers (residual + RMSNorm between them) runs in the same
+// launch, each layer prefetching the next one's D and R D into L2.
 #pragma once
 
 #include "common.cuh"
@@ -28,50 +29,63 @@ constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxTopK = 16;
 constexpr int kDecodeMaxT = 16;
-constexpr int kMaxBatches = 8;  // mbarriers per round
+constexpr int kMaxSlots = kDecodeMaxT * (kMaxTopK + 1);
+constexpr int kNumMbar = 16;
+// mbarrier roles
+constexpr int kMbRound = 0;      // 0..7: batches of the current round
+constexpr int kMbRounds = 8;
+constexpr int kMbShared = 8;     // shared-expert gate/up rows (P0 -> P1)
+constexpr int kMbDown = 9;       // 9..12: down rows staged in P1 for P2
+constexpr int kMbDownN = 4;
+constexpr int kMbU = 13;         // U rows staged in P2 for P3
 
 // One layer's weights as the decode kernel sees them.
 struct LayerW {
   const __nv_bfloat16* D;   // [L][H]
   const __nv_bfloat16* U;   // [H][L]
-  const __nv_bfloat16* R;   // [E][L]
+  const float* RD;          // [E][H] fp32: router folded with D (R D)
   const float* bias;        // [E] or null
   const uint8_t* experts;   // E records
   const uint8_t* shared;    // 1 record
   unsigned long long stride;
+  float dnorm;              // max_r sum_h |D[r][h]|: bounds |z| / max|x|
 };
 
 struct DecodeArgs {
+  LayerW l0;                // the first layer (kernel parameter: no load before P0)
   const LayerW* layers;     // device array [n_layers]
   int n_layers;
   float eps;                // RMSNorm epsilon between layers
+  int final_norm;           // 1: y = RMSNorm(x_last + y_last) (stack output)
   const __nv_bfloat16* x;   // [T][H]
   __nv_bfloat16* y;         // [T][H]
   int T;
   int H, L, E, K, F;
   // workspace
   float* z;                 // [T][L]
+  __half* zh;               // [T][L] f16 copy of z * 2^-e_t (the experts' input)
   float* logits;            // [T][E]
   float* h;                 // [T*K + T][F]  routed slots, then the shared slot of each token
-  unsigned int* hmax;       // [T*K + T]     max |h| per slot (float bits)
   float* c;                 // [T][L]
   __nv_bfloat16* ybuf;      // [2][T][H] layer outputs inside a stack
-  __nv_bfloat16* xbuf;      // [T][H]    normalised input of the current layer (debug)
+  __nv_bfloat16* xbuf;      // [2][T][H] normalised layer inputs inside a stack
   int* idx; float* w; int* counts; int* offsets; int* perm; int* pos;  // last layer's routing
   __nv_bfloat16* trace_x;   // optional [n_layers][T][H]: input of every layer
   __nv_bfloat16* trace_y;   // optional [n_layers][T][H]: output of every layer
   GridBarrier* bar;
   int* err;
-  // shared-memory plan (bytes from the dynamic base)
-  int off_act, act_bytes;   // x bf16 / z fp32 / c fp32 / h f16 (P3, together with zh)
-  int off_zh;               // zh f16 [T][L] (directly after act)
-  int off_slab, slab_bytes; // staged weights
+  // shared-memory plan (bytes from the 128-aligned dynamic base)
+  int off_xs;               // x bf16 [T][H] (P0; shares its bytes with act)
+  int off_act, act_bytes;   // top-k candidates (P1), c fp32 [T][L] (P3)
+  int off_zh;               // zh f16 [T][L]
+  int off_sh, sh_bytes;     // shared-expert gate/up rows of this CTA
   int off_res, res_rows;    // gate/up dot results: 2 x res_rows x TB fp32
+  int off_dyn, dyn_bytes;   // staged weights, per phase
 };
 
-// Shared tables at the start of dynamic shared memory.
+// Tables at the start of dynamic shared memory.
 struct alignas(16) DecTables {
-  uint64_t mbar[kMaxBatches];
+  uint64_t mbar[kNumMbar];
   int idx[kDecodeMaxT * kMaxTopK];
   float w[kDecodeMaxT * kMaxTopK];
   int perm[kDecodeMaxT * kMaxTopK];     // grouped position -> slot
@@ -79,15 +93,19 @@ struct alignas(16) DecTables {
   int gexp[kDecodeMaxT * kMaxTopK];     // distinct experts, ascending
   int goff[kDecodeMaxT * kMaxTopK + 1]; // group g = perm[goff[g] .. goff[g+1])
   int nu;                                // number of distinct experts
-  int mb_phase;                          // parity bits of mbar[] (uniform)
   int stuck;                             // bit b: a wait on mbar[b] ran out
   int round_nb;                          // batches of the current round
+  int task_ctr;                          // dynamic task counter
+  int down_staged;                       // P1 staged the down rows (P2 uses them)
+  int down_off;                          // their offset in the dynamic region
+  int u_staged;                          // P2 staged the U rows (P3 uses them)
+  int pad0;
   float zsc[kDecodeMaxT], zinv[kDecodeMaxT];
-  float hsc[kDecodeMaxT * (kMaxTopK + 1)], hinv[kDecodeMaxT * (kMaxTopK + 1)];
+  float hinv[kMaxSlots];                 // 2^e of each slot's f16 h copy
   float red[kDecWarps * kDecodeMaxT];
   float inv_rms[kDecodeMaxT];
   // per-round task tables
-  int task_row[512];                     // generic per-round row descriptors
+  int task_row[512];
   int task_aux[512];
   unsigned int task_off[512];
   unsigned int task_off2[512];

@@ -1,14 +1,16 @@
 """Reader of one packed NVFP4 expert record (oracle; test infrastructure).
 
-Written from the record layout the library documents for its packer (the
-pages fix the format, NVFP4 with one E4M3 scale per 16 weights along K and an
-fp32 scale per matrix, but no byte layout; the model card's "Architecture"
-section only says each expert is one fixed-size record).  For latent L and
-SwiGLU width F the record holds, in order, with no gaps:
+Written from the record layout the library documents for its packer.  The
+pages fix the format (NVFP4: E2M1 elements, an E4M3 scale per 16 weights along
+K, an fp32 scale per matrix) and say each expert is one fixed-size record
+("Edge0-145B · Q3_K" model card, section "Architecture"), but print no byte
+layout.  For latent L and SwiGLU width F the record holds, with no gaps:
 
-  gate codes  [F][L/2]   up codes  [F][L/2]   down codes  [L][F/2]
-  gate scales [F][L/16]  up scales [F][L/16]  down scales [L][F/16]
-  globals fp32 little-endian: gate, up, down
+  GU block: F rows of 9L/8 bytes; row f = gate codes f (L/2) | up codes f (L/2)
+            | gate scales f (L/16) | up scales f (L/16)
+  D block:  L/2 row pairs of 9F/8 bytes; pair p = down codes rows 2p, 2p+1
+            (F/2 each) | down scales rows 2p, 2p+1 (F/16 each)
+  globals:  fp32 little-endian gate, up, down
 
 Codes: two E2M1 nibbles per byte, low nibble first along K.  Records sit in an
 array at a caller-chosen stride (the library's default rounds the size up to
@@ -29,12 +31,22 @@ def record_bytes(latent: int, ffn: int) -> int:
 
 
 def read_record(buf: np.ndarray, latent: int, ffn: int):
-    """Split one record (uint8 buffer) into the logical (codes, scales, globals)."""
+    """Split one record (uint8 buffer) into the logical (codes, scales, globals).
+
+    Logical order: codes = gate [F][L/2] | up [F][L/2] | down [L][F/2];
+    scales = gate [F][L/16] | up [F][L/16] | down [L][F/16].
+    """
     L, F = latent, ffn
     buf = np.asarray(buf, dtype=np.uint8)
-    n_codes = 3 * F * L // 2
-    n_scales = 3 * F * L // 16
-    codes = buf[:n_codes]
-    scales = buf[n_codes:n_codes + n_scales]
-    glob = buf[n_codes + n_scales:n_codes + n_scales + 12].view("<f4").astype(np.float32)
+    gu_row, d_pair = 9 * L // 8, 9 * F // 8
+    gu = buf[:F * gu_row].reshape(F, gu_row)
+    dd = buf[F * gu_row:F * gu_row + (L // 2) * d_pair].reshape(L // 2, d_pair)
+    g_codes, u_codes = gu[:, :L // 2], gu[:, L // 2:L]
+    g_scales, u_scales = gu[:, L:L + L // 16], gu[:, L + L // 16:]
+    d_codes = dd[:, :F].reshape(L, F // 2)
+    d_scales = dd[:, F:].reshape(L, F // 16)
+    codes = np.concatenate([g_codes.ravel(), u_codes.ravel(), d_codes.ravel()])
+    scales = np.concatenate([g_scales.ravel(), u_scales.ravel(), d_scales.ravel()])
+    body = F * gu_row + (L // 2) * d_pair
+    glob = buf[body:body + 12].view("<f4").astype(np.float32)
     return codes, scales, glob

@@ -135,7 +135,7 @@ def test_every_token_on_the_same_experts(dev):
     spec = small_spec(seed=3)
     inp = synth.make_layer(spec)
     inp.bias = np.zeros(spec.n_experts, np.float32)
-    inp.bias[:spec.top_k] = 100.0 + np.arange(spec.top_k, 0, -1, dtype=np.float32)
+    inp.bias[:spec.top_k] = 100.0 + 20.0 * np.arange(spec.top_k, 0, -1, dtype=np.float32)
     d = dev.DeviceLayer(inp, max_tokens=16)
     lay = oracle_layer(inp)
     T = 16

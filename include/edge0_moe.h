@@ -214,6 +214,31 @@ edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, c
                                            void *trace_y, edge0_stream_t stream);
 
 /*
+ * Decode forward (T <= 16) that allocates no device memory: the paper has no
+ * counterpart; this entry exists for callers that cannot call cudaMalloc (a
+ * host program that owns every device allocation and hands out a fixed budget,
+ * a plug-in that may not grow the process's memory, a real-time loop where an
+ * allocation or the synchronisation it can cause is not allowed).
+ *   desc      the layer, as for edge0_moe_create (max_tokens is ignored)
+ *   x, y      device bf16 [T][hidden], must not overlap
+ *   status_out  device int or NULL: receives, stream-ordered after the forward,
+ *             EDGE0_OK or the device error bits (a wait that ran out)
+ * Scratch lives in one static device array of this library (about 7.8 MB, held
+ * by every GPU that loads the library until the process exits).  Limits:
+ * T <= 16, hidden <= 3072, latent <= 2048, n_experts <= 512, ffn <= 1024;
+ * larger sizes return EDGE0_ERR_UNSUPPORTED without touching the device.
+ * The first call on a device looks up the array's device address and sets the
+ * decode kernel's launch attributes (once per device, with that device
+ * current): make that first call before any stream capture.  All calls share
+ * the array and each clears the words that must start at zero; calls that
+ * overlap on the GPU race, so the caller must serialise them.  Each call also
+ * recomputes R D into the array, and z enters the expert dot products as f16
+ * without the range pre-scaling the handle path applies.
+ */
+edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc *desc, const void *x, void *y, int T,
+                                       int *status_out, edge0_stream_t stream);
+
+/*
  * Synchronise with the device and return the handle's device error word
  * (EDGE0_OK, or EDGE0_ERR_TIMEOUT if a bounded device wait ran out since the
  * last call); clears the word.

@@ -26,7 +26,7 @@ EXPORTED = (
     "edge0_pack_experts", "edge0_quantize_nvfp4", "edge0_moe_create", "edge0_moe_forward",
     "edge0_moe_debug_routing", "edge0_moe_debug_tensor", "edge0_residual_rmsnorm",
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
-    "edge0_status_string", "edge0_moe_destroy",
+    "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc",
 )
 
 
@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_get_error": (i, [vp]),
             "edge0_status_string": (ctypes.c_char_p, [i]),
             "edge0_moe_destroy": (None, [vp]),
+            "edge0_moe_forward_noalloc": (i, [ctypes.POINTER(edge0_moe_desc), vp, vp, i, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -193,6 +194,16 @@ def edge0_moe_stack_forward_trace(handles, x, y, T, eps, trace_x, trace_y, strea
                                                _ptr(x), _ptr(y), T, float(eps), _ptr(trace_x),
                                                _ptr(trace_y), _stream(stream)),
            "edge0_moe_stack_forward_trace")
+
+
+def edge0_moe_forward_noalloc(hidden, latent, n_experts, top_k, ffn, D, U, router, router_bias, experts,
+                              expert_stride, shared_expert, x, y, T, status=None, stream=None):
+    """Decode forward with no device allocation (scratch in the library's static
+    array); for callers that cannot call cudaMalloc.  See the C header."""
+    d = edge0_moe_desc(hidden, latent, n_experts, top_k, ffn, 0, _ptr(D), _ptr(U), _ptr(router),
+                       _ptr(router_bias), _ptr(experts), expert_stride, _ptr(shared_expert))
+    _check(lib().edge0_moe_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(y), T, _ptr(status),
+                                           _stream(stream)), "edge0_moe_forward_noalloc")
 
 
 def edge0_moe_get_error(handle) -> int:

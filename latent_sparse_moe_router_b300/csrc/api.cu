@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "decode.cuh"
@@ -623,3 +624,144 @@ void edge0_moe_destroy(void* handle) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ forward without allocation
+// Some callers cannot call cudaMalloc: code that runs under a fixed device-memory
+// budget handed out by another allocator, plug-ins living inside a host program
+// that owns every allocation, or real-time loops where an allocation (and the
+// device synchronisation it can trigger) is not allowed.  For them the decode
+// forward can run with its scratch in this file's static device array instead of
+// a handle's workspace.  Every GPU that loads the library holds the array until
+// the process exits.  All calls share it, so calls that overlap on the GPU (two
+// streams, two host threads) race and must be serialised by the caller.
+namespace {
+
+// Limits of the static scratch (the layer shapes it can hold).
+constexpr int kNaMaxT = kDecodeMaxT;       // 16 tokens
+constexpr int kNaMaxH = 3072, kNaMaxL = 2048, kNaMaxE = 512, kNaMaxK = kMaxTopK, kNaMaxF = 1024;
+
+constexpr size_t na_align(size_t v) { return (v + 255) / 256 * 256; }
+constexpr size_t kNaRD = 0;                                                  // fp32 [E][H]
+constexpr size_t kNaZ = kNaRD + na_align(size_t(kNaMaxE) * kNaMaxH * 4);     // fp32 [T][L]
+constexpr size_t kNaZh = kNaZ + na_align(size_t(kNaMaxT) * kNaMaxL * 4);     // f16 [T][L]
+constexpr size_t kNaLg = kNaZh + na_align(size_t(kNaMaxT) * kNaMaxL * 2);    // fp32 [T][E]
+constexpr size_t kNaH = kNaLg + na_align(size_t(kNaMaxT) * kNaMaxE * 4);     // fp32 [T*K+T][F]
+constexpr size_t kNaC = kNaH + na_align(size_t(kNaMaxT) * (kNaMaxK + 1) * kNaMaxF * 4);
+constexpr size_t kNaYb = kNaC + na_align(size_t(kNaMaxT) * kNaMaxL * 4);     // bf16 [2][T][H]
+constexpr size_t kNaXb = kNaYb + na_align(size_t(2) * kNaMaxT * kNaMaxH * 2);
+constexpr size_t kNaRt = kNaXb + na_align(size_t(2) * kNaMaxT * kNaMaxH * 2); // idx w perm pos
+constexpr size_t kNaCnt = kNaRt + na_align(size_t(4) * kNaMaxT * kNaMaxK * 4);
+constexpr size_t kNaOff = kNaCnt + na_align(size_t(kNaMaxE) * 4);
+constexpr size_t kNaBar = kNaOff + na_align(size_t(kNaMaxE + 1) * 4);        // barrier, then error word
+constexpr size_t kNaBytes = kNaBar + 256;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+  int smem_total = 0;
+};
+constexpr int kNaMaxDevices = 64;
+NoAllocDevice g_na_dev[kNaMaxDevices];
+std::mutex g_na_mutex;
+
+// Once per device, with that device current: the array's device address and the
+// decode kernel's launch limits.
+edge0_status noalloc_setup(int dev, NoAllocDevice** out) {
+  if (dev < 0 || dev >= kNaMaxDevices) return EDGE0_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  NoAllocDevice& d = g_na_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return EDGE0_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return EDGE0_ERR_CUDA;
+    if (prop.major < 10 || !prop.cooperativeLaunch) return EDGE0_ERR_UNSUPPORTED;
+    const int smem = (int)prop.sharedMemPerBlockOptin - 1024;
+    int occ = 0;
+    if (decode_prepare(smem) != cudaSuccess || decode_occupancy(smem, &occ) != cudaSuccess) return EDGE0_ERR_CUDA;
+    if (occ < 1) return EDGE0_ERR_UNSUPPORTED;
+    d.scratch = static_cast<unsigned char*>(p);
+    d.num_sms = prop.multiProcessorCount;
+    d.smem_total = smem;
+    d.ready = true;
+  }
+  *out = &d;
+  return EDGE0_OK;
+}
+
+}  // namespace
+
+extern "C" edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc* desc, const void* x, void* y, int T,
+                                                  int* status_out, edge0_stream_t stream) {
+  if (!desc || T < 0) return EDGE0_ERR_INVALID_ARG;
+  const edge0_moe_desc& d = *desc;
+  if (d.hidden <= 0 || d.hidden % 64 || !shapes_ok(d.latent, d.ffn) || d.top_k < 1 || d.top_k > kMaxTopK ||
+      d.n_experts < d.top_k || d.n_experts % 32)
+    return EDGE0_ERR_INVALID_ARG;
+  if (!d.D || !d.U || !d.router || !d.experts || !d.shared_expert || !aligned(d.D, 16) || !aligned(d.U, 16) ||
+      !aligned(d.router, 16) || !aligned(d.experts, 256) || !aligned(d.shared_expert, 256) ||
+      (d.router_bias && !aligned(d.router_bias, 4)) ||
+      d.expert_stride < edge0_expert_record_bytes(d.latent, d.ffn) || d.expert_stride % 256)
+    return EDGE0_ERR_INVALID_ARG;
+  // sizes beyond what the static scratch holds
+  if (T > kNaMaxT || d.hidden > kNaMaxH || d.latent > kNaMaxL || d.n_experts > kNaMaxE || d.ffn > kNaMaxF)
+    return EDGE0_ERR_UNSUPPORTED;
+  if (T == 0) return EDGE0_OK;
+  if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return EDGE0_ERR_INVALID_ARG;
+  const size_t xy = size_t(T) * d.hidden * 2;
+  const char* xc = static_cast<const char*>(x);
+  const char* yc = static_cast<const char*>(y);
+  if (xc < yc + xy && yc < xc + xy) return EDGE0_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EDGE0_ERR_CUDA;
+  NoAllocDevice* nd = nullptr;
+  const edge0_status st = noalloc_setup(dev, &nd);
+  if (st != EDGE0_OK) return st;
+  unsigned char* s = nd->scratch;
+  cudaStream_t cs = (cudaStream_t)stream;
+
+  // a handle-shaped view of the static scratch (nothing is allocated)
+  Handle view;
+  view.d = d;
+  view.device = dev;
+  view.num_sms = nd->num_sms;
+  view.smem_total = nd->smem_total;
+  view.rd = reinterpret_cast<float*>(s + kNaRD);
+  view.z = reinterpret_cast<float*>(s + kNaZ);
+  view.zh = reinterpret_cast<__half*>(s + kNaZh);
+  view.logits = reinterpret_cast<float*>(s + kNaLg);
+  view.h = reinterpret_cast<float*>(s + kNaH);
+  view.c = reinterpret_cast<float*>(s + kNaC);
+  view.ybuf = reinterpret_cast<__nv_bfloat16*>(s + kNaYb);
+  view.xbuf = reinterpret_cast<__nv_bfloat16*>(s + kNaXb);
+  const int tk = kNaMaxT * kNaMaxK;
+  view.idx = reinterpret_cast<int*>(s + kNaRt);
+  view.w = reinterpret_cast<float*>(s + kNaRt) + tk;
+  view.perm = reinterpret_cast<int*>(s + kNaRt) + 2 * tk;
+  view.pos = reinterpret_cast<int*>(s + kNaRt) + 3 * tk;
+  view.counts = reinterpret_cast<int*>(s + kNaCnt);
+  view.offsets = reinterpret_cast<int*>(s + kNaOff);
+  view.bar = reinterpret_cast<GridBarrier*>(s + kNaBar);
+  view.err = reinterpret_cast<int*>(s + kNaBar + 128);
+  // the array keeps the previous call's contents: the barrier and the error word
+  // must start at zero
+  if (cudaMemsetAsync(s + kNaBar, 0, 256, cs) != cudaSuccess) return EDGE0_ERR_CUDA;
+  // R D for this layer, into the scratch
+  const int H = d.hidden, L = d.latent, E = d.n_experts;
+  fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256, 0, cs>>>(
+      static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), view.rd, E, L, H);
+  if (cudaGetLastError() != cudaSuccess) return EDGE0_ERR_CUDA;
+  DecodeArgs a;
+  fill_decode_args(&view, a, x, y, T);
+  a.layers = nullptr;              // one layer: the kernel reads only a.l0
+  a.l0.dnorm = INFINITY;           // no |z| bound without a host read: z goes to f16 unscaled
+  if (decode_launch(a, nd->num_sms, nd->smem_total, cs) != cudaSuccess) return EDGE0_ERR_CUDA;
+  if (status_out &&
+      cudaMemcpyAsync(status_out, view.err, sizeof(int), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  return EDGE0_OK;
+}

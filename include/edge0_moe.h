@@ -185,6 +185,17 @@ edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t by
                                     edge0_stream_t stream);
 
 /*
+ * C = A B^T on the tensor cores (tcgen05, bf16 in, fp32 accumulate), the dense
+ * GEMM the prefill path uses for D and U:
+ *   A device bf16 [M][K] row-major, B device bf16 [N][K] row-major,
+ *   C device fp32 [M][N] row-major (overwritten); K a multiple of 64.
+ *   err   device int or NULL: a device wait that ran out ORs EDGE0_ERR_TIMEOUT's
+ *         bit (1) into it (bounded waits; the kernel always finishes).
+ */
+edge0_status edge0_gemm_bf16_tn(const void *A, const void *B, float *C, int M, int N, int K,
+                                int *err, edge0_stream_t stream);
+
+/*
  * Post-norm residual between stacked layers (bf16 in, bf16 out):
  *   out[t] = bf16( v / sqrt(mean(v^2) + eps) ),  v = x[t] + y[t]  (fp32 inside)
  * x, y, out device bf16 [T][hidden]; out may alias x or y.

@@ -26,7 +26,7 @@ EXPORTED = (
     "edge0_pack_experts", "edge0_quantize_nvfp4", "edge0_moe_create", "edge0_moe_forward",
     "edge0_moe_debug_routing", "edge0_moe_debug_tensor", "edge0_residual_rmsnorm",
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
-    "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc",
+    "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc", "edge0_gemm_bf16_tn",
 )
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "edge0_status_string": (ctypes.c_char_p, [i]),
             "edge0_moe_destroy": (None, [vp]),
             "edge0_moe_forward_noalloc": (i, [ctypes.POINTER(edge0_moe_desc), vp, vp, i, vp, vp]),
+            "edge0_gemm_bf16_tn": (i, [vp, vp, vp, i, i, i, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -169,6 +170,12 @@ def edge0_moe_debug_routing(handle, idx=None, w=None, counts=None, offsets=None,
 def edge0_moe_debug_tensor(handle, what, dst, nbytes, stream=None):
     _check(lib().edge0_moe_debug_tensor(handle, what, _ptr(dst), nbytes, _stream(stream)),
            "edge0_moe_debug_tensor")
+
+
+def edge0_gemm_bf16_tn(A, B, C, M, N, K, err=None, stream=None):
+    """C = A B^T (bf16 in, fp32 out) on the tcgen05 tensor cores."""
+    _check(lib().edge0_gemm_bf16_tn(_ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(err), _stream(stream)),
+           "edge0_gemm_bf16_tn")
 
 
 def edge0_residual_rmsnorm(x, y, out, T, hidden, eps, stream=None):

@@ -1,0 +1,66 @@
+// Plain dense bf16 GEMM entry point (C fp32 = A B^T) on the tcgen05 kernel of gemm.cuh.
+#include "../../include/edge0_moe.h"
+#include "gemm.cuh"
+#include "tmap.cuh"
+
+namespace edge0 {
+namespace {
+
+struct EpiStoreF32 {
+  float* C;
+  int ldc, N;
+  __device__ __forceinline__ void operator()(int row, int col0, const float* v) const {
+    float* dst = C + size_t(row) * ldc + col0;
+    if (col0 + 32 <= N && (ldc & 3) == 0) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < N) dst[i] = v[i];
+    }
+  }
+};
+
+constexpr int kBN = 256, kStages = 4;
+
+}  // namespace
+
+// Shared by the prefill path: the launch of one dense GEMM with a given epilogue.
+template <class Epi>
+cudaError_t launch_gemm_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N,
+                             int K, int n_split, int* err, const Epi& epi, cudaStream_t s) {
+  using Sm = GemmSmem<kBN, kStages>;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel<kBN, kStages, Epi>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const dim3 grid((N + kBN - 1) / kBN, (M + 127) / 128);
+  gemm_bf16_tn_kernel<kBN, kStages, Epi><<<grid, kGemmThreads, Sm::kBytes, s>>>(ta, tb, tb2, M, K, n_split, err, epi);
+  return cudaGetLastError();
+}
+
+}  // namespace edge0
+
+using namespace edge0;
+
+extern "C" edge0_status edge0_gemm_bf16_tn(const void* A, const void* B, float* C, int M, int N, int K,
+                                           int* err, edge0_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return EDGE0_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return EDGE0_OK;
+  if (!A || !B || !C || K == 0 || K % 64 || (reinterpret_cast<uintptr_t>(A) & 15) ||
+      (reinterpret_cast<uintptr_t>(B) & 15) || (reinterpret_cast<uintptr_t>(C) & 15))
+    return EDGE0_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, uint64_t(K) * 2, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, uint64_t(K) * 2, 64, kBN,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return EDGE0_ERR_CUDA;
+  EpiStoreF32 epi{C, N, N};
+  return launch_gemm_bf16(ta, tb, tb, M, N, K, 1 << 30, err, epi, (cudaStream_t)stream) == cudaSuccess ? EDGE0_OK
+                                                                                              : EDGE0_ERR_CUDA;
+}

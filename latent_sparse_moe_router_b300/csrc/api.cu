@@ -423,6 +423,7 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   hd->pf.idx = hd->idx; hd->pf.w = hd->w; hd->pf.counts = hd->counts; hd->pf.offsets = hd->offsets;
   hd->pf.perm = hd->perm; hd->pf.pos = hd->pos;
   hd->pf.err = hd->err;
+  hd->pf.rd = hd->rd;
   ce = cudaMemset(hd->ws, 0, o_lw);
   if (ce == cudaSuccess) {
     row_l1_max_kernel<<<1, 1024>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, d_dnorm);

@@ -40,6 +40,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -59,6 +63,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, kErrTimeout);
       return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for grids of many CTAs.  Gives up at once when *abort (if given)
+// is non-zero, so that one CTA's timeout ends the waits of every other CTA
+// within microseconds; on running out of time it ORs kErrTimeout into *err (if
+// given) and sets *abort.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_abort(uint64_t* bar, uint32_t parity, int* err, int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  unsigned int spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (abort && ld_relaxed_s32(abort)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (err) atomicOr(err, kErrTimeout);
+        if (abort) atomicExch(abort, 1);
+        return false;
+      }
     }
   }
   return true;

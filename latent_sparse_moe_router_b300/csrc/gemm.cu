@@ -26,23 +26,6 @@ constexpr int kBN = 256, kStages = 4;
 
 }  // namespace
 
-// Shared by the prefill path: the launch of one dense GEMM with a given epilogue.
-template <class Epi>
-cudaError_t launch_gemm_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N,
-                             int K, int n_split, int* err, const Epi& epi, cudaStream_t s) {
-  using Sm = GemmSmem<kBN, kStages>;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel<kBN, kStages, Epi>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const dim3 grid((N + kBN - 1) / kBN, (M + 127) / 128);
-  gemm_bf16_tn_kernel<kBN, kStages, Epi><<<grid, kGemmThreads, Sm::kBytes, s>>>(ta, tb, tb2, M, K, n_split, err, epi);
-  return cudaGetLastError();
-}
-
 }  // namespace edge0
 
 using namespace edge0;
@@ -61,6 +44,8 @@ extern "C" edge0_status edge0_gemm_bf16_tn(const void* A, const void* B, float* 
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return EDGE0_ERR_CUDA;
   EpiStoreF32 epi{C, N, N};
-  return launch_gemm_bf16(ta, tb, tb, M, N, K, 1 << 30, err, epi, (cudaStream_t)stream) == cudaSuccess ? EDGE0_OK
-                                                                                              : EDGE0_ERR_CUDA;
+  return launch_gemm_tn<kBN, kStages>(ta, tb, tb, M, N, K, 1 << 30, err, nullptr, epi, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? EDGE0_OK
+             : EDGE0_ERR_CUDA;
 }

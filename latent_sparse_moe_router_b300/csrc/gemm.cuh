@@ -34,7 +34,8 @@ struct GemmSmem {
 template <int BN, int STAGES, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, int M, int K, int n_split, int* err, Epi epi) {
+                    const __grid_constant__ CUtensorMap tmB2, int M, int K, int n_split, int* err, int* abort,
+                    Epi epi) {
   using S = GemmSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -45,7 +46,12 @@ gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * 128, n0 = blockIdx.x * BN;
   const int nk = K / 64;
+  __shared__ int s_bad;
 
+  // a wait of another launch or CTA that ran out: leave before touching anything
+  if (threadIdx.x == 0) s_bad = (abort && ld_relaxed_s32(abort)) ? 2 : 0;
+  __syncthreads();
+  if (s_bad) return;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(accf, 1);
@@ -64,7 +70,7 @@ gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      mbar_wait(&empty[s], ph ^ 1, err);
+      if (!mbar_wait_abort(&empty[s], ph ^ 1, err, abort)) { s_bad = 1; break; }
       uint8_t* sa = smem + s * S::kStage;
       mbar_arrive_expect_tx(&full[s], S::kStage);
       tma_load_2d(sa, &tmA, kb * 64, m0, &full[s]);
@@ -78,7 +84,7 @@ gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      mbar_wait(&full[s], ph, err);
+      if (!mbar_wait_abort(&full[s], ph, err, abort)) { s_bad = 1; break; }
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + s * S::kStage);
       const uint32_t sb = sa + S::kA;
@@ -89,9 +95,10 @@ gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     mma_commit(accf);
   }
-  // epilogue: every warp reads its 32 TMEM lanes
+  // epilogue: every warp reads its 32 TMEM lanes.  The issuer always commits
+  // accf, so this wait ends once every MMA issued has finished (time limit only).
   __syncwarp();
-  mbar_wait(accf, 0, err);
+  const bool acc_ok = mbar_wait_abort(accf, 0, err, nullptr);
   tc_fence_after();
   const int row = m0 + warp * 32 + lane;
 #pragma unroll 1
@@ -99,11 +106,37 @@ gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint32_t r[32];
     tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + c * 32, r);
     tmem_ld_wait();
-    if (row < M) epi(row, n0 + c * 32, reinterpret_cast<const float*>(r));
+    if (row < M && acc_ok) epi(row, n0 + c * 32, reinterpret_cast<const float*>(r));
   }
   tc_fence_before();
   __syncthreads();
+  // after a wait gave up, bulk copies issued by this CTA may still be landing:
+  // give them a bounded time before the shared memory is released
+  if (s_bad && threadIdx.x == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {}
+  }
+  __syncthreads();
   if (warp == 2) tmem_dealloc(tmem, BN);
+}
+
+// Launch of one GEMM: grid (ceil(N / BN), ceil(M / 128)); A's map has a 64 x 128
+// box, B's and B2's 64 x BN boxes (128-byte swizzle).  K a multiple of 64.
+template <int BN, int STAGES, class Epi>
+cudaError_t launch_gemm_tn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N, int K,
+                           int n_split, int* err, int* abort, const Epi& epi, cudaStream_t s) {
+  using Sm = GemmSmem<BN, STAGES>;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel<BN, STAGES, Epi>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const dim3 grid((N + BN - 1) / BN, (M + 127) / 128);
+  gemm_bf16_tn_kernel<BN, STAGES, Epi><<<grid, kGemmThreads, Sm::kBytes, s>>>(ta, tb, tb2, M, K, n_split, err, abort,
+                                                                               epi);
+  return cudaGetLastError();
 }
 
 }  // namespace edge0

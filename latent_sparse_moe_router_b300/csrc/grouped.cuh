@@ -1,0 +1,69 @@
+// Grouped NVFP4 x bf16 GEMMs of the routed and shared experts (prefill path).
+//
+// The experts of the latent-MoE layer run l -> 640 -> l as SwiGLU FFNs on NVFP4
+// weights ("Edge0-145B · Q3_K" model card, section "Architecture"; NVFP4 per
+// "Edge0-145B en local", introduction).  Tokens are grouped by expert (positions
+// p of the permutation); a work tile is (group g, token tile nt, weight tile mt):
+//   MODE 1 (gate/up): A = 64 gate rows + 64 up rows (f0 = 64 mt), B = BN token
+//     rows of the group, K = l; epilogue h = silu(g_gate * gate) * (g_up * up),
+//     stored bf16 to H[p][f].
+//   MODE 2 (down):    A = 128 latent rows (r0 = 128 mt, 64 row pairs), B = BN rows
+//     of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
+// Per CTA: warp 4 (one lane) streams raw NVFP4 codes (TMA, 4 KB per 64-wide
+// k-step), the tile's E4M3 scales (TMA, once) and the B tiles (TMA, 128-byte
+// swizzle); warps 0-3 dequantise (thread = A row: E2M1 -> f16 by cvt, moved to
+// bf16 exponent range with two logic ops, times the block scale * 2^112 in one
+// bf16x2 multiply, all exact) into 128-byte-swizzled bf16 A tiles; warp 5 (one
+// lane) issues tcgen05.mma M=128, N = the tile's token count rounded to 16,
+// K=16 into TMEM; at the end warps 0-3 read TMEM and run the epilogue through a
+// shared-memory transpose so global stores are whole rows.
+#pragma once
+
+#include "tc.cuh"
+
+namespace edge0 {
+
+constexpr int kGgThreads = 192;
+constexpr int kGgBN = 256;      // token tile
+constexpr int kGgS = 3;         // A / B stages
+constexpr int kGgR = 4;         // raw code stages
+
+struct GgSmem {
+  static constexpr int kA = 128 * 64 * 2;        // 16 KB
+  static constexpr int kB = kGgBN * 64 * 2;      // 32 KB
+  static constexpr int kRaw = 128 * 32;          // 4 KB
+  static constexpr int kSc = 16384;              // scales of the tile (<= 128 rows x 128 B)
+  static constexpr int offA = 0;
+  static constexpr int offB = offA + kGgS * kA;
+  static constexpr int offRaw = offB + kGgS * kB;
+  static constexpr int offSc = offRaw + kGgR * kRaw;
+  static constexpr int offBar = offSc + kSc;
+  static constexpr int kBytes = offBar + 1024 + 1024;  // barriers + alignment slack
+};
+
+struct GgParams {
+  int mode;                 // 1 gate/up, 2 down
+  int T, TK, L, F, E;
+  int mtiles;               // weight tiles per group (F/64 or L/128)
+  const int* counts;        // [E]   tokens per routed expert
+  const int* offsets;       // [E+1] first position of each routed expert
+  const int* tprefix;       // [E+2] first token tile of each group (group E = shared)
+  const uint8_t* experts;   // records (for the fp32 per-matrix scales)
+  unsigned long long stride;
+  const uint8_t* shared;
+  __nv_bfloat16* out;       // H [TK+T][F] (mode 1) or O [TK+T][L] (mode 2)
+  int out_ld;
+  int* err;
+  int* abort;               // set when any wait gives up; every CTA then winds down
+};
+
+struct GgMaps {
+  CUtensorMap a_codes;      // routed records: 3-D (bytes of a row, rows, expert)
+  CUtensorMap a_scales;
+  CUtensorMap s_codes;      // shared record: 2-D
+  CUtensorMap s_scales;
+  CUtensorMap b_routed;     // mode 1: gathered z rows [TK][L]; mode 2: H [TK+T][F]
+  CUtensorMap b_shared;     // mode 1: z rows [T][L]; mode 2: H again (shared rows from TK)
+};
+
+}  // namespace edge0

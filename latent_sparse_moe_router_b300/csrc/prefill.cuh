@@ -1,8 +1,10 @@
-// Prefill path (T > 16) of the latent-MoE layer.
+// Prefill path (T > 16) of the latent-MoE layer: dense tensor-core GEMMs for the
+// latent and router projections and for U, routing and permutation kernels, and
+// grouped NVFP4 tensor-core GEMMs for the experts.
 #pragma once
 
 #include "../../include/edge0_moe.h"
-#include "common.cuh"
+#include "grouped.cuh"
 
 namespace edge0 {
 
@@ -12,7 +14,22 @@ struct PrefillWorkspace {
   int* idx = nullptr; float* w = nullptr; int* counts = nullptr; int* offsets = nullptr;
   int* perm = nullptr; int* pos = nullptr;
   int* err = nullptr;
-  void* scratch = nullptr;
+  const float* rd = nullptr;        // folded router R D, fp32 [E][hidden] (handle-owned)
+  // prefill buffers (carved from the handle's workspace)
+  __nv_bfloat16* rdcat = nullptr;   // [2E][hidden]: rows 2e, 2e+1 = bf16 high / low parts of R D row e
+  __nv_bfloat16* zb = nullptr;      // [T][latent]  z rounded to bf16
+  float* logits = nullptr;          // [T][E]
+  int* chunk_cnt = nullptr;         // [T/64][E] per-chunk expert counts, then per-chunk bases
+  int* tprefix = nullptr;           // [E+2] token-tile prefix of the expert groups (+ shared)
+  __nv_bfloat16* zg = nullptr;      // [T K][latent] z rows in expert-grouped order
+  __nv_bfloat16* hb = nullptr;      // [T K + T][ffn] SwiGLU activations (routed, then shared)
+  __nv_bfloat16* ob = nullptr;      // [T K + T][latent] expert outputs (routed, then shared)
+  __nv_bfloat16* cb = nullptr;      // [T][latent] combined latent
+  __nv_bfloat16* scratch = nullptr; // [T][hidden] layer output for stacked calls
+  int* abort = nullptr;             // per-forward abort word of the bounded waits
+  // tensor maps fixed for the handle's lifetime
+  CUtensorMap m_D, m_rdcat, m_U, m_cb;
+  GgMaps maps1, maps2;
 };
 
 size_t prefill_workspace_bytes(const edge0_moe_desc& d, int max_tokens);

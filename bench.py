@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -28,16 +29,38 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     # name: latent, T, seed, layers per step, zipf pattern, instances rotated
-    "layer145b_t1": dict(latent=1792, T=1, seed=0, layers=1, zipf=(0.0,), instances=16,
+    "layer145b_t1": dict(kind="decode", latent=1792, T=1, seed=0, layers=1, zipf=(0.0,), instances=16,
                          desc="one Edge0-145B latent-MoE layer, decode T=1"),
-    "layer120b_t4": dict(latent=1280, T=4, seed=1, layers=1, zipf=(0.0,), instances=16,
+    "layer120b_t4": dict(kind="decode", latent=1280, T=4, seed=1, layers=1, zipf=(0.0,), instances=16,
                          desc="one Edge0-120B latent-MoE layer, speculative-verify batch T=4"),
-    "stack48_145b_t1": dict(latent=1792, T=1, seed=2, layers=48, zipf=(0.0,), instances=1,
+    "stack48_145b_t1": dict(kind="decode", latent=1792, T=1, seed=2, layers=48, zipf=(0.0,), instances=1,
                             desc="48 Edge0-145B layers (all 48x512 experts resident), decode T=1"),
+    "layer145b_t4096_zipf": dict(kind="prefill", latent=1792, T=4096, seed=3, layers=1, zipf=(1.1,),
+                                 instances=2, cpu_T=32,
+                                 desc="one Edge0-145B layer, prefill T=4096, Zipf(1.1) router bias"),
+    "prefill4x145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=4,
+                                 zipf=(0.0, 1.1, 0.0, 1.1), instances=1, cpu_T=32,
+                                 desc="4 Edge0-145B layers, prefill T=16384, uniform/Zipf(1.1) alternating"),
 }
-DEFAULT_WORKLOAD = "layer145b_t1"
+DEFAULT_WORKLOAD = "prefill4x145b_t16384"
 HIDDEN, E, K, F = 2560, 512, 10, 640
 METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofline"
+MIN_TIMED_S = 2.0
+
+
+def flops_per_token_layer(latent):
+    """Algorithmic FLOPs of one token through one layer: D, router, k routed and
+    the shared SwiGLU expert, U (2 per multiply-add)."""
+    return 2 * HIDDEN * latent + 2 * latent * E + (K + 1) * 3 * 2 * latent * F + 2 * latent * HIDDEN
+
+
+def stage_flops(latent, T):
+    """Algorithmic FLOPs per launch of the prefill stages that are contractions."""
+    TK = T * K
+    return {"xz_gemm": 2 * T * HIDDEN * latent + 2 * T * latent * E,
+            "gate_up_grouped": 2 * (TK + T) * latent * 2 * F,
+            "down_grouped": 2 * (TK + T) * F * latent,
+            "u_gemm": 2 * T * latent * HIDDEN}
 
 
 def record_bytes(latent):
@@ -161,13 +184,13 @@ def cpu_baseline(wl, seconds=12.0):
     spec = synth.LayerSpec(seed=wl["seed"], layer=0, latent=wl["latent"], zipf=wl["zipf"][0])
     inp = synth.make_layer(spec)
     lay = moe.Layer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn, spec.top_k)
-    T = wl["T"]
+    T = wl.get("cpu_T", wl["T"])           # prefill: a bounded token sample of the layer
     done_tokens, t0, it = 0, time.perf_counter(), 0
     while True:
         inp._cache.clear()                       # each sample dequantises its experts again
         x = synth.tokens_bf16(1000 + it, T, HIDDEN)
         moe.layer_forward(lay, x)
-        done_tokens += T * wl["layers"] and T
+        done_tokens += T
         it += 1
         el = time.perf_counter() - t0
         if el > seconds or it >= 64:
@@ -175,8 +198,9 @@ def cpu_baseline(wl, seconds=12.0):
     # per-layer tokens: each sample runs one layer; a stack step runs `layers` of them
     tok_per_s = done_tokens / el / wl["layers"]
     return {"value": tok_per_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{it} forward(s) of one layer at T={T} (fresh expert dequantisation each), "
-                      f"{el:.1f} s; stack workloads scaled by 1/{wl['layers']} layers"}
+            "sample": f"{it} forward(s) of one layer at T={T} of the workload's layer 0 (fresh expert "
+                      f"dequantisation each), {el:.1f} s; tokens/s through the step = per-layer rate / "
+                      f"{wl['layers']} layer(s)"}
 
 
 # ------------------------------------------------------------------ our implementation
@@ -193,7 +217,59 @@ def build_instances(wl, n_inst, max_tokens):
     return insts
 
 
-def run_ours(args, wl, rank, world, local):
+def timed_region(step, args, stream, world, local, est_ms=None):
+    """Warm-up, capture of the K timed steps in a CUDA graph, and the replay of that
+    graph enough times (>= MIN_TIMED_S) between events on the launching stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+    # per-step estimate from a few direct steps (sets the replay count)
+    t0 = time.perf_counter()
+    n_est = 2
+    with torch.cuda.stream(stream):
+        for i in range(n_est):
+            step(i, stream)
+    stream.synchronize()
+    est = (time.perf_counter() - t0) / n_est
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(args.warmup + i, stream)
+        stream.synchronize()
+        graph.replay()                      # one untimed replay (the graph's first launch)
+        stream.synchronize()
+    except Exception as e:                  # graph capture unavailable: launch directly
+        print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
+        graph = None
+        torch.cuda.synchronize()
+    reps = args.repeat if args.repeat else max(1, int(math.ceil(MIN_TIMED_S / max(est * args.steps, 1e-6))))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for r in range(reps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    for i in range(args.steps):
+                        step(args.warmup + i, stream)
+            ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    del graph
+    return el_ms, args.steps * reps, reps, clk.summary()
+
+
+def run_decode(args, wl, rank, world, local):
     import numpy as np
     import torch
     import synth
@@ -215,12 +291,7 @@ def run_ours(args, wl, rank, world, local):
             j = i % n_inst
             ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, s)
         launches_per_step = 1
-        # distinct experts per instance (for the algorithmic bytes)
         distinct = []
-        with torch.cuda.stream(stream):
-            for j in range(n_inst):
-                step(j, stream)
-        stream.synchronize()
         for j in range(n_inst):
             ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, stream)
             stream.synchronize()
@@ -246,64 +317,20 @@ def run_ours(args, wl, rank, world, local):
             j = i % n_tok
             ext.edge0_moe_stack_forward(handles, xs_all[j:j + 1], ys_all[j:j + 1], 1, 1e-6, s)
         launches_per_step = 1
-        bytes_per_step = None      # computed below from the routing of the last layer run
-        distinct_total = []
-        for j in range(4):
-            for l, d in enumerate(insts):
-                pass
         bytes_per_step = n_layers * decode_algorithmic_bytes(L, 1, K)
         work_note = "48 layers x (D + U + router + 10 routed + 1 shared record) per token"
 
-    # warm-up, then capture the timed steps in a CUDA graph
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i, stream)
-    stream.synchronize()
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
-                step(args.warmup + i, stream)
-        stream.synchronize()
-        graph.replay()                      # one untimed replay (the graph's first launch)
-        stream.synchronize()
-    except Exception as e:                  # graph capture unavailable: launch directly
-        print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
-        graph = None
-        torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        time.sleep(0.3)
-        reps = max(1, int(args.repeat))
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for r in range(reps):
-                if graph is not None:
-                    graph.replay()
-                else:
-                    for i in range(args.steps):
-                        step(args.warmup + i, stream)
-            ev1.record(stream)
-        stream.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    steps_done = args.steps * reps
+    el_ms, steps_done, reps, clocks = timed_region(step, args, stream, world, local)
     ms_per_step = el_ms / steps_done
-    tokens_per_step = T * world
-    value = tokens_per_step / (ms_per_step / 1e3) / (1 if n_layers == 1 else 1)
-    # roofline of the dominant (only) kernel: algorithmic bytes / launch duration
+    value = T * world / (ms_per_step / 1e3)
+    # the step is one kernel launch: its duration is the step time
     achieved_gbs = bytes_per_step / (ms_per_step / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved_gbs / hbm, 4), "traffic": None,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
-            "bytes_per_launch": bytes_per_step, "note": work_note}
+            "kernel": "moe_decode_kernel", "bytes_per_launch": bytes_per_step, "note": work_note}
 
     # e2e through the C ABI with pinned host buffers: H2D x, forward, D2H y, per step
-    e2e = None
     if n_layers == 1:
         hx = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
         hy = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
@@ -351,18 +378,148 @@ def run_ours(args, wl, rank, world, local):
     for d in insts:
         d.close()
     return dict(value=value, ms_per_step=ms_per_step, roofline=roof, e2e=e2e,
-                gpu_launches=launches_per_step * steps_done, clocks=clk.summary(), reps=reps)
+                gpu_launches=launches_per_step * steps_done, clocks=clocks, steps_done=steps_done)
+
+
+def run_prefill(args, wl, rank, world, local):
+    import numpy as np
+    import torch
+    import synth
+    import latent_sparse_moe_router_b300 as ext
+    from synth import device
+
+    torch.cuda.set_device(local)
+    T, L, n_layers = wl["T"], wl["latent"], wl["layers"]
+    hbm, bf16, bf16_s, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    n_inst = n_layers if n_layers > 1 else wl["instances"]
+    insts = []
+    for l in range(n_inst):
+        spec = synth.LayerSpec(seed=wl["seed"], layer=l, latent=L, zipf=wl["zipf"][l % len(wl["zipf"])])
+        insts.append(device.DeviceLayer(synth.make_layer(spec), max_tokens=T))
+    torch.cuda.synchronize()
+    handles = [d.handle for d in insts]
+    n_x = 1 if n_layers > 1 else n_inst
+    xs = [device.bf16_tensor(synth.tokens_bf16(wl["seed"] * 1000 + rank * 100 + i, T, HIDDEN)) for i in range(n_x)]
+    ys = [torch.empty_like(x) for x in xs]
+    if n_layers > 1:
+        def step(i, s):
+            ext.edge0_moe_stack_forward(handles, xs[0], ys[0], T, 1e-6, s)
+        # per layer: the prefill kernels plus the residual norm
+        launches_per_step = n_layers * (ext.EDGE0_PREFILL_STAGES + 1)
+    else:
+        def step(i, s):
+            j = i % n_inst
+            ext.edge0_moe_forward(handles[j], xs[j], ys[j], T, s)
+        launches_per_step = ext.EDGE0_PREFILL_STAGES
+
+    el_ms, steps_done, reps, clocks = timed_region(step, args, stream, world, local)
+    ms_per_step = el_ms / steps_done
+    value = T * world / (ms_per_step / 1e3)          # tokens through the whole step per second
+    step_flops = T * n_layers * flops_per_token_layer(L)
+    step_tflops = step_flops / (ms_per_step / 1e3) / 1e12
+
+    # per-kernel durations: the library's stage events on the launching stream,
+    # over a few direct steps after the timed region
+    for h in handles:
+        ext.edge0_moe_profile_stages(h, True)
+    n_prof = max(3, min(args.steps, 8))
+    sums = np.zeros(ext.EDGE0_PREFILL_STAGES)
+    n_launch = 0
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            if n_layers > 1:
+                for l, h in enumerate(handles):
+                    # every layer on the step's input x (per-layer stage times, read back per call)
+                    ext.edge0_moe_forward(h, xs[0], ys[0], T, stream)
+                    sums += np.array(ext.edge0_moe_stage_times(h))
+                    n_launch += 1
+            else:
+                j = i % n_inst
+                ext.edge0_moe_forward(handles[j], xs[j], ys[j], T, stream)
+                sums += np.array(ext.edge0_moe_stage_times(handles[j]))
+                n_launch += 1
+    for h in handles:
+        ext.edge0_moe_profile_stages(h, False)
+    stage_ms = sums / n_launch
+    names = ext.PREFILL_STAGE_NAMES
+    top = int(np.argmax(stage_ms))
+    sflops = stage_flops(L, T)
+    tname = names[top]
+    if tname in sflops:
+        ach = sflops[tname] / (stage_ms[top] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16_s, "unit": "TFLOP/s",
+                "frac": round(ach / bf16_s, 4), "traffic": None, "kernel": tname,
+                "flops_per_launch": sflops[tname],
+                "peak_kind": f"{peak_kind} cuBLAS bf16 sustained (kernel timed inside the step); "
+                             f"frac of burst {bf16} = {ach / bf16:.4f}"}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None, "traffic": None,
+                "kernel": tname, "note": "dominant stage is not a contraction"}
+    roof["step"] = {"tflops": round(step_tflops, 1), "frac_sustained": round(step_tflops / bf16_s, 4),
+                    "frac_burst": round(step_tflops / bf16, 4), "flops_per_step": step_flops,
+                    "flops_per_token_layer": flops_per_token_layer(L)}
+    stages = {n: round(float(m), 4) for n, m in zip(names, stage_ms)}
+    stages["timed_layer_ms_sum"] = round(float(stage_ms.sum()), 4)
+
+    # e2e through the C ABI with pinned host buffers: H2D x, forward, D2H y, per step
+    hx = torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+    hy = torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(xs[0].cpu())
+    n_e2e = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_e2e):
+            xs[0].copy_(hx, non_blocking=True)
+            if n_layers > 1:
+                ext.edge0_moe_stack_forward(handles, xs[0], ys[0], T, 1e-6, stream)
+            else:
+                ext.edge0_moe_forward(handles[0], xs[0], ys[0], T, stream)
+            hy.copy_(ys[0], non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+    stream.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+    e2e = {"value": round(T * world / (e_ms / 1e3), 1), "unit": "tok/s",
+           "h2d_bytes_per_step": T * HIDDEN * 2, "d2h_bytes_per_step": T * HIDDEN * 2}
+    errs = [ext.edge0_moe_get_error(h) for h in handles]
+    assert all(e == ext.EDGE0_OK for e in errs), f"device wait ran out: {errs}"
+    for d in insts:
+        d.close()
+    return dict(value=value, ms_per_step=ms_per_step, roofline=roof, e2e=e2e,
+                gpu_launches=launches_per_step * steps_done, clocks=clocks, steps_done=steps_done,
+                stages=stages, layer_tok_s=value * n_layers)
+
+
+def config_of(name, wl, world):
+    if wl["kind"] == "prefill":
+        l2 = (f"inputs larger than L2: x {wl['T'] * HIDDEN * 2 / 1e6:.0f} MB per layer input, "
+              f"expert records ~1 GB per layer, activations ~{wl['T'] * K * (wl['latent'] * 4 + F * 2) * 2 / 1e9:.1f} GB")
+    elif wl["layers"] == 1:
+        l2 = (f"rotating {wl['instances']} independent layer instances "
+              f"(~{wl['instances'] * decode_algorithmic_bytes(wl['latent'], wl['T'], K * wl['T']) / 1e6:.0f} MB touched) > 126 MB L2")
+    else:
+        l2 = "48-layer stack, 47.6 GB of records > 126 MB L2"
+    return {"workload": name, "desc": wl["desc"], "hidden": HIDDEN, "latent": wl["latent"],
+            "experts": E, "top_k": K, "ffn": F, "T": wl["T"], "layers_per_step": wl["layers"],
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--repeat", type=int, default=20, help="graph replays inside the timed region")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--repeat", type=int, default=0,
+                    help="graph replays inside the timed region (0: enough for >= 2 s)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the T=1 decode line that the default prefill run also reports")
     ap.add_argument("--instances", type=int, default=0,
                     help="override the number of rotated layer instances (profiling runs)")
     args = ap.parse_args()
@@ -371,13 +528,7 @@ def main():
     if args.instances:
         wl["instances"] = args.instances
     rank, world, local = dist_setup(args.gpus)
-
-    config = {"workload": args.workload, "desc": wl["desc"], "hidden": HIDDEN, "latent": wl["latent"],
-              "experts": E, "top_k": K, "ffn": F, "T": wl["T"], "layers_per_step": wl["layers"],
-              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-              "l2": (f"rotating {wl['instances']} independent layer instances "
-                     f"(~{wl['instances'] * decode_algorithmic_bytes(wl['latent'], wl['T'], K * wl['T']) / 1e6:.0f} MB touched) > 126 MB L2"
-                     if wl["layers"] == 1 else "48-layer stack, 47.6 GB of records > 126 MB L2")}
+    config = config_of(args.workload, wl, world)
 
     if args.impl == "reference":
         if rank != 0:
@@ -400,17 +551,32 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    r = run_ours(args, wl, rank, world, local)
+    run = run_prefill if wl["kind"] == "prefill" else run_decode
+    r = run(args, wl, rank, world, local)
+    extra = {}
+    if wl["kind"] == "prefill":
+        extra["stages_ms_per_layer"] = r["stages"]
+        extra["layer_tok_s"] = round(r["layer_tok_s"], 1)
+    # the metric's other half (T = 1 decode) on the same run
+    if args.workload == DEFAULT_WORKLOAD and not args.no_decode:
+        dwl = dict(WORKLOADS["layer145b_t1"])
+        import torch
+        torch.cuda.empty_cache()
+        dr = run_decode(args, dwl, rank, world, local)
+        extra["decode_t1"] = {"workload": "layer145b_t1", "value": round(dr["value"], 1), "unit": "tok/s",
+                              "ms_per_step": round(dr["ms_per_step"], 6), "roofline": dr["roofline"],
+                              "e2e": dr["e2e"], "clocks": dr["clocks"], "gpu_launches": dr["gpu_launches"]}
     if rank != 0:
         return
     cb = None if args.no_cpu_baseline else cpu_baseline(wl)
     line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tok/s", "n_gpus": world,
-            "steps": args.steps * r["reps"], "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 6),
+            "steps": r["steps_done"], "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4 weights, bf16/f16 activations, fp32 accumulate",
+            "dtype": "nvfp4 weights; bf16 operands on the tensor cores (f16 in the decode GEMV); fp32 accumulate",
             "data": "synthetic (seeded; random NVFP4 experts and N(0,1/fan_in) bf16 projections)",
             "config": config, "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
             "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
+    line.update(extra)
     print(json.dumps(line), flush=True)
 
 

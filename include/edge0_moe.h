@@ -177,9 +177,11 @@ edge0_status edge0_moe_debug_routing(void *handle, int *idx, float *w, int *coun
 
 /*
  * Copy an intermediate of the last forward (for stage-by-stage parity):
- *   what = 0: z fp32 [T][latent]; 1: router logits fp32 [T][n_experts]
- *   (2: combined latent c fp32 [T][latent]).  dst device, `bytes` >= size.
- * Returns UNSUPPORTED if the last forward's path does not materialise it.
+ *   what = 0: latent z [T][latent]; 1: router logits fp32 [T][n_experts];
+ *   2: combined latent c [T][latent].  z and c are fp32 after a decode
+ *   forward (T <= 16) and bf16 after a prefill forward (T > 16), the form
+ *   in which the experts and U consume them.  dst device, `bytes` >= size.
+ * Returns UNSUPPORTED if no forward has run yet, INVALID_ARG for other `what`.
  */
 edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t bytes,
                                     edge0_stream_t stream);
@@ -248,6 +250,23 @@ edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, c
  */
 edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc *desc, const void *x, void *y, int T,
                                        int *status_out, edge0_stream_t stream);
+
+/*
+ * Stage timing of the prefill path, for profiling.  While enabled, each
+ * prefill forward on the handle records a CUDA event on its stream before its
+ * first kernel and after each of its EDGE0_PREFILL_STAGES kernels:
+ *   0 x -> [z | logits] GEMM, 1 top-k + chunk histogram, 2 chunk scan,
+ *   3 expert offsets, 4 scatter, 5 z-row gather, 6 gate/up + SwiGLU grouped
+ *   GEMM, 7 down grouped GEMM, 8 combine, 9 U GEMM.
+ * edge0_moe_stage_times waits for the last forward's final event and writes
+ * the n = min(max, EDGE0_PREFILL_STAGES) stage durations in milliseconds to
+ * host ms[0..n); *n_out (if not NULL) = n.  UNSUPPORTED if the last forward
+ * was not a timed prefill forward.  Enabling adds event records between the
+ * kernels and nothing else; it is off by default.
+ */
+#define EDGE0_PREFILL_STAGES 10
+edge0_status edge0_moe_profile_stages(void *handle, int enable);
+edge0_status edge0_moe_stage_times(void *handle, float *ms, int max, int *n_out);
 
 /*
  * Synchronise with the device and return the handle's device error word

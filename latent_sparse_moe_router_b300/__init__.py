@@ -27,7 +27,12 @@ EXPORTED = (
     "edge0_moe_debug_routing", "edge0_moe_debug_tensor", "edge0_residual_rmsnorm",
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
     "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc", "edge0_gemm_bf16_tn",
+    "edge0_moe_profile_stages", "edge0_moe_stage_times",
 )
+
+EDGE0_PREFILL_STAGES = 10
+PREFILL_STAGE_NAMES = ("xz_gemm", "topk_hist", "scan_chunks", "offsets", "scatter", "gather_rows",
+                       "gate_up_grouped", "down_grouped", "combine", "u_gemm")
 
 
 class Edge0Error(RuntimeError):
@@ -75,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_destroy": (None, [vp]),
             "edge0_moe_forward_noalloc": (i, [ctypes.POINTER(edge0_moe_desc), vp, vp, i, vp, vp]),
             "edge0_gemm_bf16_tn": (i, [vp, vp, vp, i, i, i, vp, vp]),
+            "edge0_moe_profile_stages": (i, [vp, i]),
+            "edge0_moe_stage_times": (i, [vp, vp, i, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -211,6 +218,19 @@ def edge0_moe_forward_noalloc(hidden, latent, n_experts, top_k, ffn, D, U, route
                        _ptr(router_bias), _ptr(experts), expert_stride, _ptr(shared_expert))
     _check(lib().edge0_moe_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(y), T, _ptr(status),
                                            _stream(stream)), "edge0_moe_forward_noalloc")
+
+
+def edge0_moe_profile_stages(handle, enable: bool):
+    _check(lib().edge0_moe_profile_stages(handle, int(bool(enable))), "edge0_moe_profile_stages")
+
+
+def edge0_moe_stage_times(handle):
+    """Per-stage milliseconds of the last (timed) prefill forward, as a list."""
+    buf = (ctypes.c_float * EDGE0_PREFILL_STAGES)()
+    n = ctypes.c_int()
+    _check(lib().edge0_moe_stage_times(handle, ctypes.cast(buf, ctypes.c_void_p), EDGE0_PREFILL_STAGES,
+                                       ctypes.byref(n)), "edge0_moe_stage_times")
+    return [float(buf[i]) for i in range(n.value)]
 
 
 def edge0_moe_get_error(handle) -> int:

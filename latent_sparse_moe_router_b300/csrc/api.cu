@@ -587,6 +587,19 @@ edge0_status edge0_moe_stack_forward_trace(void* const* handles, int n_layers, c
   return stack_impl(handles, n_layers, x, y, T, eps, trace_x, trace_y, stream);
 }
 
+edge0_status edge0_moe_profile_stages(void* handle, int enable) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  return cuda_status(prefill_profile(&hd->pf, enable != 0));
+}
+
+edge0_status edge0_moe_stage_times(void* handle, float* ms, int max, int* n_out) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !ms || max < 0) return EDGE0_ERR_INVALID_ARG;
+  if (hd->last_path != 2) return EDGE0_ERR_UNSUPPORTED;
+  return prefill_stage_times(&hd->pf, ms, max, n_out);
+}
+
 edge0_status edge0_moe_get_error(void* handle) {
   Handle* hd = static_cast<Handle*>(handle);
   if (!hd) return EDGE0_ERR_INVALID_ARG;

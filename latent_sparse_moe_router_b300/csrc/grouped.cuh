@@ -9,35 +9,46 @@
 //     stored bf16 to H[p][f].
 //   MODE 2 (down):    A = 128 latent rows (r0 = 128 mt, 64 row pairs), B = BN rows
 //     of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
-// Per CTA: warp 4 (one lane) streams raw NVFP4 codes (TMA, 4 KB per 64-wide
-// k-step), the tile's E4M3 scales (TMA, once) and the B tiles (TMA, 128-byte
-// swizzle); warps 0-3 dequantise (thread = A row: E2M1 -> f16 by cvt, moved to
-// bf16 exponent range with two logic ops, times the block scale * 2^112 in one
-// bf16x2 multiply, all exact) into 128-byte-swizzled bf16 A tiles; warp 5 (one
-// lane) issues tcgen05.mma M=128, N = the tile's token count rounded to 16,
-// K=16 into TMEM; at the end warps 0-3 read TMEM and run the epilogue through a
-// shared-memory transpose so global stores are whole rows.
+// Persistent CTAs (one per SM) walk the tiles in index order with a stride of
+// the grid, tile = (token tile, weight tile) with the weight tile fastest, so
+// the CTAs working at one time share a few token tiles through L2.  Warp roles:
+//   warp 0 (one lane): TMA producer - the tile's E4M3 scales (double-buffered),
+//     raw NVFP4 codes (4 KB per 64-wide k-step) and the B rows the tile needs
+//     (64-row boxes, 128-byte swizzle);
+//   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
+//     K=16, into one of two TMEM accumulators of 256 columns;
+//   warps 2-9: dequantisation, two threads per A row (E2M1 -> f16 by cvt, moved
+//     to the bf16 exponent range with shift/mask, times the block scale * 2^112
+//     in one bf16x2 multiply, all exact) into 128-byte-swizzled bf16 A tiles;
+//   warps 10-13: epilogue of the previous accumulator (TMEM -> registers ->
+//     shared-memory transpose -> whole-row global stores) while the next tile's
+//     main loop runs.
 #pragma once
 
 #include "tc.cuh"
 
 namespace edge0 {
 
-constexpr int kGgThreads = 192;
-constexpr int kGgBN = 256;      // token tile
-constexpr int kGgS = 3;         // A / B stages
-constexpr int kGgR = 4;         // raw code stages
+constexpr int kGgThreads = 448;  // 14 warps
+constexpr int kGgDqWarp0 = 2;     // dequantisation warps 2..9
+constexpr int kGgDqThreads = 256;
+constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..13
+constexpr int kGgBN = 256;        // token tile
+constexpr int kGgS = 3;           // A / B stages
+constexpr int kGgR = 4;           // raw code stages
 
 struct GgSmem {
   static constexpr int kA = 128 * 64 * 2;        // 16 KB
   static constexpr int kB = kGgBN * 64 * 2;      // 32 KB
   static constexpr int kRaw = 128 * 32;          // 4 KB
-  static constexpr int kSc = 16384;              // scales of the tile (<= 128 rows x 128 B)
+  static constexpr int kSc = 16384;              // scales of one tile (<= 128 rows x 128 B)
+  static constexpr int kEpi = 17408;             // epilogue transpose buffers
   static constexpr int offA = 0;
   static constexpr int offB = offA + kGgS * kA;
   static constexpr int offRaw = offB + kGgS * kB;
   static constexpr int offSc = offRaw + kGgR * kRaw;
-  static constexpr int offBar = offSc + kSc;
+  static constexpr int offEpi = offSc + 2 * kSc;
+  static constexpr int offBar = offEpi + kEpi;
   static constexpr int kBytes = offBar + 1024 + 1024;  // barriers + alignment slack
 };
 

@@ -321,7 +321,7 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ ob, const int* 
   *reinterpret_cast<uint4*>(cb + size_t(t) * L + j) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int bound_tiles, cudaStream_t s) {
+cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int num_sms, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     const cudaError_t e =
@@ -329,9 +329,8 @@ cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int bound_tile
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const long grid = long(bound_tiles) * p.mtiles;
-  if (grid <= 0) return cudaSuccess;
-  grouped_nvfp4_kernel<<<unsigned(grid), kGgThreads, GgSmem::kBytes, s>>>(maps, p);
+  // persistent: one CTA per SM walks the tiles (their count is read on the device)
+  grouped_nvfp4_kernel<<<num_sms, kGgThreads, GgSmem::kBytes, s>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -400,15 +399,15 @@ cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_
   ok &= make_tmap_3d(&pf->maps1.a_scales, ex, U8, gu_row, F, E, gu_row, d.expert_stride, L / 16, 64, 1, NS);
   ok &= make_tmap_2d(&pf->maps1.s_codes, sh, U8, 1, F, gu_row, gu_row, 32, 64, NS);
   ok &= make_tmap_2d(&pf->maps1.s_scales, sh, U8, 1, F, gu_row, gu_row, L / 16, 64, NS);
-  ok &= make_tmap_2d(&pf->maps1.b_routed, pf->zg, BF, 2, TK, L, uint64_t(L) * 2, 64, kGgBN, SW);
-  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zb, BF, 2, T, L, uint64_t(L) * 2, 64, kGgBN, SW);
+  ok &= make_tmap_2d(&pf->maps1.b_routed, pf->zg, BF, 2, TK, L, uint64_t(L) * 2, 64, kGgBBox, SW);
+  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zb, BF, 2, T, L, uint64_t(L) * 2, 64, kGgBBox, SW);
   // down: records' D blocks [E][L/2 row pairs][9F/8 bytes]
   ok &= make_tmap_3d(&pf->maps2.a_codes, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, 32, 64, 1, NS);
   ok &= make_tmap_3d(&pf->maps2.a_scales, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, F / 8, 64, 1,
                      NS);
   ok &= make_tmap_2d(&pf->maps2.s_codes, sh + d_block, U8, 1, L / 2, d_pair, d_pair, 32, 64, NS);
   ok &= make_tmap_2d(&pf->maps2.s_scales, sh + d_block, U8, 1, L / 2, d_pair, d_pair, F / 8, 64, NS);
-  ok &= make_tmap_2d(&pf->maps2.b_routed, pf->hb, BF, 2, TK + T, F, uint64_t(F) * 2, 64, kGgBN, SW);
+  ok &= make_tmap_2d(&pf->maps2.b_routed, pf->hb, BF, 2, TK + T, F, uint64_t(F) * 2, 64, kGgBBox, SW);
   pf->maps2.b_shared = pf->maps2.b_routed;
   return ok ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -424,37 +423,47 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return EDGE0_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(pf->abort, 0, sizeof(int), s);
+  pf->timed = false;
+  int stage = 0;
+  auto mark = [&]() {
+    if (pf->profile && e == cudaSuccess) e = cudaEventRecord(pf->events[stage++], s);
+  };
+  mark();
   // 1. x -> zb, logits
   if (e == cudaSuccess)
     e = launch_gemm_tn<kPfBN, kPfStages>(mx, pf->m_D, pf->m_rdcat, T, L + 2 * E, H, L, pf->err, pf->abort,
                                          EpiXZ{pf->zb, pf->logits, d.router_bias, L, E}, s);
+  mark();
   // 2-4. routing and permutation
   if (e == cudaSuccess) {
     topk_hist_kernel<<<nch, 256, (8 * E + E) * 4, s>>>(pf->logits, T, E, K, pf->idx, pf->w, pf->chunk_cnt);
     e = cudaGetLastError();
   }
+  mark();
   if (e == cudaSuccess) {
     scan_chunks_kernel<<<E / 32, dim3(32, 32), 0, s>>>(pf->chunk_cnt, nch, E, pf->counts);
     e = cudaGetLastError();
   }
+  mark();
   if (e == cudaSuccess) {
     offsets_kernel<<<1, 1024, 0, s>>>(pf->counts, E, T, pf->offsets, pf->tprefix);
     e = cudaGetLastError();
   }
+  mark();
   if (e == cudaSuccess) {
     scatter_kernel<<<(nch + 7) / 8, 256, 8 * E * 4, s>>>(pf->idx, pf->chunk_cnt, pf->offsets, T, K, E, nch, pf->perm,
                                                          pf->pos);
     e = cudaGetLastError();
   }
+  mark();
   // 5. grouped z rows
   if (e == cudaSuccess) {
     const int blocks = std::min((TK + 7) / 8, num_sms * 16);
     gather_rows_kernel<<<blocks, 256, 0, s>>>(pf->zb, pf->perm, TK, K, L, pf->zg);
     e = cudaGetLastError();
   }
-  // 6-7. experts: token tiles of the routed groups are at most TK/256 + (non-empty
-  // groups) + the shared expert's
-  const int bound = TK / kGgBN + std::min(E, TK) + (T + kGgBN - 1) / kGgBN;
+  mark();
+  // 6-7. experts
   GgParams gp;
   gp.T = T; gp.TK = TK; gp.L = L; gp.F = F; gp.E = E;
   gp.counts = pf->counts; gp.offsets = pf->offsets; gp.tprefix = pf->tprefix;
@@ -465,21 +474,26 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   gp.abort = pf->abort;
   if (e == cudaSuccess) {
     gp.mode = 1; gp.mtiles = F / 64; gp.out = pf->hb; gp.out_ld = F;
-    e = launch_grouped(pf->maps1, gp, bound, s);
+    e = launch_grouped(pf->maps1, gp, num_sms, s);
   }
+  mark();
   if (e == cudaSuccess) {
     gp.mode = 2; gp.mtiles = L / 128; gp.out = pf->ob; gp.out_ld = L;
-    e = launch_grouped(pf->maps2, gp, bound, s);
+    e = launch_grouped(pf->maps2, gp, num_sms, s);
   }
+  mark();
   // 8. combine
   if (e == cudaSuccess) {
     combine_kernel<<<T, (L / 8 + 31) / 32 * 32, 0, s>>>(pf->ob, pf->pos, pf->w, T, K, L, pf->cb);
     e = cudaGetLastError();
   }
+  mark();
   // 9. y = c U^T
   if (e == cudaSuccess)
     e = launch_gemm_tn<kPfBN, kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, L, 1 << 30, pf->err, pf->abort,
                                          EpiStoreBF16{y, H, H}, s);
+  mark();
+  if (pf->profile && e == cudaSuccess) pf->timed = (stage == 11);
   return e == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA;
 }
 
@@ -494,6 +508,31 @@ const void* prefill_debug_tensor(const PrefillWorkspace* pf, int what, const edg
 
 __nv_bfloat16* prefill_stack_scratch(PrefillWorkspace* pf) { return pf->scratch; }
 
-void prefill_destroy(PrefillWorkspace*) {}
+cudaError_t prefill_profile(PrefillWorkspace* pf, bool enable) {
+  if (enable && !pf->events[0]) {
+    for (auto& ev : pf->events) {
+      const cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  pf->profile = enable;
+  pf->timed = false;
+  return cudaSuccess;
+}
+
+edge0_status prefill_stage_times(PrefillWorkspace* pf, float* ms, int max, int* n_out) {
+  if (!pf->timed) return EDGE0_ERR_UNSUPPORTED;
+  if (cudaEventSynchronize(pf->events[10]) != cudaSuccess) return EDGE0_ERR_CUDA;
+  const int n = max < 10 ? max : 10;
+  for (int i = 0; i < n; ++i)
+    if (cudaEventElapsedTime(&ms[i], pf->events[i], pf->events[i + 1]) != cudaSuccess) return EDGE0_ERR_CUDA;
+  if (n_out) *n_out = n;
+  return EDGE0_OK;
+}
+
+void prefill_destroy(PrefillWorkspace* pf) {
+  for (auto& ev : pf->events)
+    if (ev) cudaEventDestroy(ev);
+}
 
 }  // namespace edge0

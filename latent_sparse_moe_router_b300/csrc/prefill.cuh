@@ -27,6 +27,11 @@ struct PrefillWorkspace {
   __nv_bfloat16* cb = nullptr;      // [T][latent] combined latent
   __nv_bfloat16* scratch = nullptr; // [T][hidden] layer output for stacked calls
   int* abort = nullptr;             // per-forward abort word of the bounded waits
+  // stage timing (profiling): events[0] before the first kernel, events[i + 1]
+  // after stage i
+  bool profile = false;
+  bool timed = false;               // the last forward recorded the events
+  cudaEvent_t events[11] = {};
   // tensor maps fixed for the handle's lifetime
   CUtensorMap m_D, m_rdcat, m_U, m_cb;
   GgMaps maps1, maps2;
@@ -41,5 +46,7 @@ const void* prefill_debug_tensor(const PrefillWorkspace* pf, int what, const edg
                                  size_t* bytes);
 __nv_bfloat16* prefill_stack_scratch(PrefillWorkspace* pf);
 void prefill_destroy(PrefillWorkspace* pf);
+cudaError_t prefill_profile(PrefillWorkspace* pf, bool enable);
+edge0_status prefill_stage_times(PrefillWorkspace* pf, float* ms, int max, int* n_out);
 
 }  // namespace edge0

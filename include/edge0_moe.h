@@ -269,6 +269,15 @@ edge0_status edge0_moe_profile_stages(void *handle, int enable);
 edge0_status edge0_moe_stage_times(void *handle, float *ms, int max, int *n_out);
 
 /*
+ * Failure-path check: launch one block on `stream` that waits on an mbarrier
+ * no one arrives at, through the same bounded wait every kernel of the library
+ * uses (limit 1 s of %globaltimer).  The wait runs out, sets the handle's
+ * error word and the block returns; the next edge0_moe_get_error on the
+ * handle reports EDGE0_ERR_TIMEOUT.  Faults nothing; the handle stays usable.
+ */
+edge0_status edge0_moe_debug_wait_probe(void *handle, edge0_stream_t stream);
+
+/*
  * Synchronise with the device and return the handle's device error word
  * (EDGE0_OK, or EDGE0_ERR_TIMEOUT if a bounded device wait ran out since the
  * last call); clears the word.

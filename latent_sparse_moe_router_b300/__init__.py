@@ -27,7 +27,7 @@ EXPORTED = (
     "edge0_moe_debug_routing", "edge0_moe_debug_tensor", "edge0_residual_rmsnorm",
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
     "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc", "edge0_gemm_bf16_tn",
-    "edge0_moe_profile_stages", "edge0_moe_stage_times",
+    "edge0_moe_profile_stages", "edge0_moe_stage_times", "edge0_moe_debug_wait_probe",
 )
 
 EDGE0_PREFILL_STAGES = 10
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_forward_noalloc": (i, [ctypes.POINTER(edge0_moe_desc), vp, vp, i, vp, vp]),
             "edge0_gemm_bf16_tn": (i, [vp, vp, vp, i, i, i, vp, vp]),
             "edge0_moe_profile_stages": (i, [vp, i]),
+            "edge0_moe_debug_wait_probe": (i, [vp, vp]),
             "edge0_moe_stage_times": (i, [vp, vp, i, vp]),
         }
         for name, (res, args) in sig.items():
@@ -218,6 +219,11 @@ def edge0_moe_forward_noalloc(hidden, latent, n_experts, top_k, ffn, D, U, route
                        _ptr(router_bias), _ptr(experts), expert_stride, _ptr(shared_expert))
     _check(lib().edge0_moe_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(y), T, _ptr(status),
                                            _stream(stream)), "edge0_moe_forward_noalloc")
+
+
+def edge0_moe_debug_wait_probe(handle, stream=None):
+    """Make one bounded device wait run out (nothing faults); see the C header."""
+    _check(lib().edge0_moe_debug_wait_probe(handle, _stream(stream)), "edge0_moe_debug_wait_probe")
 
 
 def edge0_moe_profile_stages(handle, enable: bool):

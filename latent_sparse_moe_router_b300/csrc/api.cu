@@ -288,6 +288,17 @@ __global__ void residual_rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloa
 
 edge0_status launch_status() { return cuda_status(cudaGetLastError()); }
 
+// One mbarrier that nothing arrives at, waited on with the library's bounded wait.
+__global__ void wait_probe_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_abort(&bar, 0, err, nullptr);
+}
+
 }  // namespace
 
 extern "C" {
@@ -585,6 +596,13 @@ edge0_status edge0_moe_stack_forward_trace(void* const* handles, int n_layers, c
                                            int T, float eps, void* trace_x, void* trace_y,
                                            edge0_stream_t stream) {
   return stack_impl(handles, n_layers, x, y, T, eps, trace_x, trace_y, stream);
+}
+
+edge0_status edge0_moe_debug_wait_probe(void* handle, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(hd->err);
+  return launch_status();
 }
 
 edge0_status edge0_moe_profile_stages(void* handle, int enable) {

@@ -32,6 +32,7 @@ namespace edge0 {
 constexpr int kGgThreads = 448;  // 14 warps
 constexpr int kGgDqWarp0 = 2;     // dequantisation warps 2..9
 constexpr int kGgDqThreads = 256;
+constexpr int kGgDqWarps = 8;
 constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..13
 constexpr int kGgBN = 256;        // token tile
 constexpr int kGgS = 3;           // A / B stages

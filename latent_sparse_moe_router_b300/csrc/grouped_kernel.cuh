@@ -89,15 +89,15 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GgSmem::offBar);
-  uint64_t* a_full = bars;                 // [S] 256 dequant arrivals
+  uint64_t* a_full = bars;                 // [S] one arrival per dequant warp
   uint64_t* b_full = a_full + kGgS;        // [S] TMA bytes
   uint64_t* ab_empty = b_full + kGgS;      // [S] MMA commit
   uint64_t* raw_full = ab_empty + kGgS;    // [R] TMA bytes
-  uint64_t* raw_empty = raw_full + kGgR;   // [R] 256 dequant arrivals
+  uint64_t* raw_empty = raw_full + kGgR;   // [R] one arrival per dequant warp
   uint64_t* sc_full = raw_empty + kGgR;    // [2] TMA bytes
-  uint64_t* sc_empty = sc_full + 2;        // [2] 256 dequant arrivals
+  uint64_t* sc_empty = sc_full + 2;        // [2] one arrival per dequant warp
   uint64_t* acc_full = sc_empty + 2;       // [2] MMA commit
-  uint64_t* acc_empty = acc_full + 2;      // [2] 128 epilogue arrivals
+  uint64_t* acc_empty = acc_full + 2;      // [2] one arrival per epilogue warp
   uint64_t* mma_done = acc_empty + 2;      // final MMA commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 2);   // [0] total tiles, [1] bad
@@ -106,11 +106,12 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
   if (threadIdx.x == 0) {
     s_flags[0] = (p.abort && ld_relaxed_s32(p.abort)) ? 0 : p.tprefix[p.E + 1] * p.mtiles;
     s_flags[1] = 0;
-    for (int s = 0; s < kGgS; ++s) { mbar_init(&a_full[s], kGgDqThreads); mbar_init(&b_full[s], 1); mbar_init(&ab_empty[s], 1); }
-    for (int s = 0; s < kGgR; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kGgDqThreads); }
+    // consumer barriers take one arrival per warp (lane 0 after a __syncwarp)
+    for (int s = 0; s < kGgS; ++s) { mbar_init(&a_full[s], kGgDqWarps); mbar_init(&b_full[s], 1); mbar_init(&ab_empty[s], 1); }
+    for (int s = 0; s < kGgR; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kGgDqWarps); }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sc_full[b], 1); mbar_init(&sc_empty[b], kGgDqThreads);
-      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128);
+      mbar_init(&sc_full[b], 1); mbar_init(&sc_empty[b], kGgDqWarps);
+      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -214,25 +215,29 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       mbar_wait_abort(mma_done, 0, p.err, nullptr);
     }
   } else if (warp < kGgEpWarp0) {
-    // ---- dequantisation: thread pair (r, hh) owns A row r, elements 32 hh .. 32 hh + 31
+    // ---- dequantisation: thread pair (r, hh) owns A row r, elements 32 hh .. 32 hh + 31.
+    // A rows come in pairs 2i, 2i+1: mode 1 gate and up row f0 + i (so the epilogue
+    // finds both in neighbouring lanes), mode 2 latent rows 2(q0 + i) and 2(q0 + i) + 1.
+    // Raw codes: first 2 KB the 64 even-row slices, then the 64 odd-row slices.
     const int td = threadIdx.x - kGgDqWarp0 * 32;
     const int r = td >> 1, hh = td & 1;
-    const int raw_off = (p.mode == 1 ? r * 32 : (r & 1) * 2048 + (r >> 1) * 32) + hh * 16;
-    // this row's scales: mode 1 rows 0-63 gate, 64-127 up; mode 2 rows r = 2q + h
-    const int sc_off = (p.mode == 1 ? r * (p.L / 16) : (r >> 1) * (p.F / 8) + (r & 1) * (p.F / 16)) + hh * 2;
+    const int raw_off = (r & 1) * 2048 + (r >> 1) * 32 + hh * 16;
+    const int sc_off = (p.mode == 1 ? (r & 1) * 64 * (p.L / 16) + (r >> 1) * (p.L / 16)
+                                    : (r >> 1) * (p.F / 8) + (r & 1) * (p.F / 16)) + hh * 2;
     int it = 0, ti = 0;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
       const int sb = ti & 1;
-      if (!mbar_wait_abort(&sc_full[sb], (ti >> 1) & 1, p.err, p.abort)) { ok = false; break; }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&sc_full[sb], (ti >> 1) & 1, p.err, p.abort))) { ok = false; break; }
       const uint8_t* my_sc = smem + GgSmem::offSc + sb * GgSmem::kSc + sc_off;
       for (int kb = 0; kb < nk; ++kb, ++it) {
         const int rr = it % kGgR, s = it % kGgS;
-        if (!mbar_wait_abort(&raw_full[rr], (it / kGgR) & 1, p.err, p.abort)) { ok = false; break; }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&raw_full[rr], (it / kGgR) & 1, p.err, p.abort))) { ok = false; break; }
         const uint4 cw4 = *reinterpret_cast<const uint4*>(smem + GgSmem::offRaw + rr * GgSmem::kRaw + raw_off);
         const uint32_t s2 = *reinterpret_cast<const uint16_t*>(my_sc + kb * 4);
-        mbar_arrive(&raw_empty[rr]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rr]);
         const uint32_t sc0 = scale_bf16x2(s2 & 0xFF), sc1 = scale_bf16x2(s2 >> 8);
-        if (!mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
         uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
         const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
 #pragma unroll
@@ -250,17 +255,23 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
           *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = o;
         }
         fence_async_smem();
-        mbar_arrive(&a_full[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[s]);
       }
       if (!ok) break;
-      mbar_arrive(&sc_empty[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc_empty[sb]);
     }
   } else {
-    // ---- epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31
+    // ---- epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31 (A rows).
+    // Neighbouring lanes hold the row pair (2i, 2i+1); the even lane finishes token
+    // columns 0-15 of the chunk, the odd lane 16-31, after one shuffle each.
     const int q = warp & 3;
     const int te = threadIdx.x - kGgEpWarp0 * 32;   // 0..127
-    float* ubuf = reinterpret_cast<float*>(smem + GgSmem::offEpi);                       // [64][33] fp32
-    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi + 8448);  // [32][136] bf16
+    const int odd = lane & 1, pr = q * 16 + (lane >> 1);   // row pair in the tile
+    // mode 1: [32 tokens][72] bf16 (64 f used); mode 2: [32 tokens][68] u32 (64 latent pairs used)
+    __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi);
+    uint32_t* obuf = reinterpret_cast<uint32_t*>(smem + GgSmem::offEpi);
     int ti = 0;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
       const GgTile t = gg_tile(p, tile);
@@ -271,46 +282,44 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       tc_fence_after();
       const uint8_t* rec = t.shared ? p.shared : p.experts + size_t(t.g) * p.stride;
       const float* gl = reinterpret_cast<const float*>(rec + size_t(27) * p.F * p.L / 16);
+      const float g0 = p.mode == 1 ? gl[0] : gl[2], g1 = gl[1];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256;
+      const int tr = te >> 2, part = te & 3;
       for (int c = 0; c * 32 < t.n_rows; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + c * 32, v);
         tmem_ld_wait();
-        const int tr = te >> 2, part = te & 3;
         if (p.mode == 1) {
-          // lanes 64-127 hold up rows: hand them to the gate warps
-          if (q >= 2) {
-            const int fl = (q - 2) * 32 + lane;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ubuf[fl * 33 + j] = __uint_as_float(v[j]);
-          }
-          named_sync(1, 128);
-          if (q < 2) {
-            const int fl = q * 32 + lane;
-            const float gg = gl[0], gu = gl[1];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float h = silu_gg(gg * __uint_as_float(v[j])) * (gu * ubuf[fl * 33 + j]);
-              tbuf[j * 136 + fl] = __float2bfloat16_rn(h);
-            }
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t va = v[j], vb = v[16 + j];
+            const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
+            const float gate = odd ? x : __uint_as_float(va);
+            const float up = odd ? __uint_as_float(vb) : x;
+            hbuf[(odd * 16 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * gate) * (g1 * up));
           }
           named_sync(1, 128);
           // 32 token rows x 64 f (128 B): 4 threads per row, 32 B each
           if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(tbuf + tr * 136 + part * 16);
+            const uint4* src = reinterpret_cast<const uint4*>(hbuf + tr * 72 + part * 16);
             uint4* dst = reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 64 + part * 16);
             dst[0] = src[0];
             dst[1] = src[1];
           }
         } else {
-          const float gd = gl[2];
-          const int rl = q * 32 + lane;   // latent row in the tile
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tbuf[j * 136 + rl] = __float2bfloat16_rn(gd * __uint_as_float(v[j]));
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t va = v[j], vb = v[16 + j];
+            const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
+            const float lo = odd ? x : __uint_as_float(va);            // latent row 2i
+            const float hi = odd ? __uint_as_float(vb) : x;            // latent row 2i + 1
+            const __nv_bfloat162 b = __floats2bfloat162_rn(g0 * lo, g0 * hi);
+            obuf[(odd * 16 + j) * 68 + pr] = *reinterpret_cast<const uint32_t*>(&b);
+          }
           named_sync(1, 128);
           // 32 token rows x 128 latent rows (256 B): 4 threads per row, 64 B each
           if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(tbuf + tr * 136 + part * 32);
+            const uint4* src = reinterpret_cast<const uint4*>(obuf + tr * 68 + part * 16);
             uint4* dst =
                 reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 128 + part * 32);
 #pragma unroll
@@ -321,7 +330,8 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       }
       // the accumulator's TMEM columns are free for the tile after next
       tc_fence_before();
-      mbar_arrive(&acc_empty[ab]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
   if (!ok) s_flags[1] = 1;

@@ -264,25 +264,29 @@ __global__ void quantize_kernel(const float* __restrict__ w, int rows, int K, fl
 // out[t] = bf16(v / sqrt(mean(v^2) + eps)), v = x[t] + y[t]; one block per token.
 // Launched with the decode kernel's block size and summation order, so a stack run
 // as separate layer calls reproduces the fused stack bit for bit.
-__global__ void residual_rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* y,
-                                        __nv_bfloat16* out, int hidden, float eps) {
-  __shared__ float red[32];
-  const size_t base = size_t(blockIdx.x) * hidden;
-  float s = 0.f;
-  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
-    const float v = __bfloat162float(x[base + k]) + __bfloat162float(y[base + k]);
-    s = fmaf(v, v, s);
-  }
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-  __syncthreads();
-  float tot = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
-  const float inv = 1.0f / sqrtf(tot / float(hidden) + eps);
-  __syncthreads();
-  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
-    const float v = __bfloat162float(x[base + k]) + __bfloat162float(y[base + k]);
-    out[base + k] = __float2bfloat16_rn(v * inv);
+// out = bf16((x + y) / sqrt(mean((x + y)^2) + eps)): one warp per token row.
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* y,
+                                                               __nv_bfloat16* out, int T, int hidden, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const size_t base = size_t(t) * hidden;
+  const float inv = 1.0f / sqrtf(row_sumsq_warp(x + base, y + base, hidden, lane) / float(hidden) + eps);
+  const uint4* xv = reinterpret_cast<const uint4*>(x + base);
+  const uint4* yv = reinterpret_cast<const uint4*>(y + base);
+  uint4* ov = reinterpret_cast<uint4*>(out + base);
+  for (int g = lane; g < hidden / 8; g += 32) {
+    const uint4 a = xv[g], b = yv[g];
+    const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float v0 = __uint_as_float(aa[i] << 16) + __uint_as_float(bb[i] << 16);
+      const float v1 = __uint_as_float(aa[i] & 0xFFFF0000u) + __uint_as_float(bb[i] & 0xFFFF0000u);
+      const __nv_bfloat162 r = __floats2bfloat162_rn(v0 * inv, v1 * inv);
+      o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+    ov[g] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -531,9 +535,10 @@ edge0_status edge0_residual_rmsnorm(const void* x, const void* y, void* out, int
   if (T < 0 || hidden <= 0 || hidden % 8 || !(eps >= 0.f)) return EDGE0_ERR_INVALID_ARG;
   if (T == 0) return EDGE0_OK;
   if (!x || !y || !out) return EDGE0_ERR_INVALID_ARG;
-  residual_rmsnorm_kernel<<<T, kDecThreads, 0, (cudaStream_t)stream>>>(
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(out, 16)) return EDGE0_ERR_INVALID_ARG;
+  residual_rmsnorm_kernel<<<(T + 7) / 8, 256, 0, (cudaStream_t)stream>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(y),
-      static_cast<__nv_bfloat16*>(out), hidden, eps);
+      static_cast<__nv_bfloat16*>(out), T, hidden, eps);
   return launch_status();
 }
 

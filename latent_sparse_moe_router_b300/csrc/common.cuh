@@ -204,6 +204,31 @@ __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
   return s_ok != 0;
 }
 
+// ---------------------------------------------------------------- residual RMSNorm
+// Sum over one token row of (x + y)^2 (bf16 inputs, fp32 sums) by one warp: lane l
+// takes the 16-byte groups l, l + 32, ... (8 values each, fmaf in order), then the
+// 32 lane sums meet in an xor tree.  The one summation order of the library's
+// residual norms (the stacked decode kernel and the standalone kernel).  H % 8 == 0.
+__device__ __forceinline__ float row_sumsq_warp(const __nv_bfloat16* x, const __nv_bfloat16* y, int H, int lane) {
+  float s = 0.f;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const uint4* yv = reinterpret_cast<const uint4*>(y);
+  for (int g = lane; g < H / 8; g += 32) {
+    const uint4 a = xv[g], b = yv[g];
+    const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float v0 = __uint_as_float(aa[i] << 16) + __uint_as_float(bb[i] << 16);
+      const float v1 = __uint_as_float(aa[i] & 0xFFFF0000u) + __uint_as_float(bb[i] & 0xFFFF0000u);
+      s = fmaf(v0, v0, s);
+      s = fmaf(v1, v1, s);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
 // ---------------------------------------------------------------- NVFP4 decode
 // Two E2M1 codes (one byte, low nibble first) -> half2 (x = low, y = high).
 __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {

@@ -296,20 +296,10 @@ __device__ __forceinline__ void pow2_scale(float maxabs, float* sc, float* inv) 
 __device__ void residual_norm(DecTables* tb, const __nv_bfloat16* xp, const __nv_bfloat16* yp,
                               __nv_bfloat16* xs, int T, int H, float eps) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int t = 0; t < T; ++t) {
-    float s = 0.f;
-    for (int k = tid; k < H; k += kDecThreads) {
-      const float v = __bfloat162float(xp[size_t(t) * H + k]) + __bfloat162float(yp[size_t(t) * H + k]);
-      s = fmaf(v, v, s);
-    }
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-    if (lane == 0) tb->red[warp * kDecodeMaxT + t] = s;
-  }
-  __syncthreads();
-  if (tid < T) {
-    float s = 0.f;
-    for (int wv = 0; wv < kDecWarps; ++wv) s += tb->red[wv * kDecodeMaxT + tid];
-    tb->inv_rms[tid] = 1.0f / sqrtf(s / float(H) + eps);
+  // warp t reduces token t (T <= 16 warps), in the library's one summation order
+  if (warp < T) {
+    const float s = row_sumsq_warp(xp + size_t(warp) * H, yp + size_t(warp) * H, H, lane);
+    if (lane == 0) tb->inv_rms[warp] = 1.0f / sqrtf(s / float(H) + eps);
   }
   __syncthreads();
   for (int i = tid; i < T * H; i += kDecThreads) {

@@ -174,6 +174,75 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float* __restrict_
   for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_cnt[size_t(blockIdx.x) * E + i] = hist[i];
 }
 
+// The same for E = 32 NJ with each lane's NJ logits in registers (no shared-memory
+// pass per selection round): one warp per token, 8 tokens per warp, 64 per block.
+template <int NJ>
+__global__ void __launch_bounds__(256) topk_hist_reg_kernel(const float* __restrict__ logits, int T, int K,
+                                                            int* __restrict__ idx, float* __restrict__ w,
+                                                            int* __restrict__ chunk_cnt) {
+  constexpr int E = NJ * 32;
+  __shared__ int hist[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int tt = warp; tt < kChunk; tt += 8) {
+    const int t = blockIdx.x * kChunk + tt;
+    if (t >= T) break;
+    const float* row = logits + size_t(t) * E;
+    float v[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const float x = row[j * 32 + lane];
+      v[j] = (x != x) ? -INFINITY : x;   // a NaN logit ranks last
+    }
+    uint32_t taken = 0;
+    float myv = 0.f;
+    int myi = 0;
+    for (int r = 0; r < K; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int i = j * 32 + lane;
+        if (!((taken >> j) & 1u) && pf_better(v[j], i, bv, bi)) { bv = v[j]; bi = i; }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (pf_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == r) { myv = bv; myi = bi; }
+    }
+    const float m = __shfl_sync(0xFFFFFFFFu, myv, 0);
+    const float ex = lane < K ? expf(myv - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < K) {
+      idx[size_t(t) * K + lane] = myi;
+      w[size_t(t) * K + lane] = ex / sum;
+      atomicAdd(&hist[myi], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_cnt[size_t(blockIdx.x) * E + i] = hist[i];
+}
+
+cudaError_t launch_topk_hist(const float* logits, int T, int E, int K, int* idx, float* w, int* chunk_cnt,
+                             cudaStream_t s) {
+  const int nch = (T + kChunk - 1) / kChunk;
+  switch (E / 32) {
+    case 2: topk_hist_reg_kernel<2><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 4: topk_hist_reg_kernel<4><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 8: topk_hist_reg_kernel<8><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 16: topk_hist_reg_kernel<16><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    default: topk_hist_kernel<<<nch, 256, (8 * E + E) * 4, s>>>(logits, T, E, K, idx, w, chunk_cnt);
+  }
+  return cudaGetLastError();
+}
+
 // Per expert: total count, and the chunk counts replaced by their exclusive
 // prefix over the chunks.  Block = 32 experts x 32 chunk slices.
 __global__ void __launch_bounds__(1024) scan_chunks_kernel(int* __restrict__ chunk_cnt, int nch, int E,
@@ -436,8 +505,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   mark();
   // 2-4. routing and permutation
   if (e == cudaSuccess) {
-    topk_hist_kernel<<<nch, 256, (8 * E + E) * 4, s>>>(pf->logits, T, E, K, pf->idx, pf->w, pf->chunk_cnt);
-    e = cudaGetLastError();
+    e = launch_topk_hist(pf->logits, T, E, K, pf->idx, pf->w, pf->chunk_cnt, s);
   }
   mark();
   if (e == cudaSuccess) {

@@ -217,3 +217,16 @@ def test_layer_145b_t16384_uniform(dev):
     m = check_layer(d, lay, x_bits, bits(y), r, tokens=sel, check_perm=False)
     print("layer145b_t16384", m, "flips(all tokens)", flips)
     d.close()
+
+
+def test_prefill_generic_topk_path(dev):
+    """E = 96 (not a power-of-two multiple of 32) takes the shared-memory top-k kernel."""
+    spec = small_spec(seed=21, n_experts=96, top_k=6, zipf=0.9)
+    inp = synth.make_layer(spec)
+    T = 150
+    d = dev.DeviceLayer(inp, max_tokens=T)
+    x_bits = synth.tokens_bf16(31, T, spec.hidden)
+    y = d.forward(dev_bf16(x_bits))
+    torch.cuda.synchronize()
+    check_layer(d, oracle_layer(inp), x_bits, bits(y), d.routing(T))
+    d.close()

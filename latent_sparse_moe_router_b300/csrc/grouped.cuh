@@ -12,9 +12,10 @@
 // Persistent CTAs (one per SM) walk the tiles in index order with a stride of
 // the grid, tile = (token tile, weight tile) with the weight tile fastest, so
 // the CTAs working at one time share a few token tiles through L2.  Warp roles:
-//   warp 0 (one lane): TMA producer - the tile's E4M3 scales (double-buffered),
-//     raw NVFP4 codes (4 KB per 64-wide k-step) and the B rows the tile needs
-//     (64-row boxes, 128-byte swizzle);
+//   warp 0 (one lane): TMA producer of the tile's E4M3 scales (double-buffered)
+//     and raw NVFP4 codes (4 KB per 64-wide k-step, 8-deep ring);
+//   warp 14 (one lane): TMA producer of the B rows the tile needs (64-row boxes,
+//     128-byte swizzle), into the stages the MMA releases;
 //   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
 //     K=16, into one of two TMEM accumulators of 256 columns;
 //   warps 2-9: dequantisation, two threads per A row (E2M1 -> f16 by cvt, moved
@@ -29,21 +30,22 @@
 
 namespace edge0 {
 
-constexpr int kGgThreads = 448;  // 14 warps
+constexpr int kGgThreads = 480;  // 15 warps
 constexpr int kGgDqWarp0 = 2;     // dequantisation warps 2..9
 constexpr int kGgDqThreads = 256;
 constexpr int kGgDqWarps = 8;
 constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..13
+constexpr int kGgBWarp = 14;      // B-tile producer
 constexpr int kGgBN = 256;        // token tile
 constexpr int kGgS = 3;           // A / B stages
-constexpr int kGgR = 4;           // raw code stages
+constexpr int kGgR = 8;           // raw code stages
 
 struct GgSmem {
   static constexpr int kA = 128 * 64 * 2;        // 16 KB
   static constexpr int kB = kGgBN * 64 * 2;      // 32 KB
   static constexpr int kRaw = 128 * 32;          // 4 KB
   static constexpr int kSc = 16384;              // scales of one tile (<= 128 rows x 128 B)
-  static constexpr int kEpi = 17408;             // epilogue transpose buffers
+  static constexpr int kEpi = 9216;              // epilogue transpose buffers
   static constexpr int offA = 0;
   static constexpr int offB = offA + kGgS * kA;
   static constexpr int offRaw = offB + kGgS * kB;

@@ -130,14 +130,13 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- producer
+      // ---- scale and raw-code producer
       const int scb = p.mode == 1 ? 2 * 64 * (p.L / 16) : 64 * (p.F / 8);
       int it = 0, ti = 0;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
         const GgTile t = gg_tile(p, tile);
         const CUtensorMap* mcodes = t.shared ? &maps.s_codes : &maps.a_codes;
         const CUtensorMap* mscales = t.shared ? &maps.s_scales : &maps.a_scales;
-        const CUtensorMap* mb = (t.shared && p.mode == 1) ? &maps.b_shared : &maps.b_routed;
         const int sb = ti & 1;
         if (!mbar_wait_abort(&sc_empty[sb], ((ti >> 1) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
         mbar_arrive_expect_tx(&sc_full[sb], scb);
@@ -155,7 +154,6 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
           if (t.shared) tma_load_2d(sc, mscales, p.F, y, &sc_full[sb]);
           else tma_load_3d(sc, mscales, p.F, y, t.g, &sc_full[sb]);
         }
-        const int nbox = (t.n_rows + kGgBBox - 1) / kGgBBox;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int r = it % kGgR;
           if (!mbar_wait_abort(&raw_empty[r], ((it / kGgR) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
@@ -171,6 +169,18 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
             tma_load_3d(raw, mcodes, x0, y, t.g, &raw_full[r]);
             tma_load_3d(raw + 2048, mcodes, x1, y, t.g, &raw_full[r]);
           }
+        }
+      }
+    }
+  } else if (warp == kGgBWarp) {
+    if (lane == 0) {
+      // ---- B producer: the tile's token rows, one k-slice per stage
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const GgTile t = gg_tile(p, tile);
+        const CUtensorMap* mb = (t.shared && p.mode == 1) ? &maps.b_shared : &maps.b_routed;
+        const int nbox = (t.n_rows + kGgBBox - 1) / kGgBBox;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kGgS;
           if (!mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[s], nbox * kGgBBox * 128);
@@ -237,22 +247,26 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rr]);
         const uint32_t sc0 = scale_bf16x2(s2 & 0xFF), sc1 = scale_bf16x2(s2 >> 8);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
-        uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
+        // dequantise into registers first: only the stores wait for the stage
         const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+        uint4 o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // 16-byte chunk c = 4 hh + j of the row: elements 8c .. 8c + 7, block c / 2
           const uint32_t sc2 = j < 2 ? sc0 : sc1;
           uint32_t h0, h1, h2, h3;
           e2m1x8_to_h2x4(cw[j], h0, h1, h2, h3);
-          uint4 o;
-          o.x = h2_to_bf2_scaled(h0, sc2);
-          o.y = h2_to_bf2_scaled(h1, sc2);
-          o.z = h2_to_bf2_scaled(h2, sc2);
-          o.w = h2_to_bf2_scaled(h3, sc2);
+          o[j].x = h2_to_bf2_scaled(h0, sc2);
+          o[j].y = h2_to_bf2_scaled(h1, sc2);
+          o[j].z = h2_to_bf2_scaled(h2, sc2);
+          o[j].w = h2_to_bf2_scaled(h3, sc2);
+        }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
+        uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
           const int c = 4 * hh + j;
-          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = o;
+          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = o[j];
         }
         fence_async_smem();
         __syncwarp();

@@ -13,7 +13,7 @@
 // the grid, tile = (token tile, weight tile) with the weight tile fastest, so
 // the CTAs working at one time share a few token tiles through L2.  Warp roles:
 //   warp 0 (one lane): TMA producer of the tile's E4M3 scales (double-buffered)
-//     and raw NVFP4 codes (4 KB per 64-wide k-step, 8-deep ring);
+//     and raw NVFP4 codes (4 KB per 64-wide k-step, 6-deep ring);
 //   warp 14 (one lane): TMA producer of the B rows the tile needs (64-row boxes,
 //     128-byte swizzle), into the stages the MMA releases;
 //   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
@@ -37,8 +37,9 @@ constexpr int kGgDqWarps = 8;
 constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..13
 constexpr int kGgBWarp = 14;      // B-tile producer
 constexpr int kGgBN = 256;        // token tile
-constexpr int kGgS = 3;           // A / B stages
-constexpr int kGgR = 8;           // raw code stages
+constexpr int kGgSA = 4;          // A (dequantised weight) stages
+constexpr int kGgSB = 3;          // B (token row) stages
+constexpr int kGgR = 6;           // raw code stages
 
 struct GgSmem {
   static constexpr int kA = 128 * 64 * 2;        // 16 KB
@@ -47,8 +48,8 @@ struct GgSmem {
   static constexpr int kSc = 16384;              // scales of one tile (<= 128 rows x 128 B)
   static constexpr int kEpi = 9216;              // epilogue transpose buffers
   static constexpr int offA = 0;
-  static constexpr int offB = offA + kGgS * kA;
-  static constexpr int offRaw = offB + kGgS * kB;
+  static constexpr int offB = offA + kGgSA * kA;
+  static constexpr int offRaw = offB + kGgSB * kB;
   static constexpr int offSc = offRaw + kGgR * kRaw;
   static constexpr int offEpi = offSc + 2 * kSc;
   static constexpr int offBar = offEpi + kEpi;

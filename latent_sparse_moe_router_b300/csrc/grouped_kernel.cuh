@@ -89,10 +89,11 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GgSmem::offBar);
-  uint64_t* a_full = bars;                 // [S] one arrival per dequant warp
-  uint64_t* b_full = a_full + kGgS;        // [S] TMA bytes
-  uint64_t* ab_empty = b_full + kGgS;      // [S] MMA commit
-  uint64_t* raw_full = ab_empty + kGgS;    // [R] TMA bytes
+  uint64_t* a_full = bars;                 // [SA] one arrival per dequant warp
+  uint64_t* a_empty = a_full + kGgSA;      // [SA] MMA commit
+  uint64_t* b_full = a_empty + kGgSA;      // [SB] TMA bytes
+  uint64_t* b_empty = b_full + kGgSB;      // [SB] MMA commit
+  uint64_t* raw_full = b_empty + kGgSB;    // [R] TMA bytes
   uint64_t* raw_empty = raw_full + kGgR;   // [R] one arrival per dequant warp
   uint64_t* sc_full = raw_empty + kGgR;    // [2] TMA bytes
   uint64_t* sc_empty = sc_full + 2;        // [2] one arrival per dequant warp
@@ -107,7 +108,8 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     s_flags[0] = (p.abort && ld_relaxed_s32(p.abort)) ? 0 : p.tprefix[p.E + 1] * p.mtiles;
     s_flags[1] = 0;
     // consumer barriers take one arrival per warp (lane 0 after a __syncwarp)
-    for (int s = 0; s < kGgS; ++s) { mbar_init(&a_full[s], kGgDqWarps); mbar_init(&b_full[s], 1); mbar_init(&ab_empty[s], 1); }
+    for (int s = 0; s < kGgSA; ++s) { mbar_init(&a_full[s], kGgDqWarps); mbar_init(&a_empty[s], 1); }
+    for (int s = 0; s < kGgSB; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
     for (int s = 0; s < kGgR; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kGgDqWarps); }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sc_full[b], 1); mbar_init(&sc_empty[b], kGgDqWarps);
@@ -181,8 +183,8 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         const CUtensorMap* mb = (t.shared && p.mode == 1) ? &maps.b_shared : &maps.b_routed;
         const int nbox = (t.n_rows + kGgBBox - 1) / kGgBBox;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % kGgS;
-          if (!mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
+          const int s = it % kGgSB;
+          if (!mbar_wait_abort(&b_empty[s], ((it / kGgSB) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[s], nbox * kGgBBox * 128);
           uint8_t* bs = smem + GgSmem::offB + s * GgSmem::kB;
           for (int bx = 0; bx < nbox; ++bx)
@@ -203,19 +205,20 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % kGgS;
-          const uint32_t ph = (it / kGgS) & 1;
-          if (!mbar_wait_abort(&a_full[s], ph, p.err, p.abort) || !mbar_wait_abort(&b_full[s], ph, p.err, p.abort)) {
+          const int sa_i = it % kGgSA, sb_i = it % kGgSB;
+          if (!mbar_wait_abort(&a_full[sa_i], (it / kGgSA) & 1, p.err, p.abort) ||
+              !mbar_wait_abort(&b_full[sb_i], (it / kGgSB) & 1, p.err, p.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + GgSmem::offA + s * GgSmem::kA);
-          const uint32_t sbb = smem_u32(smem + GgSmem::offB + s * GgSmem::kB);
+          const uint32_t sa = smem_u32(smem + GgSmem::offA + sa_i * GgSmem::kA);
+          const uint32_t sbb = smem_u32(smem + GgSmem::offB + sb_i * GgSmem::kB);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_bf16(acc, sw128_desc(sa + k * 32), sw128_desc(sbb + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&ab_empty[s]);
+          mma_commit(&a_empty[sa_i]);
+          mma_commit(&b_empty[sb_i]);
         }
         if (!ok) break;
         mma_commit(&acc_full[ab]);
@@ -240,7 +243,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&sc_full[sb], (ti >> 1) & 1, p.err, p.abort))) { ok = false; break; }
       const uint8_t* my_sc = smem + GgSmem::offSc + sb * GgSmem::kSc + sc_off;
       for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int rr = it % kGgR, s = it % kGgS;
+        const int rr = it % kGgR, s = it % kGgSA;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&raw_full[rr], (it / kGgR) & 1, p.err, p.abort))) { ok = false; break; }
         const uint4 cw4 = *reinterpret_cast<const uint4*>(smem + GgSmem::offRaw + rr * GgSmem::kRaw + raw_off);
         const uint32_t s2 = *reinterpret_cast<const uint16_t*>(my_sc + kb * 4);
@@ -261,7 +264,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
           o[j].z = h2_to_bf2_scaled(h2, sc2);
           o[j].w = h2_to_bf2_scaled(h3, sc2);
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&ab_empty[s], ((it / kGgS) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&a_empty[s], ((it / kGgSA) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
         uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -212,6 +212,11 @@ edge0_status edge0_residual_rmsnorm(const void *x, const void *y, void *out, int
  * (decode) runs all layers in one persistent kernel.  x, y device bf16
  * [T][hidden], may be the same buffer.  Larger T chains forward and
  * edge0_residual_rmsnorm per layer.
+ * The decode kernel reads a small device table of the layers, held by
+ * handles[0]: a call with a list of layers different from the previous call's
+ * uploads it (stream-ordered).  A call captured into a CUDA graph must use the
+ * list of the preceding uncaptured call on handles[0]; otherwise it returns
+ * EDGE0_ERR_UNSUPPORTED (the graph would reference host memory).
  */
 edge0_status edge0_moe_stack_forward(void *const *handles, int n_layers, const void *x,
                                      void *y, int T, float eps, edge0_stream_t stream);

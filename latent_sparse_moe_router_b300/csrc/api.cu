@@ -45,6 +45,7 @@ struct Handle {
   LayerW* d_layer = nullptr;  // this layer (1 entry)
   LayerW* d_stack = nullptr;  // kStackMax entries for stack calls
   PrefillWorkspace pf;        // prefill path buffers (T > 16)
+  std::vector<LayerW> stack_tab;  // the layer table last uploaded to d_stack
   int last_T = 0;
   int last_path = 0;          // 0 none, 1 decode, 2 prefill
 };
@@ -542,6 +543,16 @@ edge0_status edge0_residual_rmsnorm(const void* x, const void* y, void* out, int
   return launch_status();
 }
 
+static bool same_layers(const std::vector<LayerW>& a, const std::vector<LayerW>& b) {
+  if (a.size() != b.size()) return false;
+  for (size_t i = 0; i < a.size(); ++i)
+    if (a[i].D != b[i].D || a[i].U != b[i].U || a[i].RD != b[i].RD || a[i].bias != b[i].bias ||
+        a[i].experts != b[i].experts || a[i].shared != b[i].shared || a[i].stride != b[i].stride ||
+        a[i].dnorm != b[i].dnorm)
+      return false;
+  return true;
+}
+
 static edge0_status stack_impl(void* const* handles, int n_layers, const void* x, void* y, int T, float eps,
                                void* trace_x, void* trace_y, edge0_stream_t stream) {
   if (!handles || n_layers < 1 || T < 0 || !(eps >= 0.f)) return EDGE0_ERR_INVALID_ARG;
@@ -574,9 +585,18 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
   std::vector<LayerW> lws(n_layers);
   for (int i = 0; i < n_layers; ++i) lws[i] = layer_of(static_cast<const Handle*>(handles[i]));
   cudaStream_t s = (cudaStream_t)stream;
-  // pageable source: the copy is staged before the call returns
-  cudaError_t e = cudaMemcpyAsync(h0->d_stack, lws.data(), sizeof(LayerW) * n_layers, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return EDGE0_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  // the device layer table is uploaded only when the list of layers changes, so a
+  // call captured into a CUDA graph refers to device data alone
+  if (!same_layers(h0->stack_tab, lws)) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EDGE0_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return EDGE0_ERR_UNSUPPORTED;
+    // pageable source: the copy is staged before the call returns
+    e = cudaMemcpyAsync(h0->d_stack, lws.data(), sizeof(LayerW) * n_layers, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return EDGE0_ERR_CUDA;
+    h0->stack_tab = lws;
+  }
   DecodeArgs a;
   fill_decode_args(h0, a, x, y, T);
   a.layers = h0->d_stack;

@@ -260,3 +260,31 @@ def test_stack_teacher_forced_and_end_to_end(dev):
     assert np.array_equal(bits(cur), bits(y))
     for d in devs:
         d.close()
+
+
+def test_stack_forward_replays_from_a_cuda_graph(dev):
+    """A stack call captured into a CUDA graph (after one uncaptured call with the
+    same layers) replays to the same bits as the direct call."""
+    n_layers, T = 3, 1
+    specs = [small_spec(seed=40, layer=l) for l in range(n_layers)]
+    devs = [dev.DeviceLayer(synth.make_layer(s), max_tokens=16) for s in specs]
+    handles = [d.handle for d in devs]
+    H = specs[0].hidden
+    x = dev_bf16(synth.tokens_bf16(41, T, H))
+    y_direct = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ext.edge0_moe_stack_forward(handles, x, y_direct, T, 1e-6)
+    torch.cuda.synchronize()
+    y = torch.empty_like(y_direct)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ext.edge0_moe_stack_forward(handles, x, y, T, 1e-6, s)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(y), bits(y_direct))
+    assert ext.edge0_moe_get_error(handles[0]) == ext.EDGE0_OK
+    del g
+    for d in devs:
+        d.close()

@@ -46,6 +46,10 @@ DEFAULT_WORKLOAD = "prefill4x145b_t16384"
 HIDDEN, E, K, F = 2560, 512, 10, 640
 METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofline"
 MIN_TIMED_S = 2.0
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from one
+# ncu capture of this build's kernels (profiles/dram_traffic_grouped_decode.md)
+TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1518631936,
+           ("layer145b_t1", "moe_decode_kernel"): 45078016}
 
 
 def flops_per_token_layer(latent):
@@ -326,7 +330,7 @@ def run_decode(args, wl, rank, world, local):
     # the step is one kernel launch: its duration is the step time
     achieved_gbs = bytes_per_step / (ms_per_step / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved_gbs / hbm, 4), "traffic": None,
+            "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC.get((wl["name"], "moe_decode_kernel")),
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "kernel": "moe_decode_kernel", "bytes_per_launch": bytes_per_step, "note": work_note}
 
@@ -449,7 +453,7 @@ def run_prefill(args, wl, rank, world, local):
     if tname in sflops:
         ach = sflops[tname] / (stage_ms[top] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16_s, "unit": "TFLOP/s",
-                "frac": round(ach / bf16_s, 4), "traffic": None, "kernel": tname,
+                "frac": round(ach / bf16_s, 4), "traffic": TRAFFIC.get((wl["name"], tname)), "kernel": tname,
                 "flops_per_launch": sflops[tname],
                 "peak_kind": f"{peak_kind} cuBLAS bf16 sustained (kernel timed inside the step); "
                              f"frac of burst {bf16} = {ach / bf16:.4f}"}
@@ -524,7 +528,7 @@ def main():
                     help="override the number of rotated layer instances (profiling runs)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
-    wl = dict(WORKLOADS[args.workload])
+    wl = dict(WORKLOADS[args.workload], name=args.workload)
     if args.instances:
         wl["instances"] = args.instances
     rank, world, local = dist_setup(args.gpus)
@@ -559,7 +563,7 @@ def main():
         extra["layer_tok_s"] = round(r["layer_tok_s"], 1)
     # the metric's other half (T = 1 decode) on the same run
     if args.workload == DEFAULT_WORKLOAD and not args.no_decode:
-        dwl = dict(WORKLOADS["layer145b_t1"])
+        dwl = dict(WORKLOADS["layer145b_t1"], name="layer145b_t1")
         import torch
         torch.cuda.empty_cache()
         dr = run_decode(args, dwl, rank, world, local)

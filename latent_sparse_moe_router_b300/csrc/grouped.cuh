@@ -14,28 +14,30 @@
 // the CTAs working at one time share a few token tiles through L2.  Warp roles:
 //   warp 0 (one lane): TMA producer of the tile's E4M3 scales (double-buffered)
 //     and raw NVFP4 codes (4 KB per 64-wide k-step, 6-deep ring);
-//   warp 14 (one lane): TMA producer of the B rows the tile needs (64-row boxes,
+//   warp 18 (one lane): TMA producer of the B rows the tile needs (64-row boxes,
 //     128-byte swizzle), into the stages the MMA releases;
 //   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
 //     K=16, into one of two TMEM accumulators of 256 columns;
 //   warps 2-9: dequantisation, two threads per A row (E2M1 -> f16 by cvt, moved
 //     to the bf16 exponent range with shift/mask, times the block scale * 2^112
 //     in one bf16x2 multiply, all exact) into 128-byte-swizzled bf16 A tiles;
-//   warps 10-13: epilogue of the previous accumulator (TMEM -> registers ->
-//     shared-memory transpose -> whole-row global stores) while the next tile's
-//     main loop runs.
+//   warps 10-17: epilogue of the previous accumulator (TMEM -> registers ->
+//     shared-memory transpose -> whole-row global stores; two warps per TMEM lane
+//     quarter, one per half of each 32-column chunk) while the next tile's main
+//     loop runs.
 #pragma once
 
 #include "tc.cuh"
 
 namespace edge0 {
 
-constexpr int kGgThreads = 480;  // 15 warps
+constexpr int kGgThreads = 608;  // 19 warps
 constexpr int kGgDqWarp0 = 2;     // dequantisation warps 2..9
 constexpr int kGgDqThreads = 256;
 constexpr int kGgDqWarps = 8;
-constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..13
-constexpr int kGgBWarp = 14;      // B-tile producer
+constexpr int kGgEpWarp0 = 10;    // epilogue warps 10..17
+constexpr int kGgEpThreads = 256;
+constexpr int kGgBWarp = 18;      // B-tile producer
 constexpr int kGgBN = 256;        // token tile
 constexpr int kGgSA = 4;          // A (dequantised weight) stages
 constexpr int kGgSB = 3;          // B (token row) stages

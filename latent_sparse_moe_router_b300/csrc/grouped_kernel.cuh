@@ -113,7 +113,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     for (int s = 0; s < kGgR; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kGgDqWarps); }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sc_full[b], 1); mbar_init(&sc_empty[b], kGgDqWarps);
-      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kGgEpThreads / 32);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -280,11 +280,13 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       if (lane == 0) mbar_arrive(&sc_empty[sb]);
     }
   } else {
-    // ---- epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31 (A rows).
-    // Neighbouring lanes hold the row pair (2i, 2i+1); the even lane finishes token
-    // columns 0-15 of the chunk, the odd lane 16-31, after one shuffle each.
+    // ---- epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31 (A rows), and
+    // half ch of every 32-column chunk (columns 16 ch .. 16 ch + 15).  Neighbouring
+    // lanes hold the row pair (2i, 2i+1); after one shuffle per column pair the even
+    // lane finishes the half's first 8 token columns, the odd lane the last 8.
     const int q = warp & 3;
-    const int te = threadIdx.x - kGgEpWarp0 * 32;   // 0..127
+    const int te = threadIdx.x - kGgEpWarp0 * 32;   // 0..255
+    const int ch = te >> 7;
     const int odd = lane & 1, pr = q * 16 + (lane >> 1);   // row pair in the tile
     // mode 1: [32 tokens][72] bf16 (64 f used); mode 2: [32 tokens][68] u32 (64 latent pairs used)
     __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi);
@@ -293,57 +295,57 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
       const GgTile t = gg_tile(p, tile);
       const int ab = ti & 1;
-      // uniform across the four warps: all agree the accumulator is complete
+      // uniform across the epilogue warps: all agree the accumulator is complete
       ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, p.err, p.abort);
-      if (!named_and(1, 128, ok)) { ok = false; break; }
+      if (!named_and(1, kGgEpThreads, ok)) { ok = false; break; }
       tc_fence_after();
       const uint8_t* rec = t.shared ? p.shared : p.experts + size_t(t.g) * p.stride;
       const float* gl = reinterpret_cast<const float*>(rec + size_t(27) * p.F * p.L / 16);
       const float g0 = p.mode == 1 ? gl[0] : gl[2], g1 = gl[1];
-      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256;
-      const int tr = te >> 2, part = te & 3;
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256 + ch * 16;
+      const int tr = te >> 3, part = te & 7;
       for (int c = 0; c * 32 < t.n_rows; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + c * 32, v);
+        uint32_t v[16];
+        tmem_ld16(tbase + c * 32, v);
         tmem_ld_wait();
+        const int col0 = ch * 16 + odd * 8;   // first token column this lane finishes
         if (p.mode == 1) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t va = v[j], vb = v[16 + j];
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t va = v[j], vb = v[8 + j];
             const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
             const float gate = odd ? x : __uint_as_float(va);
             const float up = odd ? __uint_as_float(vb) : x;
-            hbuf[(odd * 16 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * gate) * (g1 * up));
+            hbuf[(col0 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * gate) * (g1 * up));
           }
-          named_sync(1, 128);
-          // 32 token rows x 64 f (128 B): 4 threads per row, 32 B each
+          named_sync(1, kGgEpThreads);
+          // 32 token rows x 64 f (128 B): 8 threads per row, 16 B each
           if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(hbuf + tr * 72 + part * 16);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 64 + part * 16);
+            const uint4* src = reinterpret_cast<const uint4*>(hbuf + tr * 72 + part * 8);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 64 + part * 8);
             dst[0] = src[0];
-            dst[1] = src[1];
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t va = v[j], vb = v[16 + j];
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t va = v[j], vb = v[8 + j];
             const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
             const float lo = odd ? x : __uint_as_float(va);            // latent row 2i
             const float hi = odd ? __uint_as_float(vb) : x;            // latent row 2i + 1
             const __nv_bfloat162 b = __floats2bfloat162_rn(g0 * lo, g0 * hi);
-            obuf[(odd * 16 + j) * 68 + pr] = *reinterpret_cast<const uint32_t*>(&b);
+            obuf[(col0 + j) * 68 + pr] = *reinterpret_cast<const uint32_t*>(&b);
           }
-          named_sync(1, 128);
-          // 32 token rows x 128 latent rows (256 B): 4 threads per row, 64 B each
+          named_sync(1, kGgEpThreads);
+          // 32 token rows x 128 latent rows (256 B): 8 threads per row, 32 B each
           if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(obuf + tr * 68 + part * 16);
+            const uint4* src = reinterpret_cast<const uint4*>(obuf + tr * 68 + part * 8);
             uint4* dst =
-                reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 128 + part * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) dst[u] = src[u];
+                reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 128 + part * 16);
+            dst[0] = src[0];
+            dst[1] = src[1];
           }
         }
-        named_sync(1, 128);
+        named_sync(1, kGgEpThreads);
       }
       // the accumulator's TMEM columns are free for the tile after next
       tc_fence_before();

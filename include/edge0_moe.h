@@ -178,9 +178,11 @@ edge0_status edge0_moe_debug_routing(void *handle, int *idx, float *w, int *coun
 /*
  * Copy an intermediate of the last forward (for stage-by-stage parity):
  *   what = 0: latent z [T][latent]; 1: router logits fp32 [T][n_experts];
- *   2: combined latent c [T][latent].  z and c are fp32 after a decode
- *   forward (T <= 16) and bf16 after a prefill forward (T > 16), the form
- *   in which the experts and U consume them.  dst device, `bytes` >= size.
+ *   2: combined latent c [T][latent].  After a decode forward (T <= 16) z and
+ *   c are fp32.  After a prefill forward (T > 16) they are in the form the
+ *   experts and U consume: z as f16 z_t * 2^-e_t, with e_t the binary exponent
+ *   of the bound max_r sum_h |D_rh| * max_h |x_t,h| (so every value is below 1
+ *   in magnitude), and c as bf16.  dst device, `bytes` >= size.
  * Returns UNSUPPORTED if no forward has run yet, INVALID_ARG for other `what`.
  */
 edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t bytes,

@@ -446,6 +446,7 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
     ce = cudaGetLastError();
   }
   if (ce == cudaSuccess) ce = cudaMemcpy(&hd->dnorm, d_dnorm, sizeof(float), cudaMemcpyDeviceToHost);
+  hd->pf.dnorm = hd->dnorm;
   const LayerW lw = layer_of(hd);
   if (ce == cudaSuccess) {
     fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256>>>(

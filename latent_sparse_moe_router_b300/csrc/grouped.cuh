@@ -5,8 +5,8 @@
 // "Edge0-145B en local", introduction).  Tokens are grouped by expert (positions
 // p of the permutation); a work tile is (group g, token tile nt, weight tile mt):
 //   MODE 1 (gate/up): A = 64 gate rows + 64 up rows (f0 = 64 mt), B = BN token
-//     rows of the group, K = l; epilogue h = silu(g_gate * gate) * (g_up * up),
-//     stored bf16 to H[p][f].
+//     rows of the group (z * 2^-e_t in f16), K = l; f16 operands; epilogue
+//     h = silu(g_gate 2^e_t gate) * (g_up 2^e_t up), stored bf16 to H[p][f].
 //   MODE 2 (down):    A = 128 latent rows (r0 = 128 mt, 64 row pairs), B = BN rows
 //     of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
 // Persistent CTAs (one per SM) walk the tiles in index order with a stride of
@@ -18,9 +18,10 @@
 //     128-byte swizzle), into the stages the MMA releases;
 //   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
 //     K=16, into one of two TMEM accumulators of 256 columns;
-//   warps 2-9: dequantisation, two threads per A row (E2M1 -> f16 by cvt, moved
-//     to the bf16 exponent range with shift/mask, times the block scale * 2^112
-//     in one bf16x2 multiply, all exact) into 128-byte-swizzled bf16 A tiles;
+//   warps 2-9: dequantisation, two threads per A row, exact: mode 1 E2M1 -> f16
+//     by cvt times the E4M3 scale in one f16x2 multiply; mode 2 the same f16
+//     moved to the bf16 exponent range with shift/mask and multiplied by the
+//     block scale * 2^112 in bf16x2; into 128-byte-swizzled A tiles;
 //   warps 10-17: epilogue of the previous accumulator (TMEM -> registers ->
 //     shared-memory transpose -> whole-row global stores; two warps per TMEM lane
 //     quarter, one per half of each 32-column chunk) while the next tile's main
@@ -70,6 +71,7 @@ struct GgParams {
   const uint8_t* shared;
   __nv_bfloat16* out;       // H [TK+T][F] (mode 1) or O [TK+T][L] (mode 2)
   int out_ld;
+  const float* pos_inv;     // mode 1: [TK+T] inverse scale of the f16 z row at each position
   int* err;
   int* abort;               // set when any wait gives up; every CTA then winds down
 };

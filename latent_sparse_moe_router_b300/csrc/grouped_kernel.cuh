@@ -33,6 +33,18 @@ __device__ __forceinline__ uint32_t h2_to_bf2_scaled(uint32_t h, uint32_t sc2) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// f16x2 (both halves) of an E4M3 scale (exact).
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e4m3) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(e4m3 | (e4m3 << 8))));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // bf16x2 (both halves) of an E4M3 scale times 2^112.
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t e4m3) {
   const float s = e4m3_to_f32(e4m3) * 5.192296858534828e33f;  // 2^112
@@ -199,7 +211,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
         const GgTile t = gg_tile(p, tile);
         const int n_mma = (t.n_rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(128, n_mma);
+        const uint32_t idesc = p.mode == 1 ? idesc_f16_f32(128, n_mma) : idesc_bf16_f32(128, n_mma);
         const int ab = ti & 1;
         if (!mbar_wait_abort(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
         tc_fence_after();
@@ -249,20 +261,31 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         const uint32_t s2 = *reinterpret_cast<const uint16_t*>(my_sc + kb * 4);
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rr]);
-        const uint32_t sc0 = scale_bf16x2(s2 & 0xFF), sc1 = scale_bf16x2(s2 >> 8);
         // dequantise into registers first: only the stores wait for the stage
         const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
         uint4 o[4];
+        if (p.mode == 1) {
+          const uint32_t sc0 = scale_f16x2(s2 & 0xFF), sc1 = scale_f16x2(s2 >> 8);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // 16-byte chunk c = 4 hh + j of the row: elements 8c .. 8c + 7, block c / 2
-          const uint32_t sc2 = j < 2 ? sc0 : sc1;
-          uint32_t h0, h1, h2, h3;
-          e2m1x8_to_h2x4(cw[j], h0, h1, h2, h3);
-          o[j].x = h2_to_bf2_scaled(h0, sc2);
-          o[j].y = h2_to_bf2_scaled(h1, sc2);
-          o[j].z = h2_to_bf2_scaled(h2, sc2);
-          o[j].w = h2_to_bf2_scaled(h3, sc2);
+          for (int j = 0; j < 4; ++j) {
+            // 16-byte chunk c = 4 hh + j of the row: elements 8c .. 8c + 7, block c / 2
+            const uint32_t sc2 = j < 2 ? sc0 : sc1;
+            uint32_t h0, h1, h2, h3;
+            e2m1x8_to_h2x4(cw[j], h0, h1, h2, h3);
+            o[j] = make_uint4(hmul2_u32(h0, sc2), hmul2_u32(h1, sc2), hmul2_u32(h2, sc2), hmul2_u32(h3, sc2));
+          }
+        } else {
+          const uint32_t sc0 = scale_bf16x2(s2 & 0xFF), sc1 = scale_bf16x2(s2 >> 8);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t sc2 = j < 2 ? sc0 : sc1;
+            uint32_t h0, h1, h2, h3;
+            e2m1x8_to_h2x4(cw[j], h0, h1, h2, h3);
+            o[j].x = h2_to_bf2_scaled(h0, sc2);
+            o[j].y = h2_to_bf2_scaled(h1, sc2);
+            o[j].z = h2_to_bf2_scaled(h2, sc2);
+            o[j].w = h2_to_bf2_scaled(h3, sc2);
+          }
         }
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&a_empty[s], ((it / kGgSA) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
         uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
@@ -316,7 +339,10 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
             const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
             const float gate = odd ? x : __uint_as_float(va);
             const float up = odd ? __uint_as_float(vb) : x;
-            hbuf[(col0 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * gate) * (g1 * up));
+            // undo the token's power-of-two scale of z (exact)
+            const int col = c * 32 + col0 + j;
+            const float zi = col < t.n_rows ? __ldg(&p.pos_inv[t.out0 + col]) : 1.0f;
+            hbuf[(col0 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * zi * gate) * (g1 * zi * up));
           }
           named_sync(1, kGgEpThreads);
           // 32 token rows x 64 f (128 B): 8 threads per row, 16 B each

@@ -4,16 +4,18 @@
 // router logits R z + b, top-k experts with renormalised softmax weights, the
 // k routed SwiGLU experts plus the shared expert on z, their weighted sum c,
 // y = U c.  At prefill sizes every step but routing is a contraction, so:
-//   1. one tcgen05 GEMM  x [T][H] x [D ; RDcat]^T -> zb bf16 [T][L] and logits
-//      fp32 [T][E]  (RDcat: the router folded into D once, R D in fp32, split into
-//      bf16 high and low rows so the tensor cores keep ~16 mantissa bits);
+//   0. per-token power-of-two scale 2^-e_t with |z_t| * 2^-e_t < 1, from the bound
+//      |z_t| <= max_r sum_h |D_rh| * max_h |x_t,h|;
+//   1. one tcgen05 GEMM  x [T][H] x [D ; RDcat]^T -> z * 2^-e_t in f16 [T][L] and
+//      logits fp32 [T][E]  (RDcat: the router folded into D once, R D in fp32, split
+//      into bf16 high and low rows so the tensor cores keep ~16 mantissa bits);
 //   2. top-k + softmax per token, expert histogram per 64-token chunk;
 //   3. per-expert scan over the chunks, expert offsets and token-tile prefix;
 //   4. deterministic scatter: slot s = t K + k goes to position
 //      offsets[e] + (number of earlier slots of expert e), i.e. ordered by (t, k);
-//   5. gather of the z rows in that order;
+//   5. gather of the z rows in that order (and of their scales);
 //   6. grouped NVFP4 GEMM gate/up + SwiGLU -> H bf16 (routed groups and the shared
-//      expert as group E);
+//      expert as group E; f16 operands, the token scale undone in the epilogue);
 //   7. grouped NVFP4 GEMM down -> O bf16;
 //   8. combine c[t] = O[shared t] + sum_k w[t,k] O[pos[t,k]] in fixed k order;
 //   9. tcgen05 GEMM  c x U^T -> y bf16 (round to nearest even).
@@ -50,22 +52,24 @@ __global__ void split_rd_kernel(const float* __restrict__ rd, __nv_bfloat16* __r
   }
 }
 
-// Epilogue of x [D ; RDcat]^T: latent columns -> zb bf16, router column pairs
-// (high, low) -> logits fp32 (+ bias).
+// Epilogue of x [D ; RDcat]^T: latent columns -> z * 2^-e_t in f16, router column
+// pairs (high, low) -> logits fp32 (+ bias).
 struct EpiXZ {
-  __nv_bfloat16* zb;
+  __half* zh;
+  const float* zsc;
   float* logits;
   const float* bias;
   int L, E;
   __device__ __forceinline__ void operator()(int row, int col0, const float* v) const {
     if (col0 < L) {
-      uint4* dst = reinterpret_cast<uint4*>(zb + size_t(row) * L + col0);
+      const float sc = zsc[row];
+      uint4* dst = reinterpret_cast<uint4*>(zh + size_t(row) * L + col0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t u[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+          const __half2 b = __floats2half2_rn(v[8 * q + 2 * i] * sc, v[8 * q + 2 * i + 1] * sc);
           u[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
         dst[q] = make_uint4(u[0], u[1], u[2], u[3]);
@@ -342,17 +346,47 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int* __restrict__ id
   }
 }
 
-// zg[p] = zb[perm[p] / K]: one warp per row, 16-byte copies.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ zb,
+// Per-token scale: e_t = exponent of dnorm * max_h |x_t,h| (frexp: the bound lies in
+// [2^(e-1), 2^e)), zsc = 2^-e_t, zinv = 2^e_t; the shared expert's positions
+// TK + t take zinv too.  One warp per token.
+__global__ void __launch_bounds__(256) token_scale_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
+                                                          float dnorm, int TK, float* __restrict__ zsc,
+                                                          float* __restrict__ zinv, float* __restrict__ pos_inv) {
+  const int lane = threadIdx.x & 31, t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const uint4* xv = reinterpret_cast<const uint4*>(x + size_t(t) * H);
+  uint32_t m = 0;   // max |x| as bits (non-negative floats order as integers)
+  for (int g = lane; g < H / 8; g += 32) {
+    const uint4 a = xv[g];
+    const uint32_t aa[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max((aa[i] << 16) & 0x7FFF0000u, aa[i] & 0x7FFF0000u));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) {
+    const float bound = __uint_as_float(m) * dnorm;
+    int e = 0;
+    if (bound > 0.f && isfinite(bound)) frexpf(bound, &e);
+    zsc[t] = ldexpf(1.0f, -e);
+    zinv[t] = ldexpf(1.0f, e);
+    pos_inv[TK + t] = ldexpf(1.0f, e);
+  }
+}
+
+// zg[p] = zh[perm[p] / K] and its scale: one warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restrict__ zh,
+                                                          const float* __restrict__ zinv,
                                                           const int* __restrict__ perm, int TK, int K, int L,
-                                                          __nv_bfloat16* __restrict__ zg) {
+                                                          __half* __restrict__ zg, float* __restrict__ pos_inv) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n16 = L / 8;
   for (int p = blockIdx.x * 8 + warp; p < TK; p += gridDim.x * 8) {
     const int t = perm[p] / K;
-    const uint4* src = reinterpret_cast<const uint4*>(zb + size_t(t) * L);
+    const uint4* src = reinterpret_cast<const uint4*>(zh + size_t(t) * L);
     uint4* dst = reinterpret_cast<uint4*>(zg + size_t(p) * L);
     for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+    if (lane == 0) pos_inv[p] = zinv[t];
   }
 }
 
@@ -412,7 +446,9 @@ size_t prefill_workspace_bytes(const edge0_moe_desc& d, int max_tokens) {
   const size_t nch = (T + kChunk - 1) / kChunk;
   size_t n = 0;
   n += pf_align(2 * E * H * 2);               // rdcat
-  n += pf_align(T * L * 2);                   // zb
+  n += pf_align(T * L * 2);                   // zh
+  n += pf_align(T * 4) * 2;                   // zsc, zinv
+  n += pf_align((T * K + T) * 4);             // pos_inv
   n += pf_align(T * E * 4);                   // logits
   n += pf_align(nch * E * 4);                 // chunk_cnt
   n += pf_align((E + 2) * 4);                 // tprefix
@@ -433,11 +469,14 @@ void prefill_workspace_carve(const edge0_moe_desc& d, int max_tokens, char* base
   size_t o = 0;
   auto take = [&](size_t bytes) { char* p = base + o; o += pf_align(bytes); return p; };
   pf->rdcat = reinterpret_cast<__nv_bfloat16*>(take(2 * E * H * 2));
-  pf->zb = reinterpret_cast<__nv_bfloat16*>(take(T * L * 2));
+  pf->zh = reinterpret_cast<__half*>(take(T * L * 2));
+  pf->zsc = reinterpret_cast<float*>(take(T * 4));
+  pf->zinv = reinterpret_cast<float*>(take(T * 4));
+  pf->pos_inv = reinterpret_cast<float*>(take((T * K + T) * 4));
   pf->logits = reinterpret_cast<float*>(take(T * E * 4));
   pf->chunk_cnt = reinterpret_cast<int*>(take(nch * E * 4));
   pf->tprefix = reinterpret_cast<int*>(take((E + 2) * 4));
-  pf->zg = reinterpret_cast<__nv_bfloat16*>(take(T * K * L * 2));
+  pf->zg = reinterpret_cast<__half*>(take(T * K * L * 2));
   pf->hb = reinterpret_cast<__nv_bfloat16*>(take((T * K + T) * F * 2));
   pf->ob = reinterpret_cast<__nv_bfloat16*>(take((T * K + T) * L * 2));
   pf->cb = reinterpret_cast<__nv_bfloat16*>(take(T * L * 2));
@@ -468,8 +507,9 @@ cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_
   ok &= make_tmap_3d(&pf->maps1.a_scales, ex, U8, gu_row, F, E, gu_row, d.expert_stride, L / 16, 64, 1, NS);
   ok &= make_tmap_2d(&pf->maps1.s_codes, sh, U8, 1, F, gu_row, gu_row, 32, 64, NS);
   ok &= make_tmap_2d(&pf->maps1.s_scales, sh, U8, 1, F, gu_row, gu_row, L / 16, 64, NS);
-  ok &= make_tmap_2d(&pf->maps1.b_routed, pf->zg, BF, 2, TK, L, uint64_t(L) * 2, 64, kGgBBox, SW);
-  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zb, BF, 2, T, L, uint64_t(L) * 2, 64, kGgBBox, SW);
+  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  ok &= make_tmap_2d(&pf->maps1.b_routed, pf->zg, F16, 2, TK, L, uint64_t(L) * 2, 64, kGgBBox, SW);
+  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zh, F16, 2, T, L, uint64_t(L) * 2, 64, kGgBBox, SW);
   // down: records' D blocks [E][L/2 row pairs][9F/8 bytes]
   ok &= make_tmap_3d(&pf->maps2.a_codes, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, 32, 64, 1, NS);
   ok &= make_tmap_3d(&pf->maps2.a_scales, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, F / 8, 64, 1,
@@ -498,10 +538,15 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
     if (pf->profile && e == cudaSuccess) e = cudaEventRecord(pf->events[stage++], s);
   };
   mark();
-  // 1. x -> zb, logits
+  // 0. token scales
+  if (e == cudaSuccess) {
+    token_scale_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, pf->dnorm, TK, pf->zsc, pf->zinv, pf->pos_inv);
+    e = cudaGetLastError();
+  }
+  // 1. x -> z (f16, scaled), logits
   if (e == cudaSuccess)
     e = launch_gemm_tn<kPfBN, kPfStages>(mx, pf->m_D, pf->m_rdcat, T, L + 2 * E, H, L, pf->err, pf->abort,
-                                         EpiXZ{pf->zb, pf->logits, d.router_bias, L, E}, s);
+                                         EpiXZ{pf->zh, pf->zsc, pf->logits, d.router_bias, L, E}, s);
   mark();
   // 2-4. routing and permutation
   if (e == cudaSuccess) {
@@ -527,7 +572,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   // 5. grouped z rows
   if (e == cudaSuccess) {
     const int blocks = std::min((TK + 7) / 8, num_sms * 16);
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(pf->zb, pf->perm, TK, K, L, pf->zg);
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(pf->zh, pf->zinv, pf->perm, TK, K, L, pf->zg, pf->pos_inv);
     e = cudaGetLastError();
   }
   mark();
@@ -541,12 +586,12 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   gp.err = pf->err;
   gp.abort = pf->abort;
   if (e == cudaSuccess) {
-    gp.mode = 1; gp.mtiles = F / 64; gp.out = pf->hb; gp.out_ld = F;
+    gp.mode = 1; gp.mtiles = F / 64; gp.out = pf->hb; gp.out_ld = F; gp.pos_inv = pf->pos_inv;
     e = launch_grouped(pf->maps1, gp, num_sms, s);
   }
   mark();
   if (e == cudaSuccess) {
-    gp.mode = 2; gp.mtiles = L / 128; gp.out = pf->ob; gp.out_ld = L;
+    gp.mode = 2; gp.mtiles = L / 128; gp.out = pf->ob; gp.out_ld = L; gp.pos_inv = nullptr;
     e = launch_grouped(pf->maps2, gp, num_sms, s);
   }
   mark();
@@ -568,7 +613,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
 const void* prefill_debug_tensor(const PrefillWorkspace* pf, int what, const edge0_moe_desc& d, int T,
                                  size_t* bytes) {
   if (!pf->rdcat) return nullptr;
-  if (what == 0) { *bytes = size_t(T) * d.latent * 2; return pf->zb; }
+  if (what == 0) { *bytes = size_t(T) * d.latent * 2; return pf->zh; }
   if (what == 1) { *bytes = size_t(T) * d.n_experts * 4; return pf->logits; }
   if (what == 2) { *bytes = size_t(T) * d.latent * 2; return pf->cb; }
   return nullptr;

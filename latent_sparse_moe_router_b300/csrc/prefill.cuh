@@ -15,13 +15,18 @@ struct PrefillWorkspace {
   int* perm = nullptr; int* pos = nullptr;
   int* err = nullptr;
   const float* rd = nullptr;        // folded router R D, fp32 [E][hidden] (handle-owned)
+  float dnorm = 0.f;                // max_r sum_h |D[r][h]|
   // prefill buffers (carved from the handle's workspace)
   __nv_bfloat16* rdcat = nullptr;   // [2E][hidden]: rows 2e, 2e+1 = bf16 high / low parts of R D row e
-  __nv_bfloat16* zb = nullptr;      // [T][latent]  z rounded to bf16
+  __half* zh = nullptr;             // [T][latent]  z * 2^-e_t in f16 (e_t: exponent of the bound
+                                    //               dnorm * max|x_t| of |z_t|, so |z * 2^-e_t| < 1)
+  float* zsc = nullptr;             // [T] 2^-e_t
+  float* zinv = nullptr;            // [T] 2^e_t
+  float* pos_inv = nullptr;         // [T K + T] 2^e_t of the token at each grouped position
   float* logits = nullptr;          // [T][E]
   int* chunk_cnt = nullptr;         // [T/64][E] per-chunk expert counts, then per-chunk bases
   int* tprefix = nullptr;           // [E+2] token-tile prefix of the expert groups (+ shared)
-  __nv_bfloat16* zg = nullptr;      // [T K][latent] z rows in expert-grouped order
+  __half* zg = nullptr;             // [T K][latent] zh rows in expert-grouped order
   __nv_bfloat16* hb = nullptr;      // [T K + T][ffn] SwiGLU activations (routed, then shared)
   __nv_bfloat16* ob = nullptr;      // [T K + T][latent] expert outputs (routed, then shared)
   __nv_bfloat16* cb = nullptr;      // [T][latent] combined latent

@@ -118,6 +118,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// Instruction descriptor: kind::f16 with f16 A and B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
 // Byte offset of element (row r, column k) of a [rows x 64] bf16 tile in the
 // 128-byte swizzled layout (16-byte chunks of a row XOR-ed with the row % 8).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {

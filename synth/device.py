@@ -123,10 +123,12 @@ class DeviceLayer:
 
     def debug_tensor(self, what: int, T: int):
         """Stage tensor of the last forward as float64 [T, n]: z (0), logits (1), c (2).
-        z and c are fp32 on the decode path (T <= 16) and bf16 on the prefill path."""
+        z and c are fp32 on the decode path (T <= 16); on the prefill path z is f16
+        times a per-token power of two and c is bf16."""
         n = {0: self.spec.latent, 1: self.spec.n_experts, 2: self.spec.latent}[what]
         if T > 16 and what in (0, 2):
-            out = torch.empty(T * n, dtype=torch.bfloat16, device="cuda")
+            # prefill: z as f16 scaled by a power of two per token, c as bf16
+            out = torch.empty(T * n, dtype=torch.float16 if what == 0 else torch.bfloat16, device="cuda")
             ext.edge0_moe_debug_tensor(self.handle, what, out, out.numel() * 2)
             torch.cuda.synchronize()
             return out.float().cpu().numpy().astype(np.float64).reshape(T, n)

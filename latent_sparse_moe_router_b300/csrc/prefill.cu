@@ -179,9 +179,10 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float* __restrict_
 }
 
 // The same for E = 32 NJ with each lane's NJ logits in registers (no shared-memory
-// pass per selection round): one warp per token, 8 tokens per warp, 64 per block.
+// pass per selection round): one warp per token, 16 warps of 4 tokens per block
+// of 64 tokens.
 template <int NJ>
-__global__ void __launch_bounds__(256) topk_hist_reg_kernel(const float* __restrict__ logits, int T, int K,
+__global__ void __launch_bounds__(512) topk_hist_reg_kernel(const float* __restrict__ logits, int T, int K,
                                                             int* __restrict__ idx, float* __restrict__ w,
                                                             int* __restrict__ chunk_cnt) {
   constexpr int E = NJ * 32;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(256) topk_hist_reg_kernel(const float* __restr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int tt = warp; tt < kChunk; tt += 8) {
+  for (int tt = warp; tt < kChunk; tt += 16) {
     const int t = blockIdx.x * kChunk + tt;
     if (t >= T) break;
     const float* row = logits + size_t(t) * E;
@@ -238,10 +239,10 @@ cudaError_t launch_topk_hist(const float* logits, int T, int E, int K, int* idx,
                              cudaStream_t s) {
   const int nch = (T + kChunk - 1) / kChunk;
   switch (E / 32) {
-    case 2: topk_hist_reg_kernel<2><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
-    case 4: topk_hist_reg_kernel<4><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
-    case 8: topk_hist_reg_kernel<8><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
-    case 16: topk_hist_reg_kernel<16><<<nch, 256, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 2: topk_hist_reg_kernel<2><<<nch, 512, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 4: topk_hist_reg_kernel<4><<<nch, 512, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 8: topk_hist_reg_kernel<8><<<nch, 512, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
+    case 16: topk_hist_reg_kernel<16><<<nch, 512, 0, s>>>(logits, T, K, idx, w, chunk_cnt); break;
     default: topk_hist_kernel<<<nch, 256, (8 * E + E) * 4, s>>>(logits, T, E, K, idx, w, chunk_cnt);
   }
   return cudaGetLastError();

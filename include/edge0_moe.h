@@ -182,7 +182,10 @@ edge0_status edge0_moe_debug_routing(void *handle, int *idx, float *w, int *coun
  *   c are fp32.  After a prefill forward (T > 16) they are in the form the
  *   experts and U consume: z as f16 z_t * 2^-e_t, with e_t the binary exponent
  *   of the bound max_r sum_h |D_rh| * max_h |x_t,h| (so every value is below 1
- *   in magnitude), and c as bf16.  dst device, `bytes` >= size.
+ *   in magnitude), and c as bf16.  After a prefill forward also what = 3: the
+ *   SwiGLU activations H bf16 [T*top_k + T][ffn] and 4: the expert outputs O
+ *   bf16 [T*top_k + T][latent], rows in grouped position order (the shared
+ *   expert's T rows last).  dst device, `bytes` >= size.
  * Returns UNSUPPORTED if no forward has run yet, INVALID_ARG for other `what`.
  */
 edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t bytes,

@@ -527,7 +527,7 @@ edge0_status edge0_moe_debug_tensor(void* handle, int what, void* dst, size_t by
   } else {
     src = prefill_debug_tensor(&hd->pf, what, hd->d, (int)T, &n);
   }
-  if (!src) return what >= 0 && what <= 2 ? EDGE0_ERR_UNSUPPORTED : EDGE0_ERR_INVALID_ARG;
+  if (!src) return what >= 0 && what <= 4 ? EDGE0_ERR_UNSUPPORTED : EDGE0_ERR_INVALID_ARG;
   if (bytes < n) return EDGE0_ERR_INVALID_ARG;
   return cuda_status(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
 }

@@ -259,8 +259,6 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&raw_full[rr], (it / kGgR) & 1, p.err, p.abort))) { ok = false; break; }
         const uint4 cw4 = *reinterpret_cast<const uint4*>(smem + GgSmem::offRaw + rr * GgSmem::kRaw + raw_off);
         const uint32_t s2 = *reinterpret_cast<const uint16_t*>(my_sc + kb * 4);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rr]);
         // dequantise into registers first: only the stores wait for the stage
         const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
         uint4 o[4];
@@ -287,6 +285,12 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
             o[j].w = h2_to_bf2_scaled(h3, sc2);
           }
         }
+        // the raw stage is released only once every lane's codes and scales have been
+        // consumed into registers (the arithmetic above depends on both loads): a
+        // release straight after the loads let the next TMA fill overwrite the first
+        // half of the stage while a lane's read was still outstanding
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rr]);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&a_empty[s], ((it / kGgSA) & 1) ^ 1, p.err, p.abort))) { ok = false; break; }
         uint8_t* arow = smem + GgSmem::offA + s * GgSmem::kA + r * 128;
 #pragma unroll

@@ -617,6 +617,9 @@ const void* prefill_debug_tensor(const PrefillWorkspace* pf, int what, const edg
   if (what == 0) { *bytes = size_t(T) * d.latent * 2; return pf->zh; }
   if (what == 1) { *bytes = size_t(T) * d.n_experts * 4; return pf->logits; }
   if (what == 2) { *bytes = size_t(T) * d.latent * 2; return pf->cb; }
+  const size_t rows = size_t(T) * d.top_k + T;
+  if (what == 3) { *bytes = rows * d.ffn * 2; return pf->hb; }
+  if (what == 4) { *bytes = rows * d.latent * 2; return pf->ob; }
   return nullptr;
 }
 

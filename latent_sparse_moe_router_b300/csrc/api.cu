@@ -82,7 +82,8 @@ void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
   size_t off = decode_tables_bytes();
   // x (P0 only) and the fp32 activations (P1, P3) are never live together
   size_t act = TB * (size_t)(L > E ? L : E) * 4;
-  if (TB * (size_t)H * 2 > act) act = TB * (size_t)H * 2;
+  // P0 of a stacked layer: x [T][H] bf16 and the norm's group sums [T][H/8] fp32
+  if (TB * (size_t)H * 5 / 2 > act) act = TB * (size_t)H * 5 / 2;
   const size_t cand = TB * (size_t)((E + 31) / 32) * 16 * 8 * 3 / 2 + 16 * 8;   // top-k lists
   if (cand > act) act = cand;
   a.off_xs = (int)off;

@@ -98,6 +98,13 @@ __device__ __forceinline__ bool mbar_wait_abort(uint64_t* bar, uint32_t parity, 
 // ---------------------------------------------------------------- bulk copies
 // Global -> shared bulk copy (TMA, non-tensor), completion counted on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
+// 16 bytes global -> shared without a register round trip (completion: cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
   asm volatile(
@@ -205,24 +212,41 @@ __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
 }
 
 // ---------------------------------------------------------------- residual RMSNorm
-// Sum over one token row of (x + y)^2 (bf16 inputs, fp32 sums) by one warp: lane l
-// takes the 16-byte groups l, l + 32, ... (8 values each, fmaf in order), then the
-// 32 lane sums meet in an xor tree.  The one summation order of the library's
-// residual norms (the stacked decode kernel and the standalone kernel).  H % 8 == 0.
+// The library's one summation order for sum((x + y)^2) over a token row (bf16 inputs,
+// fp32 sums), shared by the stacked decode kernel and the standalone kernel:
+//   group_sumsq: the 8 squares of one 16-byte group, fmaf in element order from 0;
+//   the group sums of a row are added by lane l = g mod 32 in increasing g;
+//   the 32 lane sums meet in an xor tree.  H % 8 == 0.
+__device__ __forceinline__ float group_sumsq(uint4 a, uint4 b) {
+  const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float v0 = __uint_as_float(aa[i] << 16) + __uint_as_float(bb[i] << 16);
+    const float v1 = __uint_as_float(aa[i] & 0xFFFF0000u) + __uint_as_float(bb[i] & 0xFFFF0000u);
+    s = fmaf(v0, v0, s);
+    s = fmaf(v1, v1, s);
+  }
+  return s;
+}
+
+// One row by one warp (loads of four groups in flight together).
 __device__ __forceinline__ float row_sumsq_warp(const __nv_bfloat16* x, const __nv_bfloat16* y, int H, int lane) {
   float s = 0.f;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const uint4* yv = reinterpret_cast<const uint4*>(y);
-  for (int g = lane; g < H / 8; g += 32) {
-    const uint4 a = xv[g], b = yv[g];
-    const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+  const int ng = H / 8;
+  for (int g0 = lane; g0 < ng; g0 += 4 * 32) {
+    uint4 a[4], b[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float v0 = __uint_as_float(aa[i] << 16) + __uint_as_float(bb[i] << 16);
-      const float v1 = __uint_as_float(aa[i] & 0xFFFF0000u) + __uint_as_float(bb[i] & 0xFFFF0000u);
-      s = fmaf(v0, v0, s);
-      s = fmaf(v1, v1, s);
+    for (int j = 0; j < 4; ++j) {
+      const int g = g0 + 32 * j;
+      a[j] = g < ng ? xv[g] : make_uint4(0u, 0u, 0u, 0u);
+      b[j] = g < ng ? yv[g] : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (g0 + 32 * j < ng) s += group_sumsq(a[j], b[j]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);

@@ -88,7 +88,8 @@ __device__ __forceinline__ void row_dot(const uint8_t* wrow, int K, const void* 
 // acc[i] += sum_k e2m1(code[k]) * e4m3(scale[k/16]) * act_i[k] for n activation
 // rows (f16, pre-scaled).  Lane l of a group of nl lanes takes blocks l, l+nl, ...
 // Products of one 16-block are summed in f16x2 (two chains of 4 per half); the
-// block sum is scaled and accumulated in fp32.
+// block sum is scaled and accumulated in fp32.  With TB == 1 the single activation
+// row is used unconditionally (callers pass a valid row when n == 0).
 template <int TB>
 __device__ __forceinline__ void fp4_dot(const uint8_t* codes, const uint8_t* scales, int nblk,
                                         const __half* const* arow, int n, int l, int nl,
@@ -108,7 +109,7 @@ __device__ __forceinline__ void fp4_dot(const uint8_t* codes, const uint8_t* sca
     wv[7] = u32_as_h2(e2m1x2_to_h2(cw.y >> 24));
 #pragma unroll
     for (int i = 0; i < TB; ++i) {
-      if (i < n) {
+      if (TB == 1 || i < n) {
         const uint4* ap = reinterpret_cast<const uint4*>(arow[i] + b * 16);
         const uint4 a0 = ap[0], a1 = ap[1];
         __half2 p = __hmul2(wv[0], u32_as_h2(a0.x));
@@ -196,13 +197,13 @@ __device__ __forceinline__ int dense_cap(const RowSet* rs, int nset, int dyn_byt
   return min(512, dyn_bytes / maxrb);
 }
 
-// Rows of the sets, round by round, one half-warp per row; out_fn(m, t, row, v).
+// Rows of the sets, round by round, one warp per row; out_fn(m, t, row, v).
 // With `prestaged`, warp 0 already ran stage_rows for the first round
 // (rows [0, min(cap, total))) before the CTA's last __syncthreads.
 template <int TB, bool ACT_F32, class OutFn>
 __device__ void dense_rows(Ctx& cx, const RowSet* rs, int nset, const void* act, int K, int T,
                            uint8_t* dyn, int dyn_bytes, bool prestaged, OutFn out_fn) {
-  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
+  const int wv = threadIdx.x >> 5, wl = threadIdx.x & 31;
   int total = 0;
   for (int m = 0; m < nset; ++m) total += rs[m].r1 - rs[m].r0;
   const int n0 = rs[0].r1 - rs[0].r0;
@@ -213,22 +214,17 @@ __device__ void dense_rows(Ctx& cx, const RowSet* rs, int nset, const void* act,
       if (threadIdx.x < 32) stage_rows(cx, rs, nset, from, n, dyn);
     }
     const RoundRows rr = round_rows(rs, nset, from, n);
-    // both halves of a warp run the same trip count (shuffles in group_reduce)
-    for (int base = (hw & ~1); base < n; base += kDecThreads / 16) {
-      const int i = base + (hw & 1);
-      const bool valid = i < n;
-      const int m = (valid && i >= rr.c0) ? 1 : 0;
-      if (valid) wait_mb(cx, kMbRound + rr.batch(i));
+    for (int i = wv; i < n; i += kDecWarps) {
+      const int m = i >= rr.c0 ? 1 : 0;
+      wait_mb(cx, kMbRound + rr.batch(i));
       float acc[TB];
 #pragma unroll
       for (int t = 0; t < TB; ++t) acc[t] = 0.f;
-      if (valid) {
-        const uint8_t* wrow = dyn + rr.offset(i);
-        if (rs[m].f32) row_dot<TB, true, ACT_F32>(wrow, K, act, T, hl, 16, acc);
-        else row_dot<TB, false, ACT_F32>(wrow, K, act, T, hl, 16, acc);
-      }
-      group_reduce<TB>(acc, 16);
-      if (valid && hl == 0) {
+      const uint8_t* wrow = dyn + rr.offset(i);
+      if (rs[m].f32) row_dot<TB, true, ACT_F32>(wrow, K, act, T, wl, 32, acc);
+      else row_dot<TB, false, ACT_F32>(wrow, K, act, T, wl, 32, acc);
+      group_reduce<TB>(acc, 32);
+      if (wl == 0) {
         const int q = from + i;
         const int row = q < n0 ? rs[0].r0 + q : rs[1].r0 + (q - n0);
 #pragma unroll
@@ -292,20 +288,68 @@ __device__ __forceinline__ void pow2_scale(float maxabs, float* sc, float* inv) 
 }
 
 // x_out = bf16(v / sqrt(mean(v^2) + eps)), v = x + y, for T rows of H (all threads of
-// the CTA; the summation order matches edge0_residual_rmsnorm's kernel).
+// the CTA), in the library's one summation order (group_sumsq per 16-byte group, the
+// group sums of a row added by lane l = g mod 32 in order, then the xor tree), which
+// edge0_residual_rmsnorm's kernel shares.  Every thread's first loads are issued
+// before `hook()` runs (once per thread); the group sums go to `part` [T][H/8].
+template <class Hook>
 __device__ void residual_norm(DecTables* tb, const __nv_bfloat16* xp, const __nv_bfloat16* yp,
-                              __nv_bfloat16* xs, int T, int H, float eps) {
+                              __nv_bfloat16* xs, float* part, int T, int H, float eps, Hook hook) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // warp t reduces token t (T <= 16 warps), in the library's one summation order
-  if (warp < T) {
-    const float s = row_sumsq_warp(xp + size_t(warp) * H, yp + size_t(warp) * H, H, lane);
-    if (lane == 0) tb->inv_rms[warp] = 1.0f / sqrtf(s / float(H) + eps);
+  const int ng = T * H / 8, gpr = H / 8;
+  const uint4* xv = reinterpret_cast<const uint4*>(xp);
+  const uint4* yv = reinterpret_cast<const uint4*>(yp);
+  bool hooked = false;
+  for (int g0 = tid; g0 < ng || !hooked; g0 += 4 * kDecThreads) {
+    uint4 ga[4], gb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g = g0 + j * kDecThreads;
+      ga[j] = g < ng ? xv[g] : make_uint4(0u, 0u, 0u, 0u);
+      gb[j] = g < ng ? yv[g] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (!hooked) { hook(); hooked = true; }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g = g0 + j * kDecThreads;
+      if (g < ng) part[g] = group_sumsq(ga[j], gb[j]);
+    }
   }
   __syncthreads();
-  for (int i = tid; i < T * H; i += kDecThreads) {
-    const int t = i / H;
-    const float v = __bfloat162float(xp[i]) + __bfloat162float(yp[i]);
-    xs[i] = __float2bfloat16_rn(v * tb->inv_rms[t]);
+  if (warp < T) {
+    float sum = 0.f;
+    for (int g = lane; g < gpr; g += 32) sum += part[size_t(warp) * gpr + g];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (lane == 0) tb->inv_rms[warp] = 1.0f / sqrtf(sum / float(H) + eps);
+  }
+  __syncthreads();
+  // 16-byte groups, four per thread in flight together
+  for (int g0 = tid; g0 < ng; g0 += 4 * kDecThreads) {
+    uint4 ga[4], gb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g = g0 + j * kDecThreads;
+      ga[j] = g < ng ? xv[g] : make_uint4(0u, 0u, 0u, 0u);
+      gb[j] = g < ng ? yv[g] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g = g0 + j * kDecThreads;
+      if (g < ng) {
+        const float inv = tb->inv_rms[g / gpr];
+        const uint32_t aa[4] = {ga[j].x, ga[j].y, ga[j].z, ga[j].w}, bb[4] = {gb[j].x, gb[j].y, gb[j].z, gb[j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float v0 = __uint_as_float(aa[i] << 16) + __uint_as_float(bb[i] << 16);
+          const float v1 = __uint_as_float(aa[i] & 0xFFFF0000u) + __uint_as_float(bb[i] & 0xFFFF0000u);
+          const __nv_bfloat162 r = __floats2bfloat162_rn(v0 * inv, v1 * inv);
+          o[i] = *reinterpret_cast<const uint32_t*>(&r);
+        }
+        reinterpret_cast<uint4*>(xs)[g] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
   }
   __syncthreads();
 }
@@ -367,7 +411,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   const int nr = r1 - r0, nsr = f1 - f0;
 
   if (tid == 0) {
-    for (int b = 0; b < kNumMbar; ++b) mbar_init(&tb->mbar[b], 1);
+    for (int b = 0; b < kNumMbar; ++b) mbar_init(&tb->mbar[b], b == kMbScale ? kScaleWarps : 1);
     fence_mbar_init();
     tb->stuck = 0;
   }
@@ -379,24 +423,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     __nv_bfloat16* xcur = a.xbuf + size_t(li & 1) * T * H;
     // ================================================================ P0: z = D x, l = (R D) x + b
     {
-      // shared-expert gate/up rows of this CTA, consumed in P1
-      if (tid == 0 && nsr > 0) {
-        mbar_arrive_expect_tx(&tb->mbar[kMbShared], uint32_t(nsr) * gu_row);
-        bulk_g2s(shr, lw.shared + size_t(f0) * gu_row, uint32_t(nsr) * gu_row, &tb->mbar[kMbShared]);
+      // the shared expert's fp32 scales: loaded now, stored at the end of the phase
+      float2 sh_gu = make_float2(0.f, 0.f);
+      float sh_d = 0.f;
+      if (tid == 32) {
+        const float* gs = reinterpret_cast<const float*>(lw.shared + rec_body);
+        sh_gu = *reinterpret_cast<const float2*>(gs);
+        sh_d = gs[2];
       }
-      RowSet rs[2] = {{reinterpret_cast<const uint8_t*>(lw.D), r0, r1, H * 2, 0},
-                      {reinterpret_cast<const uint8_t*>(lw.RD), e0, e1, H * 4, 1}};
-      // the weight rows are in flight before x is even read
-      if (warp == 0 && nr + (e1 - e0) > 0)
-        stage_rows(cx, rs, 2, 0, min(dense_cap(rs, 2, a.dyn_bytes), nr + (e1 - e0)), dyn);
+      // router rows first: they are the longer ones (fp32) and feed the routing
+      RowSet rs[2] = {{reinterpret_cast<const uint8_t*>(lw.RD), e0, e1, H * 4, 1},
+                      {reinterpret_cast<const uint8_t*>(lw.D), r0, r1, H * 2, 0}};
+      // this CTA's router bias entries, in flight while x is read
+      const int ne = e1 - e0;
+      const int bj = tid - (kDecThreads - 32);          // lanes of the last warp
+      const float bv = (bj >= 0 && bj < ne && lw.bias) ? lw.bias[e0 + bj] : 0.f;
+      // the weight rows and the shared-expert rows (P1) go out right after x's loads,
+      // so that those few loads are not queued behind the bulk copies
+      auto stage = [&]() {
+        if (warp == 0 && nr + (e1 - e0) > 0)
+          stage_rows(cx, rs, 2, 0, min(dense_cap(rs, 2, a.dyn_bytes), (e1 - e0) + nr), dyn);
+        if (tid == 32 && nsr > 0) {
+          mbar_arrive_expect_tx(&tb->mbar[kMbShared], uint32_t(nsr) * gu_row);
+          bulk_g2s(shr, lw.shared + size_t(f0) * gu_row, uint32_t(nsr) * gu_row, &tb->mbar[kMbShared]);
+        }
+      };
       if (li == 0) {
         for (int i = tid; i < T * H / 8; i += kDecThreads)
-          reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
+          cp_async16(reinterpret_cast<uint4*>(xs) + i, reinterpret_cast<const uint4*>(a.x) + i);
+        cp_async_commit();
+        stage();
+        cp_async_wait_all();
         __syncthreads();
       } else {
         // x_l = bf16(RMSNorm(x_{l-1} + y_{l-1})), computed by every CTA
         residual_norm(tb, a.xbuf + size_t((li - 1) & 1) * T * H, a.ybuf + size_t((li - 1) & 1) * T * H,
-                      xs, T, H, a.eps);
+                      xs, reinterpret_cast<float*>(xs + size_t(T) * H), T, H, a.eps, stage);
       }
       if (bid == 0) {
         for (int i = tid; i < T * H / 8; i += kDecThreads)
@@ -405,6 +467,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           for (int i = tid; i < T * H / 8; i += kDecThreads)
             reinterpret_cast<uint4*>(a.trace_x + size_t(li) * T * H)[i] = reinterpret_cast<const uint4*>(xs)[i];
       }
+      if (bj >= 0 && bj < ne) tb->w[bj] = bv;       // read after the barriers below
       // per-token power-of-two scale of z for its f16 copy, from the bound
       // |z_r| <= max_r sum_h |D_rh| * max_h |x_h|, identical in every CTA
       for (int t = 0; t < T; ++t) {
@@ -423,29 +486,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       float* z = a.z;
       __half* zg = a.zh;
       float* logits = a.logits;
-      const float* bias = lw.bias;
       const float* zsc = tb->zsc;
+      const float* rbias = tb->w;
       dense_rows<TB, false>(cx, rs, 2, xs, H, T, dyn, a.dyn_bytes, true, [&](int m, int t, int row, float v) {
-        if (m == 0) {
+        if (m == 1) {
           z[size_t(t) * L + row] = v;
           zg[size_t(t) * L + row] = __float2half_rn(v * zsc[t]);
         } else {
-          logits[size_t(t) * E + row] = v + (bias ? bias[row] : 0.f);
+          logits[size_t(t) * E + row] = v + (ne <= 32 ? rbias[row - e0] : (lw.bias ? lw.bias[row] : 0.f));
         }
       });
+      if (tid == 32) tb->gsc[0] = make_float4(sh_gu.x, sh_gu.y, sh_d, 0.f);
     }
     if (!grid_sync(a.bar, a.err)) return;
     // ================================================================ P1: routing, gate/up -> h
     {
-      // U rows of this CTA into L2 for P3 (routing-independent)
-      if (tid == 0 && j1 > j0) l2_prefetch_share(lw.U + size_t(j0) * L, size_t(j1 - j0) * L * 2, 0, 1);
       if (tid == 0) tb->task_ctr = 0;
       // zh = f16(z * 2^-e) per token (warp t), and the chunk sorts of the top-k
       const int nc = (E + 31) / 32;
       Cand* cx0 = reinterpret_cast<Cand*>(act);                       // [T][nc][16]
       Cand* cx1 = cx0 + size_t(T) * nc * 16;                          // [T][(nc+1)/2][16]
       for (int i = tid; i < T * L / 8; i += kDecThreads)
-        reinterpret_cast<uint4*>(zh)[i] = reinterpret_cast<const uint4*>(a.zh)[i];
+        cp_async16(reinterpret_cast<uint4*>(zh) + i, reinterpret_cast<const uint4*>(a.zh) + i);
+      cp_async_commit();
       for (int task = warp; task < T * nc; task += kDecWarps) {
         const int t = task / nc, c = task % nc;
         const int e = c * 32 + lane;
@@ -455,6 +518,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         warp_sort_desc(v, ix, lane);
         if (lane < 16) cx0[(size_t(t) * nc + c) * 16 + lane] = Cand{v, ix};
       }
+      // U rows of this CTA into L2 for P3 (routing-independent), after the logits loads
+      if (tid == 0 && j1 > j0) l2_prefetch_share(lw.U + size_t(j0) * L, size_t(j1 - j0) * L * 2, 0, 1);
+      cp_async_wait_all();
       __syncthreads();
       // merge levels: lists 2p, 2p+1 -> p (an odd last list passes through)
       {
@@ -553,8 +619,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       const uint8_t* experts = lw.experts;
       const size_t stride = lw.stride;
-      const float* gsh = reinterpret_cast<const float*>(lw.shared + rec_body);
-      const float sgg = gsh[0], sgu = gsh[1];
+      // fp32 scales of the selected records, one per lane of warps 8..15: the loads
+      // stay in flight across the next barrier; stored and announced on kMbScale after it
+      float3 rsc = make_float3(0.f, 0.f, 0.f);
+      const int sj = tid - kScaleWarp0 * 32;            // routed group of this lane
+      if (sj >= 0 && sj < nu) {
+        const float* gs = reinterpret_cast<const float*>(experts + size_t(tb->gexp[sj]) * stride + rec_body);
+        const float2 gu = *reinterpret_cast<const float2*>(gs);
+        rsc = make_float3(gu.x, gu.y, gs[2]);
+      }
+      auto publish_scales = [&]() {
+        if (warp >= kScaleWarp0 && warp < kScaleWarp0 + kScaleWarps) {
+          if (sj < nu) tb->gsc[sj + 1] = make_float4(rsc.x, rsc.y, rsc.z, 0.f);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tb->mbar[kMbScale]);
+        }
+      };
+      const float sgg = tb->gsc[0].x, sgu = tb->gsc[0].y;
       const __half* arow_all[TB];
 #pragma unroll
       for (int i = 0; i < TB; ++i) arow_all[i] = zh + size_t(i < T ? i : 0) * L;
@@ -587,27 +668,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             }
           }
         }
-        if (stage_down && first_round && warp == 1) {
-          // down rows [r0, r1) of every used expert (shared first), for P2: the batch
-          // leader arms the barrier, then one lane per expert issues its two copies
-          uint8_t* dd = dyn + gu_alloc;
-          const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
-          for (int gbase = 0; gbase < ngr; gbase += 32) {
-            const int gi = gbase + lane;
-            if (gi < ngr && gi % per_b == 0) {
-              const int n_in = min(per_b, ngr - gi);
-              mbar_arrive_expect_tx(&tb->mbar[kMbDown + gi / per_b], uint32_t(n_in) * down_grp);
-            }
-            __syncwarp();
-            if (gi < ngr) {
-              // this CTA's row pairs of one expert's D block: one byte range
-              const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
-              bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
-                       uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
-            }
-          }
-        }
         __syncthreads();
+        if (first_round) publish_scales();
         if (first_round && nsr > 0) {
           // shared-expert rows (staged in P0) while the routed rows land
           wait_mb(cx, kMbShared);
@@ -640,8 +702,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             arow[i] = zh + size_t(t) * L;
             ainv[i] = tb->zinv[t];
           }
-          const float* gl = reinterpret_cast<const float*>(experts + size_t(gexp[g]) * stride + rec_body);
-          gateup_row<TB>(gc, gs, uc, us, L, arow, n, gl[0], gl[1], ainv, [&](int i, float hv) {
+          wait_mb(cx, kMbScale);
+          const float4 gl = tb->gsc[g + 1];
+          gateup_row<TB>(gc, gs, uc, us, L, arow, n, gl.x, gl.y, ainv, [&](int i, float hv) {
             const int slot = perm[goff[g] + i];
             a.h[size_t(slot) * F + f] = hv;
           });
@@ -653,6 +716,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         qa += nrow;
         first_round = false;
       }
+      if (first_round) publish_scales();
       if (first_round && nsr > 0) {
         // no routed rows for this CTA: the shared rows still run
         wait_mb(cx, kMbShared);
@@ -667,6 +731,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
         __syncthreads();
         release_mb(cx, 1u << kMbShared);
+      }
+      if (stage_down && warp == 1) {
+        // down rows [r0, r1) of every used expert (shared first), for P2, issued once
+        // the gate/up rows have landed so that they do not share the bandwidth: the
+        // batch leader arms the barrier, then one lane per expert issues its copy
+        uint8_t* dd = dyn + gu_alloc;
+        const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
+        for (int gbase = 0; gbase < ngr; gbase += 32) {
+          const int gi = gbase + lane;
+          if (gi < ngr && gi % per_b == 0) {
+            const int n_in = min(per_b, ngr - gi);
+            mbar_arrive_expect_tx(&tb->mbar[kMbDown + gi / per_b], uint32_t(n_in) * down_grp);
+          }
+          __syncwarp();
+          if (gi < ngr) {
+            // this CTA's row pairs of one expert's D block: one byte range
+            const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
+            bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
+                     uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
+          }
+        }
       }
       if (tid == 0 && li + 1 < a.n_layers) {
         // next layer's D and R D into L2 while this layer finishes
@@ -690,9 +775,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       const int nur = j1 - j0;
       const int u_bytes = nur * L * 2;
       const bool stage_u = down_staged && u_bytes <= tb->down_off;
-      if (tid == 0) {
-        tb->u_staged = stage_u ? 1 : 0;
-        if (stage_u && nur > 0) {
+      if (tid == 0) tb->u_staged = stage_u ? 1 : 0;
+      // the U copies go out first: P3 waits on them, and issued later they arrive late
+      bool u_issued = false;
+      auto issue_u = [&]() {
+        if (tid == 0 && stage_u && nur > 0) {
           const int nc = (u_bytes + 16383) / 16384;
           mbar_arrive_expect_tx(&tb->mbar[kMbU], uint32_t(u_bytes));
           for (int c = 0; c < nc; ++c) {
@@ -702,7 +789,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
                        &tb->mbar[kMbU]);
           }
         }
-      }
+        u_issued = true;
+      };
+      issue_u();
       // region for h rows and per-slot outputs: after the staged down rows, or the
       // whole dynamic region when the down rows go in rounds
       uint8_t* region;
@@ -717,6 +806,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       float* ob = reinterpret_cast<float*>(region);
       const int ob_bytes = (nslot * nr * 4 + 127) & ~127;
       const int hrow = F * 2;
+      wait_mb(cx, kMbScale);
       int j0g = 0;
       while (nr > 0 && j0g < ngr) {
         // groups [j0g, j1g) this round: h rows (and, without staging, down rows) must fit
@@ -831,8 +921,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           fp4_dot<TB>(codes, scl, F / 16, arow, ns, l8, 8, acc);
           group_reduce<TB>(acc, 8);
           if (valid && l8 == 0) {
-            const uint8_t* rec = (j == 0) ? lw.shared : lw.experts + size_t(tb->gexp[j - 1]) * lw.stride;
-            const float gd = reinterpret_cast<const float*>(rec + rec_body)[2];
+            const float gd = tb->gsc[j].z;
 #pragma unroll
             for (int i = 0; i < TB; ++i) {
               if (i < ns) {
@@ -849,6 +938,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         if (!down_staged) release_mb(cx, (1u << nb) - 1u);
         j0g = j1g;
       }
+      if (!u_issued) issue_u();
       if (down_staged) {
         for (int b = 0; b < n_down_b; ++b) wait_mb(cx, kMbDown + b);
         __syncthreads();
@@ -861,6 +951,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         for (int j = 0; j < K; ++j) cv = fmaf(tb->w[t * K + j], ob[size_t(t * K + j) * nr + r], cv);
         a.c[size_t(t) * L + r0 + r] = cv;
       }
+      release_mb(cx, 1u << kMbScale);
     }
     if (!grid_sync(a.bar, a.err)) return;
     // ================================================================ P3: y = U c
@@ -906,7 +997,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     }
     if (last && a.final_norm) {
       // stack output: RMSNorm(x_last + y_last); every CTA normalises, each writes its slice
-      residual_norm(tb, xcur, a.ybuf + size_t(li & 1) * T * H, xs, T, H, a.eps);
+      residual_norm(tb, xcur, a.ybuf + size_t(li & 1) * T * H, xs, reinterpret_cast<float*>(xs + size_t(T) * H), T,
+                    H, a.eps, [] {});
       const int n8 = T * H / 8;
       const int i0 = int(long(bid) * n8 / G), i1 = int(long(bid + 1) * n8 / G);
       for (int i = i0 + tid; i < i1; i += kDecThreads)

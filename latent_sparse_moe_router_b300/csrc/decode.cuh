@@ -38,6 +38,9 @@ constexpr int kMbShared = 8;     // shared-expert gate/up rows (P0 -> P1)
 constexpr int kMbDown = 9;       // 9..12: down rows staged in P1 for P2
 constexpr int kMbDownN = 4;
 constexpr int kMbU = 13;         // U rows staged in P2 for P3
+constexpr int kMbScale = 14;     // fp32 scales of the selected records (P1 -> P1, P2)
+constexpr int kScaleWarp0 = 8;   // warps 8..15 load them, one record per lane
+constexpr int kScaleWarps = 8;
 
 // One layer's weights as the decode kernel sees them.
 struct LayerW {
@@ -94,21 +97,20 @@ struct alignas(16) DecTables {
   int goff[kDecodeMaxT * kMaxTopK + 1]; // group g = perm[goff[g] .. goff[g+1])
   int nu;                                // number of distinct experts
   int stuck;                             // bit b: a wait on mbar[b] ran out
-  int round_nb;                          // batches of the current round
   int task_ctr;                          // dynamic task counter
   int down_staged;                       // P1 staged the down rows (P2 uses them)
   int down_off;                          // their offset in the dynamic region
   int u_staged;                          // P2 staged the U rows (P3 uses them)
-  int pad0;
+  int pad0, pad1;
   float zsc[kDecodeMaxT], zinv[kDecodeMaxT];
+  float4 gsc[kDecodeMaxT * kMaxTopK + 1];  // (gate, up, down, -) fp32 scales of group j:
+                                         // j = 0 the shared expert, j >= 1 expert gexp[j - 1]
   float hinv[kMaxSlots];                 // 2^e of each slot's f16 h copy
   float red[kDecWarps * kDecodeMaxT];
   float inv_rms[kDecodeMaxT];
   // per-round task tables
   int task_row[512];
   int task_aux[512];
-  unsigned int task_off[512];
-  unsigned int task_off2[512];
 };
 
 size_t decode_tables_bytes();

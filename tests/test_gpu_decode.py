@@ -149,6 +149,28 @@ def test_every_token_on_the_same_experts(dev):
     d.close()
 
 
+def test_exact_logit_ties_rank_by_lower_index(dev):
+    """Exact ties repeated in every 32-expert chunk (router weights zero, logits = bias):
+    the top-k ranks by (logit descending, index ascending), as the oracle does."""
+    spec = small_spec(seed=4, n_experts=256, top_k=16)
+    inp = synth.make_layer(spec)
+    inp.R = np.zeros_like(inp.R)                   # logits are the bias exactly
+    inp.bias = np.full(spec.n_experts, -100.0, np.float32)
+    for c in range(spec.n_experts // 32):
+        inp.bias[c * 32:c * 32 + 16] = 100.0 - np.arange(16, dtype=np.float32)
+    d = dev.DeviceLayer(inp, max_tokens=16)
+    lay = oracle_layer(inp)
+    for T in (1, 5):
+        x_bits = synth.tokens_bf16(31 + T, T, spec.hidden)
+        y = d.forward(dev_bf16(x_bits))
+        torch.cuda.synchronize()
+        r = d.routing(T)
+        want = np.concatenate([np.arange(0, 256, 32), np.arange(1, 256, 32)])
+        assert np.array_equal(r["idx"], np.tile(want, (T, 1)))
+        check_layer(d, lay, x_bits, bits(y), r)
+    d.close()
+
+
 def test_zero_routed_experts_leave_the_shared_path(dev):
     """Zeroed routed records (all codes 0): y equals U * shared(z), as in the oracle."""
     spec = small_spec(seed=8)

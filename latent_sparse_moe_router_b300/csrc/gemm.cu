@@ -1,6 +1,6 @@
-// Plain dense bf16 GEMM entry point (C fp32 = A B^T) on the tcgen05 kernel of gemm.cuh.
+// Plain dense bf16 GEMM entry point (C fp32 = A B^T) on the CTA-pair tcgen05 kernel of gemm_pair.cuh.
 #include "../../include/edge0_moe.h"
-#include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "tmap.cuh"
 
 namespace edge0 {
@@ -22,7 +22,7 @@ struct EpiStoreF32 {
   }
 };
 
-constexpr int kBN = 256, kStages = 4;
+constexpr int kStages = 6;
 
 }  // namespace
 
@@ -40,11 +40,11 @@ extern "C" edge0_status edge0_gemm_bf16_tn(const void* A, const void* B, float* 
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, uint64_t(K) * 2, 64, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, uint64_t(K) * 2, 64, kBN,
+      !make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, uint64_t(K) * 2, 64, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return EDGE0_ERR_CUDA;
   EpiStoreF32 epi{C, N, N};
-  return launch_gemm_tn<kBN, kStages>(ta, tb, tb, M, N, K, 1 << 30, err, nullptr, epi, (cudaStream_t)stream) ==
+  return launch_gemm_pair<kStages>(ta, tb, tb, M, N, K, 1 << 30, err, nullptr, epi, (cudaStream_t)stream) ==
                  cudaSuccess
              ? EDGE0_OK
              : EDGE0_ERR_CUDA;

@@ -1,0 +1,216 @@
+// Dense bf16 GEMM on a CTA pair (2-SM tcgen05), C = A * B^T.
+//
+//   A [M][K] bf16 row-major (K-major), B [N][K] bf16 row-major (K-major),
+//   fp32 accumulation in TMEM, results handed to an epilogue functor.
+// A cluster of two CTAs computes 256 x 256 output tiles: CTA r (rank in the pair)
+// stages rows m0 + 128 r .. + 127 of A and rows n0 + 128 r .. + 127 of B (128 x 64,
+// 128-byte swizzle) per 64-wide k-step, so each SM moves half the B tile a
+// single-CTA 128 x 256 tile would need through its shared memory and from L2.
+// Persistent: the pairs walk the tiles (i -> m = i / n_tiles, n = i % n_tiles) with
+// a stride of the number of pairs.  Warp roles in both CTAs:
+//   warp 0 (one lane): TMA producer; both CTAs' copies complete on rank 0's `full`
+//     barrier (two arrivals with their byte counts);
+//   warp 1 (one lane, rank 0 only): tcgen05.mma.cta_group::2 (M=256, N=256, K=16,
+//     four per k-step) into one of two TMEM accumulators of 256 columns; its commits
+//     arrive on `empty` / `acc_full` in both CTAs;
+//   warps 2-5: epilogue of the CTA's 128 accumulator rows (tcgen05.ld, thread = row,
+//     32 columns per load), overlapping the next tile's main loop; each warp then
+//     arrives on rank 0's `acc_empty` (eight arrivals).
+// Every wait is bounded; both CTAs run the same tile sequence and reach the
+// collective TMEM allocation and release.
+#pragma once
+
+#include "gemm.cuh"
+#include "pair.cuh"
+
+namespace edge0 {
+
+constexpr int kGemmPairThreads = 192;
+
+template <int STAGES>
+struct GemmPairSmem {
+  static constexpr int kA = 128 * 64 * 2;   // one A stage (bytes)
+  static constexpr int kB = 128 * 64 * 2;   // one B stage (this CTA's half)
+  static constexpr int kStage = kA + kB;
+  // barriers and tmem slot, alignment, and 16 KB of slack past the last stage
+  static constexpr int kBytes = STAGES * kStage + 1024 + 1024 + 16384;
+};
+
+// Epilogue interface: operator()(int row, int col0, const float* v32) for the 32
+// consecutive columns col0 .. col0+31 of one row; rows >= M are not passed.
+// Output columns [0, n_split) multiply B's rows, columns from n_split on multiply
+// B2's rows (n_split a multiple of 256; pass B2 = B for one matrix).
+template <int STAGES, class Epi>
+__global__ void __launch_bounds__(kGemmPairThreads, 1)
+gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmB2, int M, int N, int K, int n_split, int* err,
+                         int* abort, Epi epi) {
+  using S = GemmPairSmem<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::kStage);   // rank 0: 2 arrivals + bytes
+  uint64_t* empty = full + STAGES;         // both: MMA commit
+  uint64_t* acc_full = empty + STAGES;     // [2] both: MMA commit
+  uint64_t* acc_empty = acc_full + 2;      // [2] rank 0: one arrival per epilogue warp of the pair
+  uint64_t* mma_done = acc_empty + 2;      // rank 0
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* s_bad = reinterpret_cast<int*>(tmem_slot + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int nk = K / 64;
+  const int n_tiles = (N + 255) / 256;
+  const int total = ((M + 255) / 256) * n_tiles;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (pair >= total) return;   // both CTAs of the pair leave together
+
+  if (threadIdx.x == 0) {
+    *s_bad = 0;
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 8); }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 1) { tmem_alloc_pair(tmem_slot, 512); tmem_relinquish_pair(); }
+  tc_fence_before();
+  // both CTAs' barriers exist and the pair's TMEM is allocated before anyone signals
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmB2);
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+      int it = 0;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        const int m0 = (tile / n_tiles) * 256, n0 = (tile % n_tiles) * 256;
+        const int ya = m0 + 128 * int(rank), yb = n0 + 128 * int(rank);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_abort(&empty[s], ((it / STAGES) & 1) ^ 1, err, abort)) { ok = false; break; }
+          uint8_t* sa = smem + s * S::kStage;
+          const uint32_t fb = full0 + uint32_t(s) * 8u;
+          mbar_arrive_expect_tx_cl(fb, S::kStage);
+          tma_load_2d_pair(sa, &tmA, kb * 64, ya, fb);
+          // columns [0, n_split) come from B's rows, later columns from B2's rows
+          if (n0 < n_split) tma_load_2d_pair(sa + S::kA, &tmB, kb * 64, yb, fb);
+          else tma_load_2d_pair(sa + S::kA, &tmB2, kb * 64, yb - n_split, fb);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(256, 256);
+      int it = 0, ti = 0;
+      for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
+        const int ab = ti & 1;
+        if (!mbar_wait_cl_abort(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, err, abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + ab * 256;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          // the stage's bytes were written by bulk copies: the barrier's completion orders
+          // them before the MMA, no cluster-scope acquire is needed
+          if (!mbar_wait_abort(&full[s], (it / STAGES) & 1, err, abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * S::kStage);
+          const uint32_t sb = sa + S::kA;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_pair_f16(acc, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), idesc, (kb | k) != 0);
+          mma_pair_commit_both(&empty[s]);
+        }
+        if (!ok) break;
+        mma_pair_commit_both(&acc_full[ab]);
+      }
+      // every MMA issued has finished, and both CTAs' epilogues have released the
+      // last two accumulators (their arrivals land here), before this CTA winds down
+      mma_pair_commit(mma_done);
+      mbar_wait_abort(mma_done, 0, err, nullptr);
+      for (int j = ti - 2; ok && j < ti; ++j)
+        if (j >= 0 && !mbar_wait_cl_abort(&acc_empty[j & 1], (j >> 1) & 1, err, abort)) ok = false;
+    }
+  } else {
+    // epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31 (this CTA's rows)
+    const int q = warp & 3;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    int ti = 0;
+    for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
+      const int m0 = (tile / n_tiles) * 256, n0 = (tile % n_tiles) * 256;
+      const int ab = ti & 1;
+      ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, err, abort);
+      if (!gemm_named_and(1, 128, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int row = m0 + 128 * int(rank) + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + ab * 256 + c * 32, r);
+        tmem_ld_wait();
+        if (row < M) epi(row, n0 + c * 32, reinterpret_cast<const float*>(r));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cl(acc_empty0 + uint32_t(ab) * 8u);
+    }
+  }
+  if (!ok) *s_bad = 1;
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  // after a wait gave up, bulk copies issued by this CTA may still be landing:
+  // give them a bounded time before the shared memory is released
+  if (*s_bad && threadIdx.x == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {}
+  }
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+// Launch of one GEMM on CTA pairs: min(tiles, resident pairs) clusters of two.
+// A's, B's and B2's maps have 64 x 128 boxes (128-byte swizzle).  K a multiple of 64.
+template <int STAGES, class Epi>
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N,
+                             int K, int n_split, int* err, int* abort, const Epi& epi, cudaStream_t s) {
+  using Sm = GemmPairSmem<STAGES>;
+  auto kern = gemm_pair_bf16_tn_kernel<STAGES, Epi>;
+  static int max_pairs = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmPairThreads);
+  cfg.dynamicSmemBytes = Sm::kBytes;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (max_pairs == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
+    int dev = 0, sms = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cfg.gridDim = dim3(2 * (sms / 2));
+    int clusters = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = clusters;
+  }
+  const long tiles = long((M + 255) / 256) * ((N + 255) / 256);
+  const int pairs = int(tiles < max_pairs ? tiles : max_pairs);
+  if (pairs <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(2 * pairs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, M, N, K, n_split, err, abort, epi);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace edge0

@@ -21,7 +21,7 @@
 //   9. tcgen05 GEMM  c x U^T -> y bf16 (round to nearest even).
 #include <algorithm>
 
-#include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "grouped_kernel.cuh"
 #include "prefill.cuh"
 #include "tmap.cuh"
@@ -31,7 +31,7 @@ namespace edge0 {
 namespace {
 
 constexpr int kChunk = 64;          // tokens per routing chunk
-constexpr int kPfBN = 256, kPfStages = 4;
+constexpr int kPfBox = 128, kPfStages = 6;   // CTA-pair GEMM: 128-row B halves, 6 stages
 
 size_t pf_align(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -499,9 +499,9 @@ cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_
   const uint64_t gu_row = 9ull * L / 8, d_pair = 9ull * F / 8, d_block = uint64_t(F) * gu_row;
   bool ok = true;
   // dense GEMM operands
-  ok &= make_tmap_2d(&pf->m_D, d.D, BF, 2, L, H, uint64_t(H) * 2, 64, kPfBN, SW);
-  ok &= make_tmap_2d(&pf->m_rdcat, pf->rdcat, BF, 2, 2ull * E, H, uint64_t(H) * 2, 64, kPfBN, SW);
-  ok &= make_tmap_2d(&pf->m_U, d.U, BF, 2, H, L, uint64_t(L) * 2, 64, kPfBN, SW);
+  ok &= make_tmap_2d(&pf->m_D, d.D, BF, 2, L, H, uint64_t(H) * 2, 64, kPfBox, SW);
+  ok &= make_tmap_2d(&pf->m_rdcat, pf->rdcat, BF, 2, 2ull * E, H, uint64_t(H) * 2, 64, kPfBox, SW);
+  ok &= make_tmap_2d(&pf->m_U, d.U, BF, 2, H, L, uint64_t(L) * 2, 64, kPfBox, SW);
   ok &= make_tmap_2d(&pf->m_cb, pf->cb, BF, 2, T, L, uint64_t(L) * 2, 64, 128, SW);
   // gate/up: records' GU blocks [E][F rows][9L/8 bytes]
   ok &= make_tmap_3d(&pf->maps1.a_codes, ex, U8, gu_row, F, E, gu_row, d.expert_stride, 32, 64, 1, NS);
@@ -546,7 +546,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   }
   // 1. x -> z (f16, scaled), logits
   if (e == cudaSuccess)
-    e = launch_gemm_tn<kPfBN, kPfStages>(mx, pf->m_D, pf->m_rdcat, T, L + 2 * E, H, L, pf->err, pf->abort,
+    e = launch_gemm_pair<kPfStages>(mx, pf->m_D, pf->m_rdcat, T, L + 2 * E, H, L, pf->err, pf->abort,
                                          EpiXZ{pf->zh, pf->zsc, pf->logits, d.router_bias, L, E}, s);
   mark();
   // 2-4. routing and permutation
@@ -604,7 +604,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   mark();
   // 9. y = c U^T
   if (e == cudaSuccess)
-    e = launch_gemm_tn<kPfBN, kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, L, 1 << 30, pf->err, pf->abort,
+    e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, L, 1 << 30, pf->err, pf->abort,
                                          EpiStoreBF16{y, H, H}, s);
   mark();
   if (pf->profile && e == cudaSuccess) pf->timed = (stage == 11);

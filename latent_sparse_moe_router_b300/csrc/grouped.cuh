@@ -3,32 +3,40 @@
 // The experts of the latent-MoE layer run l -> 640 -> l as SwiGLU FFNs on NVFP4
 // weights ("Edge0-145B · Q3_K" model card, section "Architecture"; NVFP4 per
 // "Edge0-145B en local", introduction).  Tokens are grouped by expert (positions
-// p of the permutation); a work tile is (group g, token tile nt, weight tile mt):
+// p of the permutation); a work tile is (group g, token tile nt, weight tile mt),
+// and a cluster of two CTAs on two SMs (a pair) runs the weight tiles 2u, 2u + 1 of
+// one token tile as one M = 256 tcgen05.mma.cta_group::2:
 //   MODE 1 (gate/up): A = 64 gate rows + 64 up rows (f0 = 64 mt), B = BN token
 //     rows of the group (z * 2^-e_t in f16), K = l; f16 operands; epilogue
 //     h = silu(g_gate 2^e_t gate) * (g_up 2^e_t up), stored bf16 to H[p][f].
 //   MODE 2 (down):    A = 128 latent rows (r0 = 128 mt, 64 row pairs), B = BN rows
 //     of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
-// Persistent CTAs (one per SM) walk the tiles in index order with a stride of
-// the grid, tile = (token tile, weight tile) with the weight tile fastest, so
-// the CTAs working at one time share a few token tiles through L2.  Warp roles:
+// Persistent pairs (one CTA per SM) walk the pair tiles in index order with a
+// stride of the number of pairs, pair tile = (token tile, weight-tile pair u) with
+// u fastest, so the pairs working at one time share a few token tiles through L2.
+// CTA r of a pair owns weight tile 2u + r: it dequantises those 128 A rows, stages
+// half of the tile's B rows (columns r N/2 .. r N/2 + N/2 - 1 of the MMA) and holds
+// the accumulator rows of its A rows in its own TMEM.  Warp roles in both CTAs:
 //   warp 0 (one lane): TMA producer of the tile's E4M3 scales (double-buffered)
 //     and raw NVFP4 codes (4 KB per 64-wide k-step, 6-deep ring);
-//   warp 18 (one lane): TMA producer of the B rows the tile needs (64-row boxes,
-//     128-byte swizzle), into the stages the MMA releases;
-//   warp 1 (one lane): tcgen05.mma M=128, N = the tile's rows rounded to 16,
-//     K=16, into one of two TMEM accumulators of 256 columns;
+//   warp 18 (one lane): TMA producer of this CTA's half of the B rows (64-row
+//     boxes, 128-byte swizzle), into the stages the MMA releases; completion on
+//     rank 0's barrier;
+//   warp 1 (one lane, rank 0 only): tcgen05.mma.cta_group::2, M=256, N = the
+//     tile's rows rounded to 16, K=16, into one of two TMEM accumulators of 256
+//     columns in each CTA; commits arrive in both CTAs;
 //   warps 2-9: dequantisation, two threads per A row, exact: mode 1 E2M1 -> f16
 //     by cvt times the E4M3 scale in one f16x2 multiply; mode 2 the same f16
 //     moved to the bf16 exponent range with shift/mask and multiplied by the
-//     block scale * 2^112 in bf16x2; into 128-byte-swizzled A tiles;
+//     block scale * 2^112 in bf16x2; into 128-byte-swizzled A tiles; each warp
+//     then arrives on rank 0's stage barrier;
 //   warps 10-17: epilogue of the previous accumulator (TMEM -> registers ->
 //     shared-memory transpose -> whole-row global stores; two warps per TMEM lane
 //     quarter, one per half of each 32-column chunk) while the next tile's main
-//     loop runs.
+//     loop runs; each warp then arrives on rank 0's accumulator barrier.
 #pragma once
 
-#include "tc.cuh"
+#include "pair.cuh"
 
 namespace edge0 {
 
@@ -41,12 +49,12 @@ constexpr int kGgEpThreads = 256;
 constexpr int kGgBWarp = 18;      // B-tile producer
 constexpr int kGgBN = 256;        // token tile
 constexpr int kGgSA = 4;          // A (dequantised weight) stages
-constexpr int kGgSB = 3;          // B (token row) stages
+constexpr int kGgSB = 4;          // B (token row) stages
 constexpr int kGgR = 6;           // raw code stages
 
 struct GgSmem {
   static constexpr int kA = 128 * 64 * 2;        // 16 KB
-  static constexpr int kB = kGgBN * 64 * 2;      // 32 KB
+  static constexpr int kB = kGgBN / 2 * 64 * 2;  // 16 KB: this CTA's half of the token rows
   static constexpr int kRaw = 128 * 32;          // 4 KB
   static constexpr int kSc = 16384;              // scales of one tile (<= 128 rows x 128 B)
   static constexpr int kEpi = 9216;              // epilogue transpose buffers
@@ -62,7 +70,7 @@ struct GgSmem {
 struct GgParams {
   int mode;                 // 1 gate/up, 2 down
   int T, TK, L, F, E;
-  int mtiles;               // weight tiles per group (F/64 or L/128)
+  int mtiles;               // weight tiles per group (F/64 or L/128; even)
   const int* counts;        // [E]   tokens per routed expert
   const int* offsets;       // [E+1] first position of each routed expert
   const int* tprefix;       // [E+2] first token tile of each group (group E = shared)

@@ -71,16 +71,18 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 struct GgTile {
-  int g, mt, n_rows, pos0, out0;
+  int g, mt, n_rows, n_mma, pos0, out0;
   bool shared;
 };
 
-// Tile `tile` of the launch: token tile tt = tile / mtiles of group g (binary
-// search over the token-tile prefix), weight tile mt = tile % mtiles.
-__device__ __forceinline__ GgTile gg_tile(const GgParams& p, int tile) {
+// CTA `rank`'s part of pair tile `tile`: token tile tt = tile / (mtiles / 2) of
+// group g (binary search over the token-tile prefix), weight tile
+// mt = 2 (tile % (mtiles / 2)) + rank.
+__device__ __forceinline__ GgTile gg_tile(const GgParams& p, int tile, int rank) {
   GgTile t;
-  const int tt = tile / p.mtiles;
-  t.mt = tile % p.mtiles;
+  const int mp = p.mtiles >> 1;
+  const int tt = tile / mp;
+  t.mt = 2 * (tile % mp) + rank;
   int lo = 0, hi = p.E + 1;            // tprefix[lo] <= tt < tprefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -91,6 +93,7 @@ __device__ __forceinline__ GgTile gg_tile(const GgParams& p, int tile) {
   const int row0 = (tt - __ldg(&p.tprefix[lo])) * kGgBN;
   const int n_g = t.shared ? p.T : __ldg(&p.counts[lo]);
   t.n_rows = min(kGgBN, n_g - row0);
+  t.n_mma = (t.n_rows + 15) & ~15;
   t.out0 = (t.shared ? p.TK : __ldg(&p.offsets[lo])) + row0;
   t.pos0 = (t.shared && p.mode == 1) ? row0 : t.out0;
   return t;
@@ -115,27 +118,32 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 2);   // [0] total tiles, [1] bad
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = int(cluster_ctarank());
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    s_flags[0] = (p.abort && ld_relaxed_s32(p.abort)) ? 0 : p.tprefix[p.E + 1] * p.mtiles;
+    // the pair-tile count both CTAs read from the same word, so that they agree
+    s_flags[0] = p.tprefix[p.E + 1] * (p.mtiles >> 1);
     s_flags[1] = 0;
-    // consumer barriers take one arrival per warp (lane 0 after a __syncwarp)
-    for (int s = 0; s < kGgSA; ++s) { mbar_init(&a_full[s], kGgDqWarps); mbar_init(&a_empty[s], 1); }
-    for (int s = 0; s < kGgSB; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
+    // consumer barriers take one arrival per warp (lane 0 after a __syncwarp); the
+    // stage and accumulator barriers of rank 0 count both CTAs' warps
+    for (int s = 0; s < kGgSA; ++s) { mbar_init(&a_full[s], 2 * kGgDqWarps); mbar_init(&a_empty[s], 1); }
+    for (int s = 0; s < kGgSB; ++s) { mbar_init(&b_full[s], 2); mbar_init(&b_empty[s], 1); }
     for (int s = 0; s < kGgR; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kGgDqWarps); }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sc_full[b], 1); mbar_init(&sc_empty[b], kGgDqWarps);
-      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kGgEpThreads / 32);
+      mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2 * (kGgEpThreads / 32));
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   __syncthreads();
   const int total = s_flags[0];
-  if (blockIdx.x >= total) return;
-  if (warp == 1) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (pair >= total) return;   // both CTAs of the pair leave together
+  if (warp == 1) { tmem_alloc_pair(tmem_slot, 512); tmem_relinquish_pair(); }
   tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers exist and the pair's TMEM is allocated before anyone signals
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int K = p.mode == 1 ? p.L : p.F;
@@ -147,8 +155,8 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       // ---- scale and raw-code producer
       const int scb = p.mode == 1 ? 2 * 64 * (p.L / 16) : 64 * (p.F / 8);
       int it = 0, ti = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
-        const GgTile t = gg_tile(p, tile);
+      for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
+        const GgTile t = gg_tile(p, tile, rank);
         const CUtensorMap* mcodes = t.shared ? &maps.s_codes : &maps.a_codes;
         const CUtensorMap* mscales = t.shared ? &maps.s_scales : &maps.a_scales;
         const int sb = ti & 1;
@@ -188,30 +196,34 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     }
   } else if (warp == kGgBWarp) {
     if (lane == 0) {
-      // ---- B producer: the tile's token rows, one k-slice per stage
+      // ---- B producer: this CTA's half of the tile's token rows (MMA columns
+      // rank * N/2 ..), one k-slice per stage, completing on rank 0's barrier
+      const uint32_t bfull0 = mapa_shared(smem_u32(b_full), 0);
       int it = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GgTile t = gg_tile(p, tile);
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        const GgTile t = gg_tile(p, tile, rank);
         const CUtensorMap* mb = (t.shared && p.mode == 1) ? &maps.b_shared : &maps.b_routed;
-        const int nbox = (t.n_rows + kGgBBox - 1) / kGgBBox;
+        const int half = t.n_mma >> 1;
+        const int row0 = t.pos0 + rank * half;
+        const int nbox = (half + kGgBBox - 1) / kGgBBox;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kGgSB;
           if (!mbar_wait_abort(&b_empty[s], ((it / kGgSB) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(&b_full[s], nbox * kGgBBox * 128);
+          const uint32_t fb = bfull0 + uint32_t(s) * 8u;
+          mbar_arrive_expect_tx_cl(fb, nbox * kGgBBox * 128);
           uint8_t* bs = smem + GgSmem::offB + s * GgSmem::kB;
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(bs + bx * kGgBBox * 128, mb, kb * 64, t.pos0 + bx * kGgBBox, &b_full[s]);
+            tma_load_2d_pair(bs + bx * kGgBBox * 128, mb, kb * 64, row0 + bx * kGgBBox, fb);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ---- MMA issuer (rank 0 of the pair)
       int it = 0, ti = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
-        const GgTile t = gg_tile(p, tile);
-        const int n_mma = (t.n_rows + 15) & ~15;
-        const uint32_t idesc = p.mode == 1 ? idesc_f16_f32(128, n_mma) : idesc_bf16_f32(128, n_mma);
+      for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
+        const GgTile t = gg_tile(p, tile, 0);
+        const uint32_t idesc = p.mode == 1 ? idesc_f16_f32(256, t.n_mma) : idesc_bf16_f32(256, t.n_mma);
         const int ab = ti & 1;
         if (!mbar_wait_abort(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
         tc_fence_after();
@@ -228,16 +240,19 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
           const uint32_t sbb = smem_u32(smem + GgSmem::offB + sb_i * GgSmem::kB);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(acc, sw128_desc(sa + k * 32), sw128_desc(sbb + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&a_empty[sa_i]);
-          mma_commit(&b_empty[sb_i]);
+            mma_pair_f16(acc, sw128_desc(sa + k * 32), sw128_desc(sbb + k * 32), idesc, (kb | k) != 0);
+          mma_pair_commit_both(&a_empty[sa_i]);
+          mma_pair_commit_both(&b_empty[sb_i]);
         }
         if (!ok) break;
-        mma_commit(&acc_full[ab]);
+        mma_pair_commit_both(&acc_full[ab]);
       }
-      // every MMA issued has finished before the accumulators are released
-      mma_commit(mma_done);
+      // every MMA issued has finished, and both CTAs' epilogues have released the
+      // last two accumulators (their arrivals land here), before this CTA winds down
+      mma_pair_commit(mma_done);
       mbar_wait_abort(mma_done, 0, p.err, nullptr);
+      for (int j = ti - 2; ok && j < ti; ++j)
+        if (j >= 0 && !mbar_wait_abort(&acc_empty[j & 1], (j >> 1) & 1, p.err, p.abort)) ok = false;
     }
   } else if (warp < kGgEpWarp0) {
     // ---- dequantisation: thread pair (r, hh) owns A row r, elements 32 hh .. 32 hh + 31.
@@ -249,8 +264,9 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     const int raw_off = (r & 1) * 2048 + (r >> 1) * 32 + hh * 16;
     const int sc_off = (p.mode == 1 ? (r & 1) * 64 * (p.L / 16) + (r >> 1) * (p.L / 16)
                                     : (r >> 1) * (p.F / 8) + (r & 1) * (p.F / 16)) + hh * 2;
+    const uint32_t afull0 = mapa_shared(smem_u32(a_full), 0);
     int it = 0, ti = 0;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
+    for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
       const int sb = ti & 1;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_abort(&sc_full[sb], (ti >> 1) & 1, p.err, p.abort))) { ok = false; break; }
       const uint8_t* my_sc = smem + GgSmem::offSc + sb * GgSmem::kSc + sc_off;
@@ -300,7 +316,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[s]);
+        if (lane == 0) mbar_arrive_remote(afull0 + uint32_t(s) * 8u);
       }
       if (!ok) break;
       __syncwarp();
@@ -318,9 +334,10 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     // mode 1: [32 tokens][72] bf16 (64 f used); mode 2: [32 tokens][68] u32 (64 latent pairs used)
     __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi);
     uint32_t* obuf = reinterpret_cast<uint32_t*>(smem + GgSmem::offEpi);
+    const uint32_t accempty0 = mapa_shared(smem_u32(acc_empty), 0);
     int ti = 0;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
-      const GgTile t = gg_tile(p, tile);
+    for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
+      const GgTile t = gg_tile(p, tile, rank);
       const int ab = ti & 1;
       // uniform across the epilogue warps: all agree the accumulator is complete
       ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, p.err, p.abort);
@@ -380,7 +397,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       // the accumulator's TMEM columns are free for the tile after next
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if (lane == 0) mbar_arrive_remote(accempty0 + uint32_t(ab) * 8u);
     }
   }
   if (!ok) s_flags[1] = 1;
@@ -394,7 +411,9 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     while (globaltimer_ns() - t0 < 50000ull) {}
   }
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
 }  // namespace edge0

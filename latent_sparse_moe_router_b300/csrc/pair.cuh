@@ -85,6 +85,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t bar_cl, uint32
                ::"r"(bar_cl), "r"(bytes) : "memory");
 }
 
+// Arrive on a barrier of either CTA of the pair with the default semantics (release
+// at CTA scope): the pair's pipeline hand-offs, as between the CTAs of one cluster
+// in general.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cl) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
 }

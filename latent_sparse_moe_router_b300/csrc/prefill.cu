@@ -426,16 +426,32 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ ob, const int* 
 }
 
 cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int num_sms, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
+  static int max_pairs = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGgThreads);
+  cfg.dynamicSmemBytes = GgSmem::kBytes;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (max_pairs == 0) {
+    cudaError_t e =
         cudaFuncSetAttribute(grouped_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GgSmem::kBytes);
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int clusters = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&clusters, grouped_nvfp4_kernel, &cfg);
     if (e != cudaSuccess) return e;
-    attr = true;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = clusters;
   }
-  // persistent: one CTA per SM walks the tiles (their count is read on the device)
-  grouped_nvfp4_kernel<<<num_sms, kGgThreads, GgSmem::kBytes, s>>>(maps, p);
-  return cudaGetLastError();
+  // persistent: every resident pair walks the pair tiles (their count is read on the device)
+  cfg.gridDim = dim3(2 * max_pairs);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_nvfp4_kernel, maps, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

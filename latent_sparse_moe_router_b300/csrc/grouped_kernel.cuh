@@ -334,18 +334,24 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     // mode 1: [32 tokens][72] bf16 (64 f used); mode 2: [32 tokens][68] u32 (64 latent pairs used)
     __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi);
     uint32_t* obuf = reinterpret_cast<uint32_t*>(smem + GgSmem::offEpi);
+    float* zbuf = reinterpret_cast<float*>(smem + GgSmem::offEpi + GgSmem::kEpiT);   // [256] token scales
     const uint32_t accempty0 = mapa_shared(smem_u32(acc_empty), 0);
     int ti = 0;
     for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
       const GgTile t = gg_tile(p, tile, rank);
       const int ab = ti & 1;
-      // uniform across the epilogue warps: all agree the accumulator is complete
-      ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, p.err, p.abort);
-      if (!named_and(1, kGgEpThreads, ok)) { ok = false; break; }
-      tc_fence_after();
+      // the tile's global reads go out before the accumulator wait: the record's fp32
+      // scales, and (mode 1) one column's token scale per thread into the shared table
+      // (the previous tile's last named barrier has passed: no thread still reads it)
       const uint8_t* rec = t.shared ? p.shared : p.experts + size_t(t.g) * p.stride;
       const float* gl = reinterpret_cast<const float*>(rec + size_t(27) * p.F * p.L / 16);
       const float g0 = p.mode == 1 ? gl[0] : gl[2], g1 = gl[1];
+      if (p.mode == 1) zbuf[te] = te < t.n_rows ? __ldg(&p.pos_inv[t.out0 + te]) : 1.0f;
+      // uniform across the epilogue warps: all agree the accumulator is complete (this
+      // barrier also publishes the token-scale table)
+      ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, p.err, p.abort);
+      if (!named_and(1, kGgEpThreads, ok)) { ok = false; break; }
+      tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256 + ch * 16;
       const int tr = te >> 3, part = te & 7;
       for (int c = 0; c * 32 < t.n_rows; ++c) {
@@ -361,8 +367,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
             const float gate = odd ? x : __uint_as_float(va);
             const float up = odd ? __uint_as_float(vb) : x;
             // undo the token's power-of-two scale of z (exact)
-            const int col = c * 32 + col0 + j;
-            const float zi = col < t.n_rows ? __ldg(&p.pos_inv[t.out0 + col]) : 1.0f;
+            const float zi = zbuf[c * 32 + col0 + j];
             hbuf[(col0 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * zi * gate) * (g1 * zi * up));
           }
           named_sync(1, kGgEpThreads);

@@ -466,29 +466,61 @@ def run_prefill(args, wl, rank, world, local):
     stages = {n: round(float(m), 4) for n, m in zip(names, stage_ms)}
     stages["timed_layer_ms_sum"] = round(float(stage_ms.sum()), 4)
 
-    # e2e through the C ABI with pinned host buffers: H2D x, forward, D2H y, per step
+    # e2e through the C ABI with pinned host buffers: every step copies its x in from pinned
+    # host memory, runs the forward and copies its y out to pinned host memory, and the host
+    # reads each step's result.  Prefill batches are independent, so the steps are
+    # pipelined as a server would run them: step i+1's input copy and step i-1's output
+    # copy (each on its own stream) overlap step i's kernels, two device buffers each way,
+    # and the host waits for step i-1's result after launching step i.
     hx = torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
-    hy = torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+    hy = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     hx.copy_(xs[0].cpu())
+    xb = [xs[0], torch.empty_like(xs[0])]
+    yb = [ys[0], torch.empty_like(ys[0])]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    x_in = [torch.cuda.Event() for _ in range(2)]
+    y_done = [torch.cuda.Event() for _ in range(2)]
+    y_out = [torch.cuda.Event() for _ in range(2)]
     n_e2e = max(3, min(args.steps, 10))
+
+    def fwd(x, y):
+        if n_layers > 1:
+            ext.edge0_moe_stack_forward(handles, x, y, T, 1e-6, stream)
+        else:
+            ext.edge0_moe_forward(handles[0], x, y, T, stream)
+
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(n_e2e):
-            xs[0].copy_(hx, non_blocking=True)
-            if n_layers > 1:
-                ext.edge0_moe_stack_forward(handles, xs[0], ys[0], T, 1e-6, stream)
-            else:
-                ext.edge0_moe_forward(handles[0], xs[0], ys[0], T, stream)
-            hy.copy_(ys[0], non_blocking=True)
-            stream.synchronize()
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(stream)
+    h2d.wait_event(e0)
+    d2h.wait_event(e0)
+    for i in range(n_e2e):
+        b = i & 1
+        if i >= 2:
+            h2d.wait_event(y_done[b])           # the forward of step i-2 is done with xb[b]
+        with torch.cuda.stream(h2d):
+            xb[b].copy_(hx, non_blocking=True)
+        x_in[b].record(h2d)
+        stream.wait_event(x_in[b])
+        if i >= 2:
+            stream.wait_event(y_out[b])         # step i-2's y has been copied out of yb[b]
+        fwd(xb[b], yb[b])
+        y_done[b].record(stream)
+        d2h.wait_event(y_done[b])
+        with torch.cuda.stream(d2h):
+            hy[b].copy_(yb[b], non_blocking=True)
+        y_out[b].record(d2h)
+        if i >= 1:
+            y_out[(i - 1) & 1].synchronize()    # the host reads step i-1's result
+    y_out[(n_e2e - 1) & 1].synchronize()        # and the last one
+    stream.wait_event(y_out[(n_e2e - 1) & 1])
+    e1.record(stream)
+    e1.synchronize()
     e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
     e2e = {"value": round(T * world / (e_ms / 1e3), 1), "unit": "tok/s",
-           "h2d_bytes_per_step": T * HIDDEN * 2, "d2h_bytes_per_step": T * HIDDEN * 2}
+           "h2d_bytes_per_step": T * HIDDEN * 2, "d2h_bytes_per_step": T * HIDDEN * 2,
+           "pipelined": True}
     errs = [ext.edge0_moe_get_error(h) for h in handles]
     assert all(e == ext.EDGE0_OK for e in errs), f"device wait ran out: {errs}"
     for d in insts:

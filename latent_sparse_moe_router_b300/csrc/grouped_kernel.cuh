@@ -8,9 +8,9 @@ namespace edge0 {
 
 constexpr int kGgBBox = 64;       // rows of one B box (TMA)
 
-// silu(v) = v / (1 + e^-v) with the hardware exponential and reciprocal (the result
-// is rounded to bf16, far coarser than their error); v -> -inf gives -0.
-__device__ __forceinline__ float silu_gg(float v) { return v * __frcp_rn(1.0f + __expf(-v)); }
+// silu(v) = v / (1 + e^-v) with the hardware exponential and the fast division (the
+// result is rounded to bf16, far coarser than their error); v -> -inf gives -0.
+__device__ __forceinline__ float silu_gg(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // Four E2M1 pairs (one 32-bit word, byte i = elements 2i, 2i+1, low nibble first)
 // -> four f16x2.

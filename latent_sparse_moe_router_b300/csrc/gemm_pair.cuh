@@ -20,12 +20,21 @@
 // collective TMEM allocation and release.
 #pragma once
 
-#include "gemm.cuh"
 #include "pair.cuh"
 
 namespace edge0 {
 
 constexpr int kGemmPairThreads = 192;
+
+// Named barrier `id` over n threads that also returns whether pred held in all of them.
+__device__ __forceinline__ bool gemm_named_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " barrier.cta.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r) : "r"(uint32_t(pred)), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
 
 template <int STAGES>
 struct GemmPairSmem {

@@ -47,7 +47,7 @@ typedef struct CUstream_st *edge0_stream_t;
 typedef enum {
   EDGE0_OK = 0,
   EDGE0_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or alignment */
-  EDGE0_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve */
+  EDGE0_ERR_UNSUPPORTED = 2,  /* valid request the library does not support */
   EDGE0_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   EDGE0_ERR_OOM = 4,          /* workspace allocation failed */
   EDGE0_ERR_TIMEOUT = 5       /* a device-side bounded wait ran out */

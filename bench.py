@@ -48,7 +48,7 @@ METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofli
 MIN_TIMED_S = 2.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from one
 # ncu capture of the current kernels (profiles/dram_traffic_grouped_decode.md)
-TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1521547008,
+TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1522560256,
            ("layer145b_t1", "moe_decode_kernel"): 45097984}
 
 

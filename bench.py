@@ -36,13 +36,17 @@ WORKLOADS = {
     "stack48_145b_t1": dict(kind="decode", latent=1792, T=1, seed=2, layers=48, zipf=(0.0,), instances=1,
                             desc="48 Edge0-145B layers (all 48x512 experts resident), decode T=1"),
     "layer145b_t4096_zipf": dict(kind="prefill", latent=1792, T=4096, seed=3, layers=1, zipf=(1.1,),
-                                 instances=2, cpu_T=32,
+                                 instances=2,
                                  desc="one Edge0-145B layer, prefill T=4096, Zipf(1.1) router bias"),
     "prefill4x145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=4,
-                                 zipf=(0.0, 1.1, 0.0, 1.1), instances=1, cpu_T=32,
+                                 zipf=(0.0, 1.1, 0.0, 1.1), instances=1,
                                  desc="4 Edge0-145B layers, prefill T=16384, uniform/Zipf(1.1) alternating"),
 }
 DEFAULT_WORKLOAD = "prefill4x145b_t16384"
+# reported with the default workload, each as an object of the same line
+OTHER_CONFIGS = ("layer145b_t1", "layer120b_t4", "stack48_145b_t1", "layer145b_t4096_zipf")
+SWEEP_T = tuple(range(1, 17))          # verify-window sizes of the T = 1..16 decode sweep
+REF_SAMPLE_T = {"prefill": 4}          # tokens per reference-arm step (prefill workloads)
 HIDDEN, E, K, F = 2560, 512, 10, 640
 METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofline"
 MIN_TIMED_S = 2.0
@@ -174,37 +178,144 @@ def measured_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
-# ------------------------------------------------------------------ CPU oracle baseline
-def cpu_baseline(wl, seconds=12.0):
-    """The oracle as it stands, on host cores, for a bounded sample of the workload."""
-    import numpy as np
-    import synth
-    from oracle import moe
+# ------------------------------------------------------------------ oracle legs
+# The bench runs the oracle (test infrastructure) in three places only, all outside
+# the timed regions: the CPU baseline, the reference arm (--impl reference) and the
+# parity report on a token sample of the timed inputs.
+def _cores():
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
-        cores = os.cpu_count() or 1
-    spec = synth.LayerSpec(seed=wl["seed"], layer=0, latent=wl["latent"], zipf=wl["zipf"][0])
+        return os.cpu_count() or 1
+
+
+def _oracle_layer(seed, layer, latent, zipf):
+    import synth
+    from oracle import moe
+    spec = synth.LayerSpec(seed=seed, layer=layer, latent=latent, zipf=zipf)
     inp = synth.make_layer(spec)
-    lay = moe.Layer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn, spec.top_k)
-    T = wl.get("cpu_T", wl["T"])           # prefill: a bounded token sample of the layer
-    done_tokens, t0, it = 0, time.perf_counter(), 0
-    while True:
-        inp._cache.clear()                       # each sample dequantises its experts again
-        x = synth.tokens_bf16(1000 + it, T, HIDDEN)
+    return moe.Layer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn,
+                     spec.top_k), inp
+
+
+def _pool_init():
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(1)
+    except Exception:
+        pass
+
+
+def oracle_task(task):
+    """One parity task (run in a spawned worker): ("layer", seed, layer, latent, zipf,
+    x, y, idx) -> per-layer metrics on the GPU's input and routing; ("chain", seed,
+    n_layers, latent, zipfs, x, idx per layer, y) -> end-to-end error of the oracle
+    stack forced to the GPU's routing."""
+    from oracle import compare, moe
+    import numpy as np
+    if task[0] == "layer":
+        _, seed, layer, latent, zipf, x, y, idx = task
+        lay, _ = _oracle_layer(seed, layer, latent, zipf)
+        rel, mx, flips, bad = compare.layer_check_metrics(lay, x, y, idx)
+        return {"kind": "layer", "rel_l2": rel, "max_abs_over_rms": mx, "flips": flips, "bad": len(bad),
+                "tokens": int(x.shape[0])}
+    _, seed, n_layers, latent, zipfs, x, idx_layers, y = task
+    lays = [_oracle_layer(seed, l, latent, zipfs[l % len(zipfs)])[0] for l in range(n_layers)]
+    xf, flips, bad = compare.stack_chain(lays, x, idx_layers)
+    got, ref = moe.bf16_to_f64(y), moe.bf16_to_f64(xf)
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    return {"kind": "chain", "rel_l2": rel, "flips": flips, "bad": len(bad), "tokens": int(x.shape[0]),
+            "bound": compare.stack_rel_l2(n_layers)}
+
+
+def parity_summary(results):
+    """Aggregate a config's oracle tasks: worst per-layer errors, flips, end to end."""
+    from oracle import compare
+    lay = [r for r in results if r["kind"] == "layer"]
+    ch = [r for r in results if r["kind"] == "chain"]
+    out = {"tokens": max([r["tokens"] for r in results] or [0]), "layers_checked": len(lay),
+           "rel_l2_max": round(max([r["rel_l2"] for r in lay] or [0.0]), 6),
+           "max_abs_over_rms_max": round(max([r["max_abs_over_rms"] for r in lay] or [0.0]), 6),
+           "near_tie_flips": int(sum(r["flips"] for r in lay)),
+           "flips_beyond_gap": int(sum(r["bad"] for r in lay + ch)),
+           "tolerance": {"rel_l2": compare.REL_L2, "max_abs_over_rms": compare.MAX_ABS, "gap": compare.GAP},
+           "teacher_forced": "each layer on the GPU's input; where the GPU's experts differ at a near-tie, "
+                             "the oracle is re-run on the GPU's experts"}
+    if ch:
+        out["end_to_end_rel_l2"] = round(max(r["rel_l2"] for r in ch), 6)
+        out["end_to_end_bound"] = round(ch[0]["bound"], 6)
+    out["pass"] = (out["rel_l2_max"] <= compare.REL_L2 and out["max_abs_over_rms_max"] <= compare.MAX_ABS and
+                   out["flips_beyond_gap"] == 0 and
+                   all(r["rel_l2"] <= r["bound"] for r in ch))
+    return out
+
+
+def cpu_baseline(wl, T_sample=1024):
+    """The oracle as it stands, on host cores, for a bounded sample of the workload:
+    one forward of the workload's first layer at T_sample tokens (prefill), or
+    forwards of the workload's T tokens until ~10 s have passed (decode)."""
+    import synth
+    from oracle import moe
+    lay, inp = _oracle_layer(wl["seed"], 0, wl["latent"], wl["zipf"][0])
+    if wl["kind"] == "prefill":
+        T = min(T_sample, wl["T"])
+        x = synth.tokens_bf16(1000, T, HIDDEN)
+        for e in range(E + 1):               # input bytes generated before the timed region
+            inp.expert(e)
+        t0 = time.perf_counter()
         moe.layer_forward(lay, x)
-        done_tokens += T
-        it += 1
         el = time.perf_counter() - t0
-        if el > seconds or it >= 64:
-            break
-    # per-layer tokens: each sample runs one layer; a stack step runs `layers` of them
-    tok_per_s = done_tokens / el / wl["layers"]
-    return {"value": tok_per_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{it} forward(s) of one layer at T={T} of the workload's layer 0 (fresh expert "
-                      f"dequantisation each), {el:.1f} s; tokens/s through the step = per-layer rate / "
-                      f"{wl['layers']} layer(s)"}
+        v = T / el / wl["layers"]
+        sample = (f"one oracle forward of the workload's layer 0 at T={T} (each expert it uses dequantised "
+                  f"once, fp64 matmuls), {el:.1f} s; tokens/s through the {wl['layers']}-layer step = "
+                  f"per-layer rate / {wl['layers']} (every layer has the same shapes)")
+    else:
+        T = wl["T"]
+        done, it, t0 = 0, 0, time.perf_counter()
+        while True:
+            moe.layer_forward(lay, synth.tokens_bf16(1000 + it, T, HIDDEN))
+            done += T
+            it += 1
+            el = time.perf_counter() - t0
+            if el > 10.0 or it >= 64:
+                break
+        v = done / el / wl["layers"]
+        sample = f"{it} oracle forward(s) of the workload's layer 0 at T={T}, {el:.1f} s"
+    return {"value": round(v, 4), "unit": "tok/s", "cores": _cores(), "kind": "oracle", "sample": sample}
+
+
+def reference_arm(args, wl, config):
+    """--impl reference: the oracle timed on the host, each step one bounded sample
+    of the workload (tokens through every layer of the step), W untimed + K timed."""
+    import synth
+    from oracle import moe
+    lays = [_oracle_layer(wl["seed"], l, wl["latent"], wl["zipf"][l % len(wl["zipf"])])[0]
+            for l in range(wl["layers"])]
+    T_s = REF_SAMPLE_T.get(wl["kind"], 1) if wl["kind"] == "prefill" else wl["T"]
+    times = []
+    for s in range(args.warmup + args.steps):
+        x = synth.tokens_bf16(2000 + s, T_s, HIDDEN)
+        t0 = time.perf_counter()
+        if wl["layers"] > 1:
+            moe.stack_forward(lays, x)
+        else:
+            moe.layer_forward(lays[0], x)
+        el = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(el)
+    step_s = statistics.median(times)
+    v = T_s / step_s
+    sample = (f"{T_s} token(s) of the workload through all {wl['layers']} layer(s) per step "
+              f"(oracle, fp64; each step dequantises the experts its tokens use)")
+    cfg = dict(config, sample=sample, sample_tokens_per_step=T_s)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": cfg,
+            "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 # ------------------------------------------------------------------ our implementation
@@ -221,10 +332,11 @@ def build_instances(wl, n_inst, max_tokens):
     return insts
 
 
-def timed_region(step, args, stream, world, local, est_ms=None):
+def timed_region(step, args, stream, world, local, min_s=MIN_TIMED_S, steps=None):
     """Warm-up, capture of the K timed steps in a CUDA graph, and the replay of that
-    graph enough times (>= MIN_TIMED_S) between events on the launching stream."""
+    graph enough times (>= min_s) between events on the launching stream."""
     import torch
+    steps = steps or args.steps
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i, stream)
@@ -241,7 +353,7 @@ def timed_region(step, args, stream, world, local, est_ms=None):
     try:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
+            for i in range(steps):
                 step(args.warmup + i, stream)
         stream.synchronize()
         graph.replay()                      # one untimed replay (the graph's first launch)
@@ -250,7 +362,7 @@ def timed_region(step, args, stream, world, local, est_ms=None):
         print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
         graph = None
         torch.cuda.synchronize()
-    reps = args.repeat if args.repeat else max(1, int(math.ceil(MIN_TIMED_S / max(est * args.steps, 1e-6))))
+    reps = args.repeat if args.repeat else max(1, int(math.ceil(min_s / max(est * steps, 1e-6))))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -262,7 +374,7 @@ def timed_region(step, args, stream, world, local, est_ms=None):
                 if graph is not None:
                     graph.replay()
                 else:
-                    for i in range(args.steps):
+                    for i in range(steps):
                         step(args.warmup + i, stream)
             ev1.record(stream)
         stream.synchronize()
@@ -270,10 +382,57 @@ def timed_region(step, args, stream, world, local, est_ms=None):
     barrier(world)
     el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     del graph
-    return el_ms, args.steps * reps, reps, clk.summary()
+    return el_ms, steps * reps, reps, clk.summary()
 
 
-def run_decode(args, wl, rank, world, local):
+def e2e_graphs(stream, calls):
+    """One CUDA graph per call: H2D copy of its input from pinned host memory, the
+    library call, D2H copy of its output to pinned host memory."""
+    import torch
+    graphs = []
+    for c in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            c(stream)
+        graphs.append(g)
+    stream.synchronize()
+    return graphs
+
+
+def serial_e2e(stream, graphs, n_steps, world):
+    """Steps one after another, the host reading each step's result before the next
+    (autoregressive decode); CUDA events around the loop on the launching stream."""
+    import torch
+    for g in graphs:
+        g.replay()
+    stream.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n_steps):
+        graphs[i % len(graphs)].replay()
+        stream.synchronize()                  # the host reads the step's result
+    e1.record(stream)
+    stream.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1), world) / n_steps
+
+
+def decode_bytes_of(insts, xs, ys, T, L, stream):
+    """Algorithmic bytes of one forward per instance (distinct routed experts read once)."""
+    import numpy as np
+    import latent_sparse_moe_router_b300 as ext
+    out, distinct = [], []
+    for j, d in enumerate(insts):
+        ext.edge0_moe_forward(d.handle, xs[j], ys[j], T, stream)
+        stream.synchronize()
+        u = len(np.unique(d.routing(T)["idx"]))
+        distinct.append(u)
+        out.append(decode_algorithmic_bytes(L, T, u))
+    return float(np.mean(out)), float(np.mean(distinct))
+
+
+def run_decode(args, wl, rank, world, local, sweep=None, parity_tokens=2):
+    """Decode workloads: one layer at T <= 16 over rotated instances, or the 48-layer stack."""
     import numpy as np
     import torch
     import synth
@@ -284,6 +443,8 @@ def run_decode(args, wl, rank, world, local):
     T, L, n_layers = wl["T"], wl["latent"], wl["layers"]
     hbm, bf16, bf16_s, peak_kind = measured_peaks()
     stream = torch.cuda.Stream()
+    jobs = []
+    sweep_out = None
     if n_layers == 1:
         insts = build_instances(wl, wl["instances"], max_tokens=16)
         n_inst = len(insts)
@@ -294,14 +455,27 @@ def run_decode(args, wl, rank, world, local):
         def step(i, s):
             j = i % n_inst
             ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, s)
-        launches_per_step = 1
-        distinct = []
-        for j in range(n_inst):
+        bytes_per_step, mean_u = decode_bytes_of(insts, xs, ys, T, L, stream)
+        work_note = f"mean distinct routed experts {mean_u:.2f} over {n_inst} rotated instances"
+        # parity sample: the timed inputs of the first instances
+        for j in range(min(parity_tokens, n_inst)):
             ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, stream)
             stream.synchronize()
-            distinct.append(len(np.unique(insts[j].routing(T)["idx"])))
-        bytes_per_step = float(np.mean([decode_algorithmic_bytes(L, T, d) for d in distinct]))
-        work_note = f"mean distinct routed experts {np.mean(distinct):.2f}"
+            jobs.append(("layer", wl["seed"], j, L, wl["zipf"][j % len(wl["zipf"])],
+                         device.bf16_bits(xs[j]), device.bf16_bits(ys[j]), insts[j].routing(T)["idx"]))
+        # e2e: pinned host buffers, H2D x, forward, D2H y per step, host waits per step
+        hx = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(n_inst)]
+        hy = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(n_inst)]
+        for j in range(n_inst):
+            hx[j].copy_(xs[j].cpu())
+
+        def e2e_call(j):
+            def c(s):
+                xs[j].copy_(hx[j], non_blocking=True)
+                ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, s)
+                hy[j].copy_(ys[j], non_blocking=True)
+            return c
+        e2e_bytes = T * HIDDEN * 2
     else:
         # the 48-layer stack: all 48 x 512 records resident in one allocation
         stride = ext.edge0_expert_record_stride(L, F)
@@ -314,15 +488,41 @@ def run_decode(args, wl, rank, world, local):
         torch.cuda.synchronize()
         handles = [d.handle for d in insts]
         n_tok = 256
-        xs_all = device.bf16_tensor(synth.tokens_bf16(wl["seed"], n_tok, HIDDEN))
+        x_bits_all = synth.tokens_bf16(wl["seed"], n_tok, HIDDEN)
+        xs_all = device.bf16_tensor(x_bits_all)
         ys_all = torch.empty_like(xs_all)
 
         def step(i, s):
             j = i % n_tok
             ext.edge0_moe_stack_forward(handles, xs_all[j:j + 1], ys_all[j:j + 1], 1, 1e-6, s)
-        launches_per_step = 1
         bytes_per_step = n_layers * decode_algorithmic_bytes(L, 1, K)
         work_note = "48 layers x (D + U + router + 10 routed + 1 shared record) per token"
+        # parity sample: tokens of the timed sequence, every layer traced
+        for j in range(parity_tokens):
+            tx = torch.empty((n_layers, 1, HIDDEN), dtype=torch.bfloat16, device="cuda")
+            ty = torch.empty_like(tx)
+            ti = torch.empty((n_layers, 1, K), dtype=torch.int32, device="cuda")
+            yj = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device="cuda")
+            ext.edge0_moe_stack_forward_trace(handles, xs_all[j:j + 1], yj, 1, 1e-6, tx, ty, ti, stream)
+            stream.synchronize()
+            txb, tyb, tib = device.bf16_bits(tx), device.bf16_bits(ty), ti.cpu().numpy()
+            for l in range(n_layers):
+                jobs.append(("layer", wl["seed"], l, L, 0.0, txb[l], tyb[l], tib[l]))
+            jobs.append(("chain", wl["seed"], n_layers, L, (0.0,), x_bits_all[j:j + 1], tib, device.bf16_bits(yj)))
+        hx = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+        hy = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(xs_all[:1].cpu())
+        xd = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device="cuda")
+        yd = torch.empty_like(xd)
+        n_inst = 1
+
+        def e2e_call(j):
+            def c(s):
+                xd.copy_(hx, non_blocking=True)
+                ext.edge0_moe_stack_forward(handles, xd, yd, 1, 1e-6, s)
+                hy.copy_(yd, non_blocking=True)
+            return c
+        e2e_bytes = HIDDEN * 2
 
     el_ms, steps_done, reps, clocks = timed_region(step, args, stream, world, local)
     ms_per_step = el_ms / steps_done
@@ -333,59 +533,41 @@ def run_decode(args, wl, rank, world, local):
             "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC.get((wl["name"], "moe_decode_kernel")),
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "kernel": "moe_decode_kernel", "bytes_per_launch": bytes_per_step, "note": work_note}
+    graphs = e2e_graphs(stream, [e2e_call(j) for j in range(n_inst)])
+    e_ms = serial_e2e(stream, graphs, max(args.steps, 32) if n_layers == 1 else 16, world)
+    del graphs
+    e2e = {"value": round(T * world / (e_ms / 1e3), 2), "unit": "tok/s", "h2d_bytes_per_step": e2e_bytes,
+           "d2h_bytes_per_step": e2e_bytes, "pipelined": False,
+           "note": "each step a CUDA graph of [H2D x from pinned host, forward, D2H y to pinned host]; "
+                   "the host waits for every step's result before the next"}
 
-    # e2e through the C ABI with pinned host buffers: H2D x, forward, D2H y, per step
-    if n_layers == 1:
-        hx = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
-        hy = [torch.empty((T, HIDDEN), dtype=torch.bfloat16, pin_memory=True) for _ in range(len(insts))]
-        for j in range(len(insts)):
-            hx[j].copy_(xs[j].cpu())
-        n_e2e = max(args.steps, 32)
-        torch.cuda.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for i in range(n_e2e):
-                j = i % len(insts)
-                xs[j].copy_(hx[j], non_blocking=True)
-                ext.edge0_moe_forward(insts[j].handle, xs[j], ys[j], T, stream)
-                hy[j].copy_(ys[j], non_blocking=True)
-                stream.synchronize()             # the host reads the step's result
-            e1.record(stream)
-        stream.synchronize()
-        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
-        e2e = {"value": round(T * world / (e_ms / 1e3), 1), "unit": "tok/s",
-               "h2d_bytes_per_step": T * HIDDEN * 2, "d2h_bytes_per_step": T * HIDDEN * 2}
-    else:
-        hx = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
-        hy = torch.empty((1, HIDDEN), dtype=torch.bfloat16, pin_memory=True)
-        hx.copy_(xs_all[:1].cpu())
-        xd = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device="cuda")
-        yd = torch.empty_like(xd)
-        n_e2e = 16
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for i in range(n_e2e):
-                xd.copy_(hx, non_blocking=True)
-                ext.edge0_moe_stack_forward(handles, xd, yd, 1, 1e-6, stream)
-                hy.copy_(yd, non_blocking=True)
-                stream.synchronize()
-            e1.record(stream)
-        stream.synchronize()
-        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
-        e2e = {"value": round(world / (e_ms / 1e3), 2), "unit": "tok/s",
-               "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 2}
+    if sweep:
+        # verify-window sweep: T tokens per forward over the same rotated instances
+        sweep_out = []
+        for Ts in sweep:
+            xs_s = [device.bf16_tensor(synth.tokens_bf16(7000 + Ts * 100 + i, Ts, HIDDEN)) for i in range(n_inst)]
+            ys_s = [torch.empty_like(x) for x in xs_s]
+            b, mu = decode_bytes_of(insts, xs_s, ys_s, Ts, L, stream)
 
+            def step_s(i, s, xs_s=xs_s, ys_s=ys_s, Ts=Ts):
+                j = i % n_inst
+                ext.edge0_moe_forward(insts[j].handle, xs_s[j], ys_s[j], Ts, s)
+            el, nd, _, ck = timed_region(step_s, args, stream, world, local, min_s=0.4)
+            ms = el / nd
+            gbs = b / (ms / 1e3) / 1e9
+            sweep_out.append({"T": Ts, "tok_s": round(Ts * world / (ms / 1e3), 1), "us_per_forward": round(ms * 1e3, 2),
+                              "distinct_experts": round(mu, 2), "bytes_per_forward": round(b),
+                              "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                              "sm_mhz": ck["sm_mhz"]})
+    errs = [ext.edge0_moe_get_error(d.handle) for d in insts]
+    assert all(e == ext.EDGE0_OK for e in errs), f"device wait ran out: {errs}"
     for d in insts:
         d.close()
     return dict(value=value, ms_per_step=ms_per_step, roofline=roof, e2e=e2e,
-                gpu_launches=launches_per_step * steps_done, clocks=clocks, steps_done=steps_done)
+                gpu_launches=1 * steps_done, clocks=clocks, steps_done=steps_done, jobs=jobs, sweep=sweep_out)
 
 
-def run_prefill(args, wl, rank, world, local):
+def run_prefill(args, wl, rank, world, local, parity_tokens=8):
     import numpy as np
     import torch
     import synth
@@ -404,18 +586,20 @@ def run_prefill(args, wl, rank, world, local):
     torch.cuda.synchronize()
     handles = [d.handle for d in insts]
     n_x = 1 if n_layers > 1 else n_inst
-    xs = [device.bf16_tensor(synth.tokens_bf16(wl["seed"] * 1000 + rank * 100 + i, T, HIDDEN)) for i in range(n_x)]
+    x_bits = [synth.tokens_bf16(wl["seed"] * 1000 + rank * 100 + i, T, HIDDEN) for i in range(n_x)]
+    xs = [device.bf16_tensor(b) for b in x_bits]
     ys = [torch.empty_like(x) for x in xs]
+    per_fwd = ext.PREFILL_KERNELS_PER_FORWARD
     if n_layers > 1:
         def step(i, s):
             ext.edge0_moe_stack_forward(handles, xs[0], ys[0], T, 1e-6, s)
         # per layer: the prefill kernels plus the residual norm
-        launches_per_step = n_layers * (ext.EDGE0_PREFILL_STAGES + 1)
+        launches_per_step = n_layers * (per_fwd + 1)
     else:
         def step(i, s):
             j = i % n_inst
             ext.edge0_moe_forward(handles[j], xs[j], ys[j], T, s)
-        launches_per_step = ext.EDGE0_PREFILL_STAGES
+        launches_per_step = per_fwd
 
     el_ms, steps_done, reps, clocks = timed_region(step, args, stream, world, local)
     ms_per_step = el_ms / steps_done
@@ -452,19 +636,44 @@ def run_prefill(args, wl, rank, world, local):
     tname = names[top]
     if tname in sflops:
         ach = sflops[tname] / (stage_ms[top] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16_s, "unit": "TFLOP/s",
-                "frac": round(ach / bf16_s, 4), "traffic": TRAFFIC.get((wl["name"], tname)), "kernel": tname,
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(ach / bf16, 4), "traffic": TRAFFIC.get((wl["name"], tname)), "kernel": tname,
                 "flops_per_launch": sflops[tname],
-                "peak_kind": f"{peak_kind} cuBLAS bf16 sustained (kernel timed inside the step); "
-                             f"frac of burst {bf16} = {ach / bf16:.4f}"}
+                "peak_kind": f"{peak_kind} cuBLAS bf16 dense burst (kernel timed alone by stage events at "
+                             f"median SM {clocks['sm_mhz']} MHz of max {clocks['sm_max_mhz']})",
+                "frac_of_sustained": round(ach / bf16_s, 4),
+                "sustained_peak": bf16_s}
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None, "traffic": None,
                 "kernel": tname, "note": "dominant stage is not a contraction"}
-    roof["step"] = {"tflops": round(step_tflops, 1), "frac_sustained": round(step_tflops / bf16_s, 4),
-                    "frac_burst": round(step_tflops / bf16, 4), "flops_per_step": step_flops,
+    roof["step"] = {"tflops": round(step_tflops, 1), "frac_burst": round(step_tflops / bf16, 4),
+                    "frac_sustained": round(step_tflops / bf16_s, 4), "flops_per_step": step_flops,
                     "flops_per_token_layer": flops_per_token_layer(L)}
     stages = {n: round(float(m), 4) for n, m in zip(names, stage_ms)}
     stages["timed_layer_ms_sum"] = round(float(stage_ms.sum()), 4)
+
+    # parity sample: seeded token rows of the timed input, every layer on the GPU's
+    # input to it (per-layer calls reproduce the stack's bits) and the stack end to end
+    jobs = []
+    sel = np.sort(np.random.default_rng(77).choice(T, parity_tokens, replace=False))
+    cur = xs[0]
+    idx_layers = []
+    for l in range(n_layers):
+        yl = torch.empty_like(cur)
+        ext.edge0_moe_forward(handles[l], cur, yl, T, stream)
+        stream.synchronize()
+        idx = insts[l].routing(T)["idx"][sel]
+        idx_layers.append(idx)
+        jobs.append(("layer", wl["seed"], l, L, wl["zipf"][l % len(wl["zipf"])],
+                     device.bf16_bits(cur)[sel], device.bf16_bits(yl)[sel], idx))
+        if n_layers > 1:
+            nx = torch.empty_like(cur)
+            ext.edge0_residual_rmsnorm(cur, yl, nx, T, HIDDEN, 1e-6, stream)
+            cur = nx
+    if n_layers > 1:
+        stream.synchronize()
+        jobs.append(("chain", wl["seed"], n_layers, L, wl["zipf"], x_bits[0][sel], idx_layers,
+                     device.bf16_bits(cur)[sel]))
 
     # e2e through the C ABI with pinned host buffers: every step copies its x in from pinned
     # host memory, runs the forward and copies its y out to pinned host memory, and the host
@@ -527,7 +736,7 @@ def run_prefill(args, wl, rank, world, local):
         d.close()
     return dict(value=value, ms_per_step=ms_per_step, roofline=roof, e2e=e2e,
                 gpu_launches=launches_per_step * steps_done, clocks=clocks, steps_done=steps_done,
-                stages=stages, layer_tok_s=value * n_layers)
+                stages=stages, layer_tok_s=value * n_layers, jobs=jobs)
 
 
 def config_of(name, wl, world):
@@ -544,6 +753,18 @@ def config_of(name, wl, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
 
 
+def sub_line(name, r, world):
+    """The other configurations' objects in the default line."""
+    wl = WORKLOADS[name]
+    out = {"workload": name, "desc": wl["desc"], "value": round(r["value"], 2), "unit": "tok/s",
+           "ms_per_step": round(r["ms_per_step"], 6), "roofline": r["roofline"], "e2e": r["e2e"],
+           "clocks": r["clocks"], "gpu_launches": r["gpu_launches"], "steps": r["steps_done"],
+           "config": config_of(name, dict(wl, name=name), world)}
+    if wl["kind"] == "prefill":
+        out["stages_ms_per_layer"] = r["stages"]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,7 +776,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
-                    help="skip the T=1 decode line that the default prefill run also reports")
+                    help="report the default workload alone (skip the other configurations and the sweep)")
+    ap.add_argument("--no-parity", action="store_true", help="skip the oracle parity report")
+    ap.add_argument("--only", default="",
+                    help="comma list of the other configurations to report with the default workload")
     ap.add_argument("--instances", type=int, default=0,
                     help="override the number of rotated layer instances (profiling runs)")
     args = ap.parse_args()
@@ -569,41 +793,50 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        t_steps = []
-        sample = None
-        for s in range(args.warmup + args.steps):
-            cb = cpu_baseline(wl, seconds=max(2.0, 60.0 / (args.steps + args.warmup)))
-            if s >= args.warmup:
-                t_steps.append(cb["value"])
-            sample = cb
-        v = statistics.median(t_steps)
-        line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tok/s", "n_gpus": 1,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wl["T"] / v, 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded)", "config": config,
-                "cpu_baseline": {"value": round(v, 3), "unit": "tok/s", "cores": sample["cores"],
-                                 "kind": "oracle", "sample": sample["sample"]},
-                "e2e": {"value": round(v, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(reference_arm(args, wl, config)), flush=True)
         return
 
+    # the oracle's parity workers are spawned before any CUDA work of this process
+    pool = None
+    if not args.no_parity and rank == 0:
+        import multiprocessing as mp
+        pool = mp.get_context("spawn").Pool(max(1, min(32, os.cpu_count() or 1)), initializer=_pool_init)
+
     run = run_prefill if wl["kind"] == "prefill" else run_decode
-    r = run(args, wl, rank, world, local)
-    extra = {}
+    kw = {"sweep": SWEEP_T} if (wl["name"] == "layer145b_t1" and not args.no_decode) else {}
+    r = run(args, wl, rank, world, local, **kw)
+    extra, jobs = {}, {args.workload: r["jobs"]}
     if wl["kind"] == "prefill":
         extra["stages_ms_per_layer"] = r["stages"]
         extra["layer_tok_s"] = round(r["layer_tok_s"], 1)
-    # the metric's other half (T = 1 decode) on the same run
+    if r.get("sweep"):
+        extra["verify_sweep"] = r["sweep"]
+    # the other configurations (and the T = 2..16 verify-window sweep) on the same run
     if args.workload == DEFAULT_WORKLOAD and not args.no_decode:
-        dwl = dict(WORKLOADS["layer145b_t1"], name="layer145b_t1")
         import torch
-        torch.cuda.empty_cache()
-        dr = run_decode(args, dwl, rank, world, local)
-        extra["decode_t1"] = {"workload": "layer145b_t1", "value": round(dr["value"], 1), "unit": "tok/s",
-                              "ms_per_step": round(dr["ms_per_step"], 6), "roofline": dr["roofline"],
-                              "e2e": dr["e2e"], "clocks": dr["clocks"], "gpu_launches": dr["gpu_launches"]}
+        others = [n for n in OTHER_CONFIGS if not args.only or n in args.only.split(",")]
+        for name in others:
+            torch.cuda.empty_cache()
+            owl = dict(WORKLOADS[name], name=name)
+            if owl["kind"] == "decode":
+                o = run_decode(args, owl, rank, world, local, sweep=SWEEP_T if name == "layer145b_t1" else None)
+            else:
+                o = run_prefill(args, owl, rank, world, local)
+            jobs[name] = o["jobs"]
+            key = "decode_t1" if name == "layer145b_t1" else name
+            extra[key] = sub_line(name, o, world)
+            if o.get("sweep"):
+                extra["verify_sweep"] = {"workload": name, "layer": "Edge0-145B", "points": o["sweep"]}
     if rank != 0:
         return
+    if pool is not None:
+        parity = {}
+        for name, js in jobs.items():
+            res = pool.map(oracle_task, js) if js else []
+            parity[name] = parity_summary(res)
+        pool.close()
+        pool.join()
+        extra["parity"] = parity
     cb = None if args.no_cpu_baseline else cpu_baseline(wl)
     line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "tok/s", "n_gpus": world,
             "steps": r["steps_done"], "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 6),

@@ -227,14 +227,16 @@ edge0_status edge0_moe_stack_forward(void *const *handles, int n_layers, const v
                                      void *y, int T, float eps, edge0_stream_t stream);
 
 /*
- * edge0_moe_stack_forward that also records every layer's input and output
- * (for layer-by-layer checks): trace_x, trace_y device bf16 [n_layers][T][hidden]
- * (either may be NULL).  Decode sizes only (T <= 16, n_layers <= 64); other
- * sizes return UNSUPPORTED when a trace is requested.
+ * edge0_moe_stack_forward that also records every layer's input, output and
+ * routing (for layer-by-layer checks): trace_x, trace_y device bf16
+ * [n_layers][T][hidden]; trace_idx device int32 [n_layers][T][top_k], the
+ * experts each layer kept for each token in rank order (any may be NULL).
+ * Decode sizes only (T <= 16, n_layers <= 64); other sizes return UNSUPPORTED
+ * when a trace is requested.
  */
 edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, const void *x,
                                            void *y, int T, float eps, void *trace_x,
-                                           void *trace_y, edge0_stream_t stream);
+                                           void *trace_y, int *trace_idx, edge0_stream_t stream);
 
 /*
  * Decode forward (T <= 16) that allocates no device memory: the paper has no
@@ -248,15 +250,18 @@ edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, c
  *             EDGE0_OK or the device error bits (a wait that ran out)
  * Scratch lives in one static device array of this library (about 7.8 MB, held
  * by every GPU that loads the library until the process exits).  Limits:
- * T <= 16, hidden <= 3072, latent <= 2048, n_experts <= 512, ffn <= 1024;
- * larger sizes return EDGE0_ERR_UNSUPPORTED without touching the device.
+ * T <= 16, hidden <= 3072, latent <= 2048, n_experts <= 512, ffn <= 1024, and
+ * the decode kernel's shared-memory plan must fit the device (the check
+ * edge0_moe_create makes); other sizes return EDGE0_ERR_UNSUPPORTED without
+ * launching anything.
  * The first call on a device looks up the array's device address and sets the
  * decode kernel's launch attributes (once per device, with that device
  * current): make that first call before any stream capture.  All calls share
  * the array and each clears the words that must start at zero; calls that
  * overlap on the GPU race, so the caller must serialise them.  Each call also
- * recomputes R D into the array, and z enters the expert dot products as f16
- * without the range pre-scaling the handle path applies.
+ * recomputes R D and the |z| bound max_r sum_h |D_rh| into the array (two
+ * small kernels before the forward; the forward then scales z per token by a
+ * power of two exactly as the handle path does).
  */
 edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc *desc, const void *x, void *y, int T,
                                        int *status_out, edge0_stream_t stream);

@@ -31,6 +31,9 @@ EXPORTED = (
 )
 
 EDGE0_PREFILL_STAGES = 10
+# kernels one prefill forward launches (token scale, x -> [z | logits], top-k +
+# histogram, scan, offsets, scatter, row gather, gate/up, down, combine, U)
+PREFILL_KERNELS_PER_FORWARD = 11
 PREFILL_STAGE_NAMES = ("xz_gemm", "topk_hist", "scan_chunks", "offsets", "scatter", "gather_rows",
                        "gate_up_grouped", "down_grouped", "combine", "u_gemm")
 
@@ -74,7 +77,7 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_debug_tensor": (i, [vp, i, vp, sz, vp]),
             "edge0_residual_rmsnorm": (i, [vp, vp, vp, i, i, f, vp]),
             "edge0_moe_stack_forward": (i, [vp, i, vp, vp, i, f, vp]),
-            "edge0_moe_stack_forward_trace": (i, [vp, i, vp, vp, i, f, vp, vp, vp]),
+            "edge0_moe_stack_forward_trace": (i, [vp, i, vp, vp, i, f, vp, vp, vp, vp]),
             "edge0_moe_get_error": (i, [vp]),
             "edge0_status_string": (ctypes.c_char_p, [i]),
             "edge0_moe_destroy": (None, [vp]),
@@ -203,11 +206,11 @@ def edge0_moe_stack_forward(handles, x, y, T, eps, stream=None):
            "edge0_moe_stack_forward")
 
 
-def edge0_moe_stack_forward_trace(handles, x, y, T, eps, trace_x, trace_y, stream=None):
+def edge0_moe_stack_forward_trace(handles, x, y, T, eps, trace_x, trace_y, trace_idx=None, stream=None):
     arr = _handle_array(handles)
     _check(lib().edge0_moe_stack_forward_trace(ctypes.cast(arr, ctypes.c_void_p), len(handles),
                                                _ptr(x), _ptr(y), T, float(eps), _ptr(trace_x),
-                                               _ptr(trace_y), _stream(stream)),
+                                               _ptr(trace_y), _ptr(trace_idx), _stream(stream)),
            "edge0_moe_stack_forward_trace")
 
 

@@ -103,6 +103,18 @@ void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
   a.dyn_bytes = (int)((hd->smem_total - off) & ~size_t(1023));
 }
 
+// Every decode bucket leaves room in the staged-weight region for at least an fp32
+// R D row pair and a gate/up row pair (the smallest unit each phase stages).
+bool decode_fits(const Handle* hd) {
+  for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
+    DecodeArgs a;
+    decode_plan(hd, TB, a);
+    const int need = 4 * hd->d.hidden * 2 + 8192;
+    if (a.dyn_bytes < need) return false;
+  }
+  return true;
+}
+
 edge0_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA; }
 
 LayerW layer_of(const Handle* hd) {
@@ -185,23 +197,20 @@ __global__ void fold_router_kernel(const __nv_bfloat16* __restrict__ R, const __
   }
 }
 
-// out = max_r sum_h |D[r][h]| (one block; fixed reduction order)
+// *out = max_r sum_h |D[r][h]|: one warp per row (lane-strided sums, then an xor
+// tree: a fixed order per row); the maximum is taken with an integer atomicMax on
+// the bits of the non-negative sums, which is exact in any order.  *out must be 0.
 __global__ void row_l1_max_kernel(const __nv_bfloat16* __restrict__ D, int rows, int cols, float* out) {
-  __shared__ float red[32];
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
   float m = 0.f;
-  for (int r = threadIdx.x >> 5; r < rows; r += blockDim.x >> 5) {
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
     float s = 0.f;
-    for (int c = threadIdx.x & 31; c < cols; c += 32) s += fabsf(__bfloat162float(D[size_t(r) * cols + c]));
+    for (int c = lane; c < cols; c += 32) s += fabsf(__bfloat162float(D[size_t(r) * cols + c]));
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     m = fmaxf(m, s);
   }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mm = fmaxf(mm, red[i]);
-    *out = mm;
-  }
+  if (lane == 0 && m > 0.f) atomicMax(reinterpret_cast<int*>(out), __float_as_int(m));
 }
 
 // E4M3FN round-to-nearest-even of a non-negative double, saturating at 448.
@@ -386,13 +395,7 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   if (prop.major < 10 || !prop.cooperativeLaunch) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
   hd->num_sms = prop.multiProcessorCount;
   hd->smem_total = (int)prop.sharedMemPerBlockOptin - 1024;
-  // every decode bucket must leave room for at least one staged row and one P3 group
-  for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
-    DecodeArgs a;
-    decode_plan(hd, TB, a);
-    const int need = 4 * d.hidden * 2 + 8192;   // an fp32 R D row pair, a gate/up row pair
-    if (a.dyn_bytes < need) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
-  }
+  if (!decode_fits(hd)) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
   if ((ce = decode_prepare(hd->smem_total)) != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
   int occ = 0;
   if ((ce = decode_occupancy(hd->smem_total, &occ)) != cudaSuccess || occ < 1) {
@@ -443,7 +446,7 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   hd->pf.rd = hd->rd;
   ce = cudaMemset(hd->ws, 0, o_lw);
   if (ce == cudaSuccess) {
-    row_l1_max_kernel<<<1, 1024>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, d_dnorm);
+    row_l1_max_kernel<<<(L + 7) / 8, 256>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, d_dnorm);
     ce = cudaGetLastError();
   }
   if (ce == cudaSuccess) ce = cudaMemcpy(&hd->dnorm, d_dnorm, sizeof(float), cudaMemcpyDeviceToHost);
@@ -556,7 +559,7 @@ static bool same_layers(const std::vector<LayerW>& a, const std::vector<LayerW>&
 }
 
 static edge0_status stack_impl(void* const* handles, int n_layers, const void* x, void* y, int T, float eps,
-                               void* trace_x, void* trace_y, edge0_stream_t stream) {
+                               void* trace_x, void* trace_y, int* trace_idx, edge0_stream_t stream) {
   if (!handles || n_layers < 1 || T < 0 || !(eps >= 0.f)) return EDGE0_ERR_INVALID_ARG;
   if (T == 0) return EDGE0_OK;
   Handle* h0 = static_cast<Handle*>(handles[0]);
@@ -569,7 +572,7 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
       return EDGE0_ERR_INVALID_ARG;
   }
   if (T > kDecodeMaxT || n_layers > kStackMax) {
-    if (trace_x || trace_y) return EDGE0_ERR_UNSUPPORTED;
+    if (trace_x || trace_y || trace_idx) return EDGE0_ERR_UNSUPPORTED;
     // chain: layer forward into the prefill scratch of handle 0, then the residual norm
     if (T > h0->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
     __nv_bfloat16* tmp = prefill_stack_scratch(&h0->pf);
@@ -607,6 +610,7 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
   a.final_norm = 1;
   a.trace_x = static_cast<__nv_bfloat16*>(trace_x);
   a.trace_y = static_cast<__nv_bfloat16*>(trace_y);
+  a.trace_idx = trace_idx;
   e = decode_launch(a, h0->num_sms, h0->smem_total, s);
   if (e != cudaSuccess) return EDGE0_ERR_CUDA;
   h0->last_T = T;
@@ -616,13 +620,13 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
 
 edge0_status edge0_moe_stack_forward(void* const* handles, int n_layers, const void* x, void* y, int T,
                                      float eps, edge0_stream_t stream) {
-  return stack_impl(handles, n_layers, x, y, T, eps, nullptr, nullptr, stream);
+  return stack_impl(handles, n_layers, x, y, T, eps, nullptr, nullptr, nullptr, stream);
 }
 
 edge0_status edge0_moe_stack_forward_trace(void* const* handles, int n_layers, const void* x, void* y,
-                                           int T, float eps, void* trace_x, void* trace_y,
+                                           int T, float eps, void* trace_x, void* trace_y, int* trace_idx,
                                            edge0_stream_t stream) {
-  return stack_impl(handles, n_layers, x, y, T, eps, trace_x, trace_y, stream);
+  return stack_impl(handles, n_layers, x, y, T, eps, trace_x, trace_y, trace_idx, stream);
 }
 
 edge0_status edge0_moe_debug_wait_probe(void* handle, edge0_stream_t stream) {
@@ -711,7 +715,7 @@ constexpr size_t kNaXb = kNaYb + na_align(size_t(2) * kNaMaxT * kNaMaxH * 2);
 constexpr size_t kNaRt = kNaXb + na_align(size_t(2) * kNaMaxT * kNaMaxH * 2); // idx w perm pos
 constexpr size_t kNaCnt = kNaRt + na_align(size_t(4) * kNaMaxT * kNaMaxK * 4);
 constexpr size_t kNaOff = kNaCnt + na_align(size_t(kNaMaxE) * 4);
-constexpr size_t kNaBar = kNaOff + na_align(size_t(kNaMaxE + 1) * 4);        // barrier, then error word
+constexpr size_t kNaBar = kNaOff + na_align(size_t(kNaMaxE + 1) * 4);        // barrier, error word, dnorm
 constexpr size_t kNaBytes = kNaBar + 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
@@ -806,18 +810,23 @@ extern "C" edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc* desc, co
   view.offsets = reinterpret_cast<int*>(s + kNaOff);
   view.bar = reinterpret_cast<GridBarrier*>(s + kNaBar);
   view.err = reinterpret_cast<int*>(s + kNaBar + 128);
-  // the array keeps the previous call's contents: the barrier and the error word
-  // must start at zero
+  // the decode kernel's shared-memory plan must fit this device (as create checks)
+  if (!decode_fits(&view)) return EDGE0_ERR_UNSUPPORTED;
+  // the array keeps the previous call's contents: the barrier, the error word and
+  // the |z| bound's maximum must start at zero
   if (cudaMemsetAsync(s + kNaBar, 0, 256, cs) != cudaSuccess) return EDGE0_ERR_CUDA;
-  // R D for this layer, into the scratch
+  float* dnorm_dev = reinterpret_cast<float*>(s + kNaBar + 192);
+  // R D and the bound max_r sum_h |D_rh| for this layer, into the scratch (the
+  // kernel scales z per token by a power of two from that bound, as on a handle)
   const int H = d.hidden, L = d.latent, E = d.n_experts;
   fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256, 0, cs>>>(
       static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), view.rd, E, L, H);
+  row_l1_max_kernel<<<(L + 7) / 8, 256, 0, cs>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, dnorm_dev);
   if (cudaGetLastError() != cudaSuccess) return EDGE0_ERR_CUDA;
   DecodeArgs a;
   fill_decode_args(&view, a, x, y, T);
   a.layers = nullptr;              // one layer: the kernel reads only a.l0
-  a.l0.dnorm = INFINITY;           // no |z| bound without a host read: z goes to f16 unscaled
+  a.dnorm_dev = dnorm_dev;
   if (decode_launch(a, nd->num_sms, nd->smem_total, cs) != cudaSuccess) return EDGE0_ERR_CUDA;
   if (status_out &&
       cudaMemcpyAsync(status_out, view.err, sizeof(int), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)

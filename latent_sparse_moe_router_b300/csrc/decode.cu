@@ -208,6 +208,10 @@ __device__ void dense_rows(Ctx& cx, const RowSet* rs, int nset, const void* act,
   for (int m = 0; m < nset; ++m) total += rs[m].r1 - rs[m].r0;
   const int n0 = rs[0].r1 - rs[0].r0;
   const int cap = dense_cap(rs, nset, dyn_bytes);
+  if (cap < 1) {   // not even one row fits (the host rejects such shapes): stop, do not spin
+    if (threadIdx.x == 0 && total > 0) atomicOr(cx.err, kErrTimeout);
+    return;
+  }
   for (int from = 0; from < total; from += cap) {
     const int n = min(cap, total - from);
     if (!(prestaged && from == 0)) {
@@ -410,6 +414,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   const int j0 = int(long(bid) * H / G), j1 = int(long(bid + 1) * H / G);      // hidden rows
   const int nr = r1 - r0, nsr = f1 - f0;
 
+  // a launch after one whose wait ran out finds the grid barrier mid-round (reset
+  // by edge0_moe_get_error): it does no work and leaves the error word set
+  if (ld_relaxed_u32(&a.bar->abort)) {
+    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    return;
+  }
   if (tid == 0) {
     for (int b = 0; b < kNumMbar; ++b) mbar_init(&tb->mbar[b], b == kMbScale ? kScaleWarps : 1);
     fence_mbar_init();
@@ -480,7 +490,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       if (tid < T) {
         float m = 0.f;
         for (int wv = 0; wv < kDecWarps; ++wv) m = fmaxf(m, tb->red[wv * kDecodeMaxT + tid]);
-        pow2_scale(m * lw.dnorm, &tb->zsc[tid], &tb->zinv[tid]);
+        const float dn = (li == 0 && a.dnorm_dev) ? *a.dnorm_dev : lw.dnorm;
+        pow2_scale(m * dn, &tb->zsc[tid], &tb->zinv[tid]);
       }
       __syncthreads();
       float* z = a.z;
@@ -603,6 +614,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         tb->down_staged = stage_down ? 1 : 0;
         tb->down_off = gu_alloc;
       }
+      if (bid == 0 && a.trace_idx)
+        for (int s = tid; s < TK; s += kDecThreads) a.trace_idx[size_t(li) * TK + s] = tb->idx[s];
       // bid 0 publishes the routing of the last layer
       if (bid == 0 && last) {
         for (int s = tid; s < TK; s += kDecThreads) {
@@ -647,6 +660,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       while (qa < q1) {
         // with the down rows staged behind it, every round stays inside gu_alloc
         const int cap = min(256, (stage_down ? gu_alloc : a.dyn_bytes) / per_row);
+        if (cap < 1) {   // not even one row fits (the host rejects such shapes): stop, do not spin
+          if (tid == 0) atomicOr(a.err, kErrTimeout);
+          break;
+        }
         const int nrow = min(cap, q1 - qa);
         // batches of BR rows, one lane of warp 0 each (a batch may span a group boundary)
         const int BR = (nrow + kMbRounds - 1) / kMbRounds;

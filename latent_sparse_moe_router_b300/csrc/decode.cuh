@@ -75,6 +75,8 @@ struct DecodeArgs {
   int* idx; float* w; int* counts; int* offsets; int* perm; int* pos;  // last layer's routing
   __nv_bfloat16* trace_x;   // optional [n_layers][T][H]: input of every layer
   __nv_bfloat16* trace_y;   // optional [n_layers][T][H]: output of every layer
+  int* trace_idx;           // optional [n_layers][T][K]: experts each layer picked, in rank order
+  const float* dnorm_dev;   // optional: device copy of the first layer's dnorm (used in place of l0.dnorm)
   GridBarrier* bar;
   int* err;
   // shared-memory plan (bytes from the 128-aligned dynamic base)

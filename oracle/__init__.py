@@ -13,6 +13,9 @@ Modules
           SwiGLU experts, shared expert, combine, U) and the post-norm stack.
   record  a reader of the packed expert record, written from the layout the
           library's header documents (pins the packer byte for byte).
+  compare tolerances and routing-flip rule of the parity checks, the per-layer
+          teacher-forced comparison and the teacher-forced stack chain (used by
+          the tests and by the bench's parity report).
 
 Parity status: the decoders, top-k, weights, permutation, SwiGLU, RMSNorm and
 the record reader are pinned by tests against definitions, brute force and

@@ -1,53 +1,14 @@
-"""Comparison of the CUDA path against the oracle (shared by the GPU tests and smoke)."""
+"""Comparison of the CUDA path against the oracle (shared by the GPU tests and smoke).
+
+The tolerances, the routing-flip rule and the teacher-forced stack chain live in
+``oracle.compare`` (test infrastructure), which the bench's parity report uses too."""
 from __future__ import annotations
 
 import numpy as np
 
 from oracle import moe
-
-GAP = 1e-3        # routing flips allowed only where the oracle's logits are this close
-REL_L2 = 1e-2     # relative L2 error of y over the whole output tensor
-MAX_ABS = 3e-2    # max |y_gpu - y_oracle| <= MAX_ABS * rms(y_oracle)
-
-
-def routing_flips(gpu_idx: np.ndarray, logits: np.ndarray, k: int):
-    """Tokens whose GPU expert list (in rank order) differs from the oracle's.
-
-    Returns (flipped token indices, bad token indices): a flip is legal only if
-    every disagreement is between experts whose oracle logits differ by < GAP
-    (an expert kept in place of another, or two experts ranked the other way).
-    """
-    flipped, bad = [], []
-    for t in range(gpu_idx.shape[0]):
-        l = logits[t]
-        order = np.lexsort((np.arange(l.size), -l))
-        ref = order[:k]
-        g = gpu_idx[t]
-        if np.array_equal(g, ref):
-            continue
-        flipped.append(t)
-        ok = len(set(g.tolist())) == k
-        extra = set(g.tolist()) - set(ref.tolist())
-        missing = set(ref.tolist()) - set(g.tolist())
-        for e in extra:
-            for f in missing:
-                ok &= (l[f] - l[e]) < GAP
-        for i in range(k):
-            for j in range(i + 1, k):
-                if l[g[i]] < l[g[j]] or (l[g[i]] == l[g[j]] and g[i] > g[j]):
-                    ok &= (l[g[j]] - l[g[i]]) < GAP
-        if not ok:
-            bad.append(t)
-    return flipped, bad
-
-
-def error_metrics(y_gpu_bits: np.ndarray, y_ref: np.ndarray):
-    yg = moe.bf16_to_f64(y_gpu_bits)
-    d = yg - y_ref
-    rel = float(np.linalg.norm(d) / max(np.linalg.norm(y_ref), 1e-300))
-    rms = float(np.sqrt(np.mean(y_ref ** 2)))
-    mx = float(np.abs(d).max() / max(rms, 1e-300))
-    return rel, mx
+from oracle.compare import (GAP, MAX_ABS, REL_L2, error_metrics, layer_check_metrics,  # noqa: F401
+                            routing_flips, stack_chain, stack_rel_l2)
 
 
 def check_layer(dev, lay, x_bits: np.ndarray, y_gpu_bits: np.ndarray, routing: dict,
@@ -74,3 +35,4 @@ def check_layer(dev, lay, x_bits: np.ndarray, y_gpu_bits: np.ndarray, routing: d
     assert rel <= REL_L2, f"rel L2 {rel:.3e}"
     assert mx <= MAX_ABS, f"max abs / rms {mx:.3e}"
     return dict(rel_l2=rel, max_abs_over_rms=mx, flips=len(flipped), tokens=len(sel))
+

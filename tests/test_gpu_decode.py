@@ -244,33 +244,37 @@ def test_layer_120b_t4(dev):
 
 
 def test_stack_teacher_forced_and_end_to_end(dev):
+    from parity import layer_check_metrics, stack_chain, stack_rel_l2
     n_layers, T = 4, 2
     specs = [small_spec(seed=2, layer=l, zipf=(0.0 if l % 2 == 0 else 1.1)) for l in range(n_layers)]
     inps = [synth.make_layer(s) for s in specs]
     devs = [dev.DeviceLayer(i, max_tokens=16) for i in inps]
     lays = [oracle_layer(i) for i in inps]
     x_bits = synth.tokens_bf16(2, T, specs[0].hidden)
-    H = specs[0].hidden
+    H, K = specs[0].hidden, specs[0].top_k
     tx = torch.empty((n_layers, T, H), dtype=torch.bfloat16, device="cuda")
     ty = torch.empty_like(tx)
+    ti = torch.empty((n_layers, T, K), dtype=torch.int32, device="cuda")
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    ext.edge0_moe_stack_forward_trace([d.handle for d in devs], dev_bf16(x_bits), y, T, 1e-6, tx, ty)
+    ext.edge0_moe_stack_forward_trace([d.handle for d in devs], dev_bf16(x_bits), y, T, 1e-6, tx, ty, ti)
     torch.cuda.synchronize()
-    txb, tyb = bits(tx), bits(ty)
+    txb, tyb, tib = bits(tx), bits(ty), ti.cpu().numpy()
     assert np.array_equal(txb[0], x_bits)
     for l in range(n_layers):
-        # each layer checked on the GPU's own input to it
-        ref = moe.layer_forward(lays[l], txb[l])["y"]
-        rel, mx = error_metrics(tyb[l], ref)
-        assert rel < 1e-2 and mx < 3e-2, (l, rel, mx)
+        # each layer checked on the GPU's own input to it and on its own routing
+        rel, mx, _, bad = layer_check_metrics(lays[l], txb[l], tyb[l], tib[l])
+        assert not bad and rel <= 1e-2 and mx <= 3e-2, (l, rel, mx, bad)
         if l + 1 < n_layers:
             nxt = moe.residual_rmsnorm(txb[l], tyb[l])
             assert np.mean(nxt == txb[l + 1]) > 0.99
-    # end to end through the oracle stack
-    xf, _ = moe.stack_forward(lays, x_bits)
+    # the last layer's routing is also published through edge0_moe_debug_routing
+    assert np.array_equal(devs[0].routing(T)["idx"], tib[-1])
+    # end to end through the oracle stack forced to the GPU's routing
+    xf, _, bad = stack_chain(lays, x_bits, tib)
+    assert not bad
     got = moe.bf16_to_f64(bits(y))
     ref = moe.bf16_to_f64(xf)
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 2e-2
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= stack_rel_l2(n_layers)
     # the same stack through per-layer calls gives the same bits
     cur = dev_bf16(x_bits)
     for d in devs:

@@ -152,19 +152,33 @@ def test_prefill_invalid_arguments(small):
 
 
 def test_prefill_stack_chain(dev):
-    """T > 16 stacks chain layer calls and the residual norm; compare with the oracle stack."""
+    """T > 16 stacks chain layer calls and the residual norm; compare with the oracle
+    stack forced to each layer's GPU routing (per-layer calls reproduce the stack bits)."""
+    from parity import stack_chain, stack_rel_l2
     n_layers, T = 3, 48
     specs = [small_spec(seed=5, layer=l, zipf=(0.0 if l % 2 == 0 else 1.1)) for l in range(n_layers)]
     inps = [synth.make_layer(s) for s in specs]
     devs = [dev.DeviceLayer(i, max_tokens=T) for i in inps]
     lays = [oracle_layer(i) for i in inps]
-    x_bits = synth.tokens_bf16(6, T, specs[0].hidden)
-    y = torch.empty((T, specs[0].hidden), dtype=torch.bfloat16, device="cuda")
+    H = specs[0].hidden
+    x_bits = synth.tokens_bf16(6, T, H)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     ext.edge0_moe_stack_forward([d.handle for d in devs], dev_bf16(x_bits), y, T, 1e-6)
     torch.cuda.synchronize()
-    xf, _ = moe.stack_forward(lays, x_bits)
+    cur, idx_layers = dev_bf16(x_bits), []
+    for d in devs:
+        yl = d.forward(cur)
+        torch.cuda.synchronize()
+        idx_layers.append(d.routing(T)["idx"])
+        nx = torch.empty_like(cur)
+        ext.edge0_residual_rmsnorm(cur, yl, nx, T, H, 1e-6)
+        cur = nx
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(cur), bits(y))
+    xf, _, bad = stack_chain(lays, x_bits, idx_layers)
+    assert not bad
     got, ref = moe.bf16_to_f64(bits(y)), moe.bf16_to_f64(xf)
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 2e-2
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= stack_rel_l2(n_layers)
     for d in devs:
         d.close()
 

@@ -86,6 +86,52 @@ def test_teacher_forcing_with_own_indices_is_identity():
     assert np.array_equal(out["y"], again["y"])
 
 
+def test_teacher_forcing_with_other_indices_matches_brute_force():
+    """idx_override with experts the oracle would not pick: y and w must follow the
+    given indices, with weights renormalised from the fp64 logits over exactly those
+    experts (per-token torch/scipy composition).  An override that was ignored, or
+    weights taken from the oracle's own top-k, fails here."""
+    import scipy.special
+    spec = tiny_spec(seed=31, n_experts=16, top_k=3, zipf=0.7)
+    inp = synth.make_layer(spec)
+    lay = oracle_layer(inp)
+    T = 5
+    x = synth.tokens_bf16(12, T, spec.hidden)
+    own = moe.layer_forward(lay, x, want=("idx", "logits"))
+    # J: ranks 3..5 of each token's ordering (never the oracle's choice), in a
+    # rotated order so that the rank order of J differs from the logits' order too
+    J = np.empty((T, 3), dtype=np.int32)
+    for t in range(T):
+        order = np.lexsort((np.arange(16), -own["logits"][t]))
+        J[t] = np.roll(order[3:6], t)
+        assert not set(J[t]) & set(own["idx"][t])
+    out = moe.layer_forward(lay, x, idx_override=J, want=("idx", "w"))
+    assert np.array_equal(out["idx"], J)
+    L, F = spec.latent, spec.ffn
+
+    def mats(src):
+        c, s, g = src
+        return (_t(nvfp4.dequantize(c[:F * L // 2].reshape(F, -1), s[:F * L // 16].reshape(F, -1), g[0])),
+                _t(nvfp4.dequantize(c[F * L // 2:F * L].reshape(F, -1), s[F * L // 16:F * L // 8].reshape(F, -1), g[1])),
+                _t(nvfp4.dequantize(c[F * L:].reshape(L, -1), s[F * L // 8:].reshape(L, -1), g[2])))
+
+    D, U, R = (_t(moe.bf16_to_f64(a)) for a in (inp.D, inp.U, inp.R))
+    for t in range(T):
+        zt = D @ _t(moe.bf16_to_f64(x[t]))
+        lt = (R @ zt).numpy() + inp.bias.astype(np.float64)
+        p = scipy.special.softmax(lt)[J[t]]
+        wt = p / p.sum()
+        assert np.allclose(out["w"][t], wt, rtol=1e-12, atol=0)
+        Wg, Wu, Wd = mats(inp.shared())
+        ct = Wd @ (torch.nn.functional.silu(Wg @ zt) * (Wu @ zt))
+        for j, e in enumerate(J[t]):
+            Wg, Wu, Wd = mats(inp.expert(int(e)))
+            ct = ct + wt[j] * (Wd @ (torch.nn.functional.silu(Wg @ zt) * (Wu @ zt)))
+        assert np.allclose(out["y"][t], (U @ ct).numpy(), rtol=1e-10, atol=1e-12)
+    # and the override changes the answer: the oracle's own routing gives another y
+    assert not np.allclose(out["y"], own["y"], rtol=1e-3, atol=1e-6)
+
+
 def test_combine_is_linear_in_routed_outputs():
     """Halving every routed expert's down global halves the routed part of c."""
     spec = tiny_spec(seed=11)

@@ -11,8 +11,9 @@ import torch
 
 import synth
 import latent_sparse_moe_router_b300 as ext
+from conftest import oracle_layer
 from oracle import moe
-from parity import MAX_ABS, REL_L2
+from parity import MAX_ABS, REL_L2, error_metrics
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +54,56 @@ def test_noalloc_matches_handle_forward_twice(shape):
     for _ in range(2):                 # the static scratch keeps the last call's contents
         _close(_noalloc(dl, x, T), ref)
     dl.close()
+
+
+@pytest.mark.parametrize("shape", ["small", "145b"])
+def test_noalloc_scales_large_inputs_like_the_handle_path(shape):
+    """Inputs 2^13 times larger than the workloads': |z| reaches ~3e4, so the f16
+    products of the expert dot products (|e2m1| <= 6) would overflow without the
+    per-token power-of-two scaling of z.  The call computes that scaling's bound on
+    the device, so its output matches the oracle, twice in a row."""
+    from synth import device
+    if shape == "small":
+        spec = synth.LayerSpec(seed=6, layer=0, latent=256, hidden=512, n_experts=64, top_k=4, ffn=128)
+        T = 3
+    else:
+        spec = synth.LayerSpec(seed=0, layer=0, latent=1792)
+        T = 1
+    inp = synth.make_layer(spec)
+    dl = device.DeviceLayer(inp, max_tokens=16)
+    x_bits = synth.tokens_bf16(23, T, spec.hidden)
+    big = synth.f32_to_bf16_bits(moe.bf16_to_f64(x_bits).astype(np.float32) * np.float32(8192.0))
+    z = moe.d_projection(moe.bf16_to_f64(big), moe.bf16_to_f64(inp.D))
+    assert 6.0 * np.abs(z).max() > 65504.0          # an unscaled f16 product would overflow
+    ref = moe.layer_forward(oracle_layer(inp), big)["y"]
+    x = device.bf16_tensor(big)
+    for _ in range(2):
+        y = _noalloc(dl, x, T)
+        rel, mx = error_metrics(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+        assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+    _close(_noalloc(dl, x, T), dl.forward(x))
+    dl.close()
+
+
+def test_noalloc_rejects_a_plan_that_does_not_fit_shared_memory():
+    """hidden 3072, latent 2048, ffn 1024 at T=16 are inside the scratch limits, but the
+    decode kernel's shared-memory plan leaves no room for a staged row: the call must
+    return UNSUPPORTED before launching anything (the buffers are never read)."""
+    H, L, E, K, F, T = 3072, 2048, 512, 10, 1024, 16
+    stride = ext.edge0_expert_record_stride(L, F)
+    D = torch.zeros((L, H), dtype=torch.bfloat16, device="cuda")
+    U = torch.zeros((H, L), dtype=torch.bfloat16, device="cuda")
+    R = torch.zeros((E, L), dtype=torch.bfloat16, device="cuda")
+    rec = torch.zeros(E * stride, dtype=torch.uint8, device="cuda")
+    sh = torch.zeros(stride, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ext.Edge0Error) as ei:
+        ext.edge0_moe_forward_noalloc(H, L, E, K, F, D, U, R, None, rec, stride, sh, x, y, T, status)
+    assert ei.value.status == ext.EDGE0_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert int(status.item()) == -1                  # nothing was enqueued
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():

@@ -284,6 +284,26 @@ edge0_status edge0_moe_profile_stages(void *handle, int enable);
 edge0_status edge0_moe_stage_times(void *handle, float *ms, int max, int *n_out);
 
 /*
+ * Phase timing of the decode kernel, for profiling.  While enabled (the first
+ * enable allocates a small stamp buffer on the handle), each decode forward or
+ * stack call on the handle zeroes that buffer on its stream before the launch
+ * and the kernel records %globaltimer stamps at its phase boundaries.
+ * edge0_moe_decode_phase_times synchronises the device and writes, for each layer
+ * of the last profiled launch, EDGE0_DECODE_PHASES microsecond values to host us[]:
+ *   0 P0 (z and logits) on CTA 0's clock to the last CTA's end, 1 spread of the
+ *   CTAs' P0 ends, 2 grid barrier 1, 3 routing (top-k, weights, permutation) on
+ *   CTA 0, 4 rest of P1 (gate/up) to the last CTA's end, 5 spread of P1 ends,
+ *   6 barrier 2, 7 P2 (down + combine), 8 spread, 9 barrier 3, 10 P3 (U), 11
+ *   spread, 12 barrier 4 (stacks; 0 otherwise), 13 the layer's total.
+ * n = min(max, layers * EDGE0_DECODE_PHASES); *n_out = n.  UNSUPPORTED if no
+ * profiled decode launch ran.  Profiling adds one memset per launch and a few
+ * stores per CTA and phase.
+ */
+#define EDGE0_DECODE_PHASES 14
+edge0_status edge0_moe_profile_decode(void *handle, int enable);
+edge0_status edge0_moe_decode_phase_times(void *handle, float *us, int max, int *n_out);
+
+/*
  * Failure-path check: launch one block on `stream` that waits on an mbarrier
  * no one arrives at, through the same bounded wait every kernel of the library
  * uses (limit 1 s of %globaltimer).  The wait runs out, sets the handle's

@@ -28,6 +28,7 @@ EXPORTED = (
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
     "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc", "edge0_gemm_bf16_tn",
     "edge0_moe_profile_stages", "edge0_moe_stage_times", "edge0_moe_debug_wait_probe",
+    "edge0_moe_profile_decode", "edge0_moe_decode_phase_times",
 )
 
 EDGE0_PREFILL_STAGES = 10
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_profile_stages": (i, [vp, i]),
             "edge0_moe_debug_wait_probe": (i, [vp, vp]),
             "edge0_moe_stage_times": (i, [vp, vp, i, vp]),
+            "edge0_moe_profile_decode": (i, [vp, i]),
+            "edge0_moe_decode_phase_times": (i, [vp, vp, i, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -240,6 +243,28 @@ def edge0_moe_stage_times(handle):
     _check(lib().edge0_moe_stage_times(handle, ctypes.cast(buf, ctypes.c_void_p), EDGE0_PREFILL_STAGES,
                                        ctypes.byref(n)), "edge0_moe_stage_times")
     return [float(buf[i]) for i in range(n.value)]
+
+
+EDGE0_DECODE_PHASES = 14
+DECODE_PHASE_NAMES = ("p0", "p0_spread", "barrier1", "routing", "p1_gate_up", "p1_spread", "barrier2",
+                      "p2_down_combine", "p2_spread", "barrier3", "p3_u", "p3_spread", "barrier4", "layer_total")
+
+
+def edge0_moe_profile_decode(handle, enable: bool):
+    _check(lib().edge0_moe_profile_decode(handle, int(bool(enable))), "edge0_moe_profile_decode")
+
+
+def edge0_moe_decode_phase_times(handle, n_layers: int = 1):
+    """Per-layer phase microseconds of the last profiled decode launch: a list of
+    dicts keyed by DECODE_PHASE_NAMES."""
+    n_max = EDGE0_DECODE_PHASES * n_layers
+    buf = (ctypes.c_float * n_max)()
+    n = ctypes.c_int()
+    _check(lib().edge0_moe_decode_phase_times(handle, ctypes.cast(buf, ctypes.c_void_p), n_max, ctypes.byref(n)),
+           "edge0_moe_decode_phase_times")
+    vals = [float(buf[i]) for i in range(n.value)]
+    return [dict(zip(DECODE_PHASE_NAMES, vals[l * EDGE0_DECODE_PHASES:(l + 1) * EDGE0_DECODE_PHASES]))
+            for l in range(n.value // EDGE0_DECODE_PHASES)]
 
 
 def edge0_moe_get_error(handle) -> int:

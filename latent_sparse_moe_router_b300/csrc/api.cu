@@ -48,6 +48,10 @@ struct Handle {
   std::vector<LayerW> stack_tab;  // the layer table last uploaded to d_stack
   int last_T = 0;
   int last_path = 0;          // 0 none, 1 decode, 2 prefill
+  // decode phase profiling (off by default)
+  bool dec_profile = false;
+  unsigned long long* stamps = nullptr;   // [kStackMax][kStampSlots], own allocation
+  int stamped_layers = 0;                 // layers of the last profiled decode launch
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -303,6 +307,14 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const __nv_bfloat
 
 edge0_status launch_status() { return cuda_status(cudaGetLastError()); }
 
+// A profiled decode launch carries the handle's zeroed stamp buffer.
+cudaError_t attach_stamps(Handle* hd, DecodeArgs& a, int n_layers, cudaStream_t s) {
+  if (!hd->dec_profile) return cudaSuccess;
+  a.stamps = hd->stamps;
+  hd->stamped_layers = n_layers;
+  return cudaMemsetAsync(hd->stamps, 0, sizeof(unsigned long long) * kStampSlots * n_layers, s);
+}
+
 // One mbarrier that nothing arrives at, waited on with the library's bounded wait.
 __global__ void wait_probe_kernel(int* err) {
   __shared__ uint64_t bar;
@@ -485,6 +497,7 @@ edge0_status edge0_moe_forward(void* handle, const void* x, void* y, int T, edge
   if (T <= kDecodeMaxT) {
     DecodeArgs a;
     fill_decode_args(hd, a, x, y, T);
+    if (attach_stamps(hd, a, 1, (cudaStream_t)stream) != cudaSuccess) return EDGE0_ERR_CUDA;
     const cudaError_t e = decode_launch(a, hd->num_sms, hd->smem_total, (cudaStream_t)stream);
     if (e != cudaSuccess) return EDGE0_ERR_CUDA;
     hd->last_T = T;
@@ -611,6 +624,7 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
   a.trace_x = static_cast<__nv_bfloat16*>(trace_x);
   a.trace_y = static_cast<__nv_bfloat16*>(trace_y);
   a.trace_idx = trace_idx;
+  if (attach_stamps(h0, a, n_layers, s) != cudaSuccess) return EDGE0_ERR_CUDA;
   e = decode_launch(a, h0->num_sms, h0->smem_total, s);
   if (e != cudaSuccess) return EDGE0_ERR_CUDA;
   h0->last_T = T;
@@ -649,6 +663,47 @@ edge0_status edge0_moe_stage_times(void* handle, float* ms, int max, int* n_out)
   return prefill_stage_times(&hd->pf, ms, max, n_out);
 }
 
+edge0_status edge0_moe_profile_decode(void* handle, int enable) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  if (enable && !hd->stamps) {
+    if (cudaMalloc(&hd->stamps, sizeof(unsigned long long) * kStampSlots * kStackMax) != cudaSuccess) {
+      cudaGetLastError();
+      return EDGE0_ERR_OOM;
+    }
+  }
+  hd->dec_profile = enable != 0;
+  hd->stamped_layers = 0;
+  return EDGE0_OK;
+}
+
+edge0_status edge0_moe_decode_phase_times(void* handle, float* us, int max, int* n_out) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !us || max < 0) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->stamps || hd->stamped_layers < 1) return EDGE0_ERR_UNSUPPORTED;
+  unsigned long long st[kStampSlots * kStackMax];
+  const int nl = hd->stamped_layers;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(st, hd->stamps, sizeof(unsigned long long) * kStampSlots * nl, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  int n = 0;
+  for (int l = 0; l < nl; ++l) {
+    const unsigned long long* t = st + l * kStampSlots;
+    auto d = [](unsigned long long a, unsigned long long b) { return b >= a ? float(b - a) * 1e-3f : 0.f; };
+    const unsigned long long e0 = ~t[kStP0EndMin], e1 = ~t[kStP1EndMin], e2 = ~t[kStP2EndMin], e3 = ~t[kStP3EndMin];
+    const float v[EDGE0_DECODE_PHASES] = {
+        d(t[kStP0Start], t[kStP0EndMax]), d(e0, t[kStP0EndMax]), d(t[kStP0EndMax], t[kStBar1]),
+        d(t[kStBar1], t[kStRouted]), d(t[kStRouted], t[kStP1EndMax]), d(e1, t[kStP1EndMax]),
+        d(t[kStP1EndMax], t[kStBar2]), d(t[kStBar2], t[kStP2EndMax]), d(e2, t[kStP2EndMax]),
+        d(t[kStP2EndMax], t[kStBar3]), d(t[kStBar3], t[kStP3EndMax]), d(e3, t[kStP3EndMax]),
+        t[kStBar4] ? d(t[kStP3EndMax], t[kStBar4]) : 0.f,
+        d(t[kStP0Start], t[kStBar4] ? t[kStBar4] : t[kStP3EndMax])};
+    for (int i = 0; i < EDGE0_DECODE_PHASES && n < max; ++i) us[n++] = v[i];
+  }
+  if (n_out) *n_out = n;
+  return EDGE0_OK;
+}
+
 edge0_status edge0_moe_get_error(void* handle) {
   Handle* hd = static_cast<Handle*>(handle);
   if (!hd) return EDGE0_ERR_INVALID_ARG;
@@ -682,6 +737,7 @@ void edge0_moe_destroy(void* handle) {
   if (!hd) return;
   cudaDeviceSynchronize();
   prefill_destroy(&hd->pf);
+  if (hd->stamps) cudaFree(hd->stamps);
   cudaFree(hd->ws);
   delete hd;
 }

@@ -427,9 +427,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   }
   __syncthreads();
 
+  // profiling stamps (no-ops unless the launch carries a stamp buffer)
+  auto stamp0 = [&](int li, int slot) {
+    if (a.stamps && bid == 0 && tid == 0) a.stamps[li * kStampSlots + slot] = globaltimer_ns();
+  };
+  auto stamp_end = [&](int li, int slot) {   // slot: the max slot; slot + 1 the min slot
+    if (a.stamps) {                          // uniform: the whole CTA is done with the phase
+      __syncthreads();
+      if (tid == 0) {
+        const unsigned long long t = globaltimer_ns();
+        atomicMax(&a.stamps[li * kStampSlots + slot], t);
+        atomicMax(&a.stamps[li * kStampSlots + slot + 1], ~t);
+      }
+    }
+  };
   LayerW lw = a.l0;
   for (int li = 0; li < a.n_layers; ++li) {
     const bool last = (li == a.n_layers - 1);
+    stamp0(li, kStP0Start);
     __nv_bfloat16* xcur = a.xbuf + size_t(li & 1) * T * H;
     // ================================================================ P0: z = D x, l = (R D) x + b
     {
@@ -509,7 +524,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       });
       if (tid == 32) tb->gsc[0] = make_float4(sh_gu.x, sh_gu.y, sh_d, 0.f);
     }
+    stamp_end(li, kStP0EndMax);
     if (!grid_sync(a.bar, a.err)) return;
+    stamp0(li, kStBar1);
     // ================================================================ P1: routing, gate/up -> h
     {
       if (tid == 0) tb->task_ctr = 0;
@@ -595,6 +612,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         if (lane == 0) { tb->nu = base; tb->goff[base] = TK; }
       }
       __syncthreads();
+      stamp0(li, kStRouted);
       const int nu = tb->nu;
       // routed gate/up rows: q in [q0, q1) of nu * F (group-major)
       const long nq = long(nu) * F;
@@ -777,7 +795,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         l2_prefetch_share(nx.RD, size_t(E) * H * 4, bid, G);
       }
     }
+    stamp_end(li, kStP1EndMax);
     if (!grid_sync(a.bar, a.err)) return;
+    stamp0(li, kStBar2);
     // ================================================================ P2: down + combine -> c
     LayerW nxt = lw;
     if (li + 1 < a.n_layers) nxt = a.layers[li + 1];
@@ -824,46 +844,57 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       const int ob_bytes = (nslot * nr * 4 + 127) & ~127;
       const int hrow = F * 2;
       wait_mb(cx, kMbScale);
-      int j0g = 0;
-      while (nr > 0 && j0g < ngr) {
-        // groups [j0g, j1g) this round: h rows (and, without staging, down rows) must fit
-        int j1g = j0g, nslots_r = 0, wbytes = 0;
-        while (j1g < ngr) {
-          const int ns = (j1g == 0) ? T : (tb->goff[j1g] - tb->goff[j1g - 1]);
+      // Slots in one order q: q < T the shared expert's slot of token q (slot TK + q),
+      // q >= T grouped position q - T (slot perm[q - T]).  Group j covers
+      // [qlo(j), qhi(j)): j = 0 the shared expert, j >= 1 routed expert gexp[j - 1].
+      // A round takes slots [qa, qb); its first and last group may be partial, so a
+      // group whose h rows exceed the region is split over rounds.
+      auto qlo = [&](int j) { return j == 0 ? 0 : T + tb->goff[j - 1]; };
+      auto qhi = [&](int j) { return j == 0 ? T : T + tb->goff[j]; };
+      int qa = 0, ja = 0;
+      while (nr > 0 && qa < nslot) {
+        while (qhi(ja) <= qa) ++ja;                 // the group holding slot qa
+        int qb = qa, ng = 0;
+        {
           const int wb = down_staged ? 0 : down_grp;
-          if (ob_bytes + (nslots_r + ns) * hrow + wbytes + wb > region_bytes || (j1g - j0g) >= 512) break;
-          nslots_r += ns; wbytes += wb; ++j1g;
+          int bytes = ob_bytes;
+          for (int j = ja; j < ngr && ng < 512 && ng < (down_staged ? 512 : kMbRounds * 64); ++j) {
+            const int want = qhi(j) - qb;
+            const int room = (region_bytes - bytes - wb) / hrow;
+            if (room <= 0) break;
+            const int take = min(want, room);
+            bytes += wb + take * hrow;
+            qb += take;
+            ++ng;
+            if (take < want) break;
+          }
         }
-        const int ng = j1g - j0g;
-        if (ng == 0) {  // cannot happen for validated shapes; stop instead of spinning
+        if (ng == 0) {  // the region holds less than one h row and one down block: stop, do not spin
           if (tid == 0) atomicOr(a.err, kErrTimeout);
           break;
         }
+        const int nq = qb - qa;
         const int nb = down_staged ? 0 : min(kMbRounds, ng);
-        uint8_t* wbase = down_staged ? dyn + tb->down_off : region + ob_bytes + nslots_r * hrow;
+        uint8_t* wbase = down_staged ? dyn + tb->down_off : region + ob_bytes + nq * hrow;
         if (tid == 0 && !down_staged) {
           for (int b = 0; b < nb; ++b) {
-            const int ga = j0g + ng * b / nb, gb = j0g + ng * (b + 1) / nb;
+            const int ga = ng * b / nb, gb = ng * (b + 1) / nb;
             mbar_arrive_expect_tx(&tb->mbar[kMbRound + b], uint32_t(gb - ga) * down_grp);
-            for (int j = ga; j < gb; ++j) {
+            for (int jj = ga; jj < gb; ++jj) {
+              const int j = ja + jj;
               const uint8_t* rec = (j == 0) ? lw.shared : lw.experts + size_t(tb->gexp[j - 1]) * lw.stride;
-              bulk_g2s(wbase + size_t(j - j0g) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
+              bulk_g2s(wbase + size_t(jj) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
                        uint32_t(down_grp), &tb->mbar[kMbRound + b]);
-              tb->task_aux[j - j0g] = b;
+              tb->task_aux[jj] = b;
             }
           }
         }
-        // h rows of the round's slots, scaled to f16: shared slots first, then routed by position
+        // h rows of the round's slots, scaled to f16 (row i = slot q = qa + i)
         __half* hs = reinterpret_cast<__half*>(region + ob_bytes);
-        const int sh = (j0g == 0) ? T : 0;
-        const int p0 = (j0g == 0) ? 0 : tb->goff[j0g - 1];
-        if (tid < ng) {
-          const int j = j0g + tid;
-          tb->task_row[tid] = (j == 0) ? 0 : sh + (tb->goff[j - 1] - p0);
-        }
-        for (int i = warp; i < nslots_r; i += kDecWarps) {
+        for (int i = warp; i < nq; i += kDecWarps) {
           // one warp per slot: the row in registers (one round trip), max |h|, scaled f16 copy
-          const int slot = (i < sh) ? TK + i : tb->perm[p0 + (i - sh)];
+          const int q = qa + i;
+          const int slot = (q < T) ? TK + q : tb->perm[q - T];
           const float4* src = reinterpret_cast<const float4*>(a.h + size_t(slot) * F);
           __half2* dst = reinterpret_cast<__half2*>(hs + size_t(i) * F);
           for (int k0 = 0; k0 < F / 4; k0 += 32 * 8) {
@@ -919,8 +950,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           const int task = tbase + (lane >> 3);
           const bool valid = task < ng * nr;
           const int jj = valid ? task / nr : 0, r = valid ? task % nr : 0;
-          const int j = j0g + jj;
-          const int ns = !valid ? 0 : (j == 0) ? T : (tb->goff[j] - tb->goff[j - 1]);
+          const int j = ja + jj;
+          const int qs = max(qa, qlo(j));                       // the group's slots in this round
+          const int ns = !valid ? 0 : min(qb, qhi(j)) - qs;
           if (valid) {
             if (down_staged) wait_mb(cx, kMbDown + j / per_b);
             else wait_mb(cx, kMbRound + tb->task_aux[jj]);
@@ -931,7 +963,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           const uint8_t* scl = pr + F + (r & 1) * (F / 16);
           const __half* arow[TB];
 #pragma unroll
-          for (int i = 0; i < TB; ++i) arow[i] = hs + size_t(tb->task_row[jj] + (i < ns ? i : 0)) * F;
+          for (int i = 0; i < TB; ++i) arow[i] = hs + size_t(qs - qa + (i < ns ? i : 0)) * F;
           float acc[TB];
 #pragma unroll
           for (int i = 0; i < TB; ++i) acc[i] = 0.f;
@@ -942,7 +974,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
 #pragma unroll
             for (int i = 0; i < TB; ++i) {
               if (i < ns) {
-                const int slot = (j == 0) ? TK + i : tb->perm[tb->goff[j - 1] + i];
+                const int q = qs + i;
+                const int slot = (q < T) ? TK + q : tb->perm[q - T];
                 ob[size_t(slot) * nr + r] = gd * tb->hinv[slot] * acc[i];
               }
             }
@@ -953,7 +986,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
         __syncthreads();
         if (!down_staged) release_mb(cx, (1u << nb) - 1u);
-        j0g = j1g;
+        qa = qb;
       }
       if (!u_issued) issue_u();
       if (down_staged) {
@@ -970,7 +1003,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       release_mb(cx, 1u << kMbScale);
     }
+    stamp_end(li, kStP2EndMax);
     if (!grid_sync(a.bar, a.err)) return;
+    stamp0(li, kStBar3);
     // ================================================================ P3: y = U c
     {
       for (int i = tid; i < T * L / 4; i += kDecThreads)
@@ -1009,8 +1044,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
                              [&](int, int t, int j, float v) { emit(t, j, v); });
       }
     }
+    stamp_end(li, kStP3EndMax);
     if (!last || a.final_norm) {
       if (!grid_sync(a.bar, a.err)) return;
+      stamp0(li, kStBar4);
     }
     if (last && a.final_norm) {
       // stack output: RMSNorm(x_last + y_last); every CTA normalises, each writes its slice

@@ -42,6 +42,19 @@ constexpr int kMbScale = 14;     // fp32 scales of the selected records (P1 -> P
 constexpr int kScaleWarp0 = 8;   // warps 8..15 load them, one record per lane
 constexpr int kScaleWarps = 8;
 
+// Phase stamps of a profiled launch, per layer (ns of %globaltimer): CTA 0's time at
+// each point, and the latest (max) / earliest (stored as ~t, max) phase end over all
+// CTAs before each grid barrier.
+enum DecStamp {
+  kStP0Start = 0,    // CTA 0, start of P0 (after the kernel's set-up)
+  kStP0EndMax, kStP0EndMin, kStBar1,        // P0 end over CTAs; CTA 0 after barrier 1
+  kStRouted,                                // CTA 0, routing done (before the expert copies)
+  kStP1EndMax, kStP1EndMin, kStBar2,
+  kStP2EndMax, kStP2EndMin, kStBar3,
+  kStP3EndMax, kStP3EndMin, kStBar4,        // barrier 4: stacks only
+  kStampSlots = 16
+};
+
 // One layer's weights as the decode kernel sees them.
 struct LayerW {
   const __nv_bfloat16* D;   // [L][H]
@@ -77,6 +90,7 @@ struct DecodeArgs {
   __nv_bfloat16* trace_y;   // optional [n_layers][T][H]: output of every layer
   int* trace_idx;           // optional [n_layers][T][K]: experts each layer picked, in rank order
   const float* dnorm_dev;   // optional: device copy of the first layer's dnorm (used in place of l0.dnorm)
+  unsigned long long* stamps; // optional [n_layers][kStampSlots] %globaltimer phase stamps (zeroed before launch)
   GridBarrier* bar;
   int* err;
   // shared-memory plan (bytes from the 128-aligned dynamic base)

@@ -41,11 +41,28 @@ def layer_task(args):
 
 
 def chain_task(args):
-    """One token (or a few) through the whole oracle stack, routing forced to the GPU's."""
+    """One token (or a few) through the whole oracle stack, routing forced to the GPU's.
+
+    With ``perturb`` the chain also runs from an input whose bf16 values are moved by
+    one unit in the last place in a seeded tenth of the elements, and returns the
+    relative size of that input change and of the resulting output change: the
+    chain's own amplification of a rounding-level perturbation."""
+    from oracle import moe
     from parity import stack_chain
-    seed, n_layers, latent, zipfs, x_bits, idx_per_layer = args
+    seed, n_layers, latent, zipfs, x_bits, idx_per_layer, perturb = args
     lays = [_oracle_layer(seed, l, latent, zipfs[l % len(zipfs)]) for l in range(n_layers)]
-    return stack_chain(lays, x_bits, idx_per_layer)
+    xf, flips, bad = stack_chain(lays, x_bits, idx_per_layer)
+    if not perturb:
+        return xf, flips, bad, None
+    xp = np.array(x_bits, dtype=np.uint16)
+    sel = np.random.default_rng(seed + 99).random(xp.shape) < 0.1
+    xp[sel] ^= np.uint16(1)                       # one ulp of bf16 in those elements
+    x0, x1 = moe.bf16_to_f64(x_bits), moe.bf16_to_f64(xp)
+    d_in = float(np.linalg.norm(x1 - x0) / np.linalg.norm(x0))
+    xpf, _, _ = stack_chain(lays, xp, idx_per_layer)
+    f0, f1 = moe.bf16_to_f64(xf), moe.bf16_to_f64(xpf)
+    d_out = float(np.linalg.norm(f1 - f0) / np.linalg.norm(f0))
+    return xf, flips, bad, (d_in, d_out)
 
 
 def make_pool():

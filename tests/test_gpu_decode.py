@@ -231,6 +231,22 @@ def test_layer_145b_t1(dev):
     d.close()
 
 
+@pytest.mark.parametrize("T", [11, 16])
+def test_layer_145b_large_buckets(dev, T):
+    """The T = 16 bucket at Edge0-145B shapes: P2 runs in several rounds, with the
+    shared expert's slots split over rounds where its h rows do not fit at once."""
+    spec = synth.LayerSpec(seed=17, layer=0, latent=1792)
+    inp = synth.make_layer(spec)
+    d = dev.DeviceLayer(inp, max_tokens=16)
+    x_bits = synth.tokens_bf16(170 + T, T, spec.hidden)
+    y = d.forward(dev_bf16(x_bits))
+    torch.cuda.synchronize()
+    assert ext.edge0_moe_get_error(d.handle) == ext.EDGE0_OK
+    m = check_layer(d, oracle_layer(inp), x_bits, bits(y), d.routing(T))
+    print(f"layer145b T={T}", m)
+    d.close()
+
+
 def test_layer_120b_t4(dev):
     spec = synth.LayerSpec(seed=1, layer=0, latent=1280)
     inp = synth.make_layer(spec)

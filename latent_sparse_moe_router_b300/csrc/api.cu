@@ -88,7 +88,7 @@ void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
   size_t act = TB * (size_t)(L > E ? L : E) * 4;
   // P0 of a stacked layer: x [T][H] bf16 and the norm's group sums [T][H/8] fp32
   if (TB * (size_t)H * 5 / 2 > act) act = TB * (size_t)H * 5 / 2;
-  const size_t cand = TB * (size_t)((E + 31) / 32) * 16 * 8 * 3 / 2 + 16 * 8;   // top-k lists
+  const size_t cand = TB * (size_t)E * 4 + size_t(kDecWarps) * kTopkCand * 8;   // logits + top-k candidates
   if (cand > act) act = cand;
   a.off_xs = (int)off;
   a.off_act = (int)off;

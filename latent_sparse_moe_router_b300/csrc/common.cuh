@@ -269,6 +269,40 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF)));
 }
 
+// Four E2M1 pairs (one 32-bit word, byte i = elements 2i, 2i+1, low nibble first)
+// -> four f16x2.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
+                                               uint32_t& h3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
+}
+
+// f16x2 (both halves) of an E4M3 scale (exact).
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e4m3) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(e4m3 | (e4m3 << 8))));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// D += A B (m16n8k16, f16 inputs, fp32 accumulate), warp-wide.  Fragments per
+// thread (g = lane / 4, c = lane % 4): a0 (row g, k 2c, 2c+1), a1 (row g + 8, same
+// k), a2 (row g, k 2c + 8, 2c + 9), a3 (row g + 8, same); b0 (k 2c, 2c+1, column g),
+// b1 (k 2c + 8, 2c + 9, column g); d0, d1 (row g, columns 2c, 2c + 1), d2, d3 (row
+// g + 8, same columns).  The lower-indexed element of a pair sits in the low half.
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

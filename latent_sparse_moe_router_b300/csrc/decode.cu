@@ -255,31 +255,178 @@ __device__ __forceinline__ bool cand_first(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// Bitonic sort of one (v, i) per lane across the warp, descending.
-__device__ __forceinline__ void warp_sort_desc(float& v, int& i, int lane) {
+// Top-k of one token's E logits (E a multiple of 32, in shared memory) by one warp,
+// ranked by (value descending, index ascending); a NaN logit ranks as -inf.
+// tau, the K-th largest of the 32 lane maxima (lane l sees logits l, l + 32, ...),
+// is reached by K distinct logits, so every logit of the top K is >= tau: only
+// the candidates >= tau (few for any spread-out row) are ranked, each by counting
+// the candidates that beat it.  More than kTopkCap candidates (ties, -inf rows)
+// take K rounds of a warp-wide selection instead.  Writes idx[0..K) in rank order
+// and w[0..K) = exp(l_k - l_0) / sum_j exp(l_j - l_0).
+constexpr int kTopkCap = kTopkCand;
+
+__device__ __forceinline__ float logit_at(const float* row, int i) {
+  const float v = row[i];
+  return v != v ? -INFINITY : v;
+}
+
+// Any E (a multiple of 32): the logits stay in shared memory.
+__device__ void warp_topk_any(const float* row, int E, int K, Cand* cand, int* idx, float* w) {
+  const int lane = threadIdx.x & 31, nj = E >> 5;
+  float m = -INFINITY;
+  for (int j = 0; j < nj; ++j) m = fmaxf(m, logit_at(row, j * 32 + lane));
+  float s = m;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, v, j);
-      const int oi = __shfl_xor_sync(kFull, i, j);
-      const bool desc = (lane & k) == 0 || k == 32;
-      const bool lower = (lane & j) == 0;
-      const bool o_first = cand_first(ov, oi, v, i);
-      if ((lower == desc) ? o_first : !o_first) { v = ov; i = oi; }
+      const float o = __shfl_xor_sync(kFull, s, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0 || k == 32);
+      s = keep_max ? fmaxf(s, o) : fminf(s, o);
     }
   }
+  const float tau = __shfl_sync(kFull, s, K - 1);
+  int cnt = 0;
+  for (int j = 0; j < nj; ++j) cnt += logit_at(row, j * 32 + lane) >= tau;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(kFull, incl, 31);
+  if (total <= kTopkCap) {
+    int at = incl - cnt;
+    for (int j = 0; j < nj; ++j) {
+      const float v = logit_at(row, j * 32 + lane);
+      if (v >= tau) cand[at++] = Cand{v, j * 32 + lane};
+    }
+    __syncwarp();
+    for (int i = lane; i < total; i += 32) {
+      const Cand c = cand[i];
+      int r = 0;
+      for (int q = 0; q < total; ++q) {
+        const Cand o = cand[q];
+        r += cand_first(o.v, o.i, c.v, c.i);
+      }
+      if (r < K) idx[r] = c.i;
+    }
+  } else {
+    for (int r = 0; r < K; ++r) {
+      // K rounds of a warp-wide selection among the logits not yet chosen
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int j = 0; j < nj; ++j) {
+        const int i = j * 32 + lane;
+        const float v = logit_at(row, i);
+        bool taken = false;
+        for (int q = 0; q < r; ++q) taken |= idx[q] == i;
+        if (!taken && cand_first(v, i, bv, bi)) { bv = v; bi = i; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        if (cand_first(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) idx[r] = bi;
+      __syncwarp();
+    }
+  }
+  __syncwarp();
+  const float vk = lane < K ? logit_at(row, idx[lane]) : 0.f;
+  const float top0 = __shfl_sync(kFull, vk, 0);
+  const float ev = lane < K ? expf(vk - top0) : 0.f;
+  float den = ev;
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+  if (lane < K) w[lane] = ev / den;
 }
 
-// Merge of a bitonic sequence across the warp into descending order.
-__device__ __forceinline__ void warp_merge_desc(float& v, int& i, int lane) {
+// NJ = E / 32 logits per lane, held in registers (one load each, issued together).
+template <int NJ>
+__device__ void warp_topk_reg(const float* row, int K, Cand* cand, int* idx, float* w) {
+  const int lane = threadIdx.x & 31;
+  float v[NJ];
 #pragma unroll
-  for (int j = 16; j > 0; j >>= 1) {
-    const float ov = __shfl_xor_sync(kFull, v, j);
-    const int oi = __shfl_xor_sync(kFull, i, j);
-    const bool lower = (lane & j) == 0;
-    const bool o_first = cand_first(ov, oi, v, i);
-    if (lower ? o_first : !o_first) { v = ov; i = oi; }
+  for (int j = 0; j < NJ; ++j) v[j] = logit_at(row, j * 32 + lane);
+  float m = v[0];
+#pragma unroll
+  for (int j = 1; j < NJ; ++j) m = fmaxf(m, v[j]);
+  // the 32 lane maxima sorted descending across the warp (bitonic network)
+  float s = m;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, s, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0 || k == 32);
+      s = keep_max ? fmaxf(s, o) : fminf(s, o);
+    }
+  }
+  const float tau = __shfl_sync(kFull, s, K - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) cnt += v[j] >= tau;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(kFull, incl, 31);
+  if (total <= kTopkCap) {
+    int at = incl - cnt;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (v[j] >= tau) cand[at++] = Cand{v[j], j * 32 + lane};
+    __syncwarp();
+    for (int i = lane; i < total; i += 32) {
+      const Cand c = cand[i];
+      int r = 0;
+      for (int q = 0; q < total; ++q) {
+        const Cand o = cand[q];
+        r += cand_first(o.v, o.i, c.v, c.i);
+      }
+      if (r < K) idx[r] = c.i;
+    }
+  } else {
+    uint32_t taken = 0;   // bit j: logit j * 32 + lane already chosen
+    for (int r = 0; r < K; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int i = j * 32 + lane;
+        if (!((taken >> j) & 1u) && cand_first(v[j], i, bv, bi)) { bv = v[j]; bi = i; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        if (cand_first(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == 0) idx[r] = bi;
+    }
+  }
+  __syncwarp();
+  const float vk = lane < K ? logit_at(row, idx[lane]) : 0.f;
+  const float top0 = __shfl_sync(kFull, vk, 0);
+  const float ev = lane < K ? expf(vk - top0) : 0.f;
+  float den = ev;
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+  if (lane < K) w[lane] = ev / den;
+}
+
+__device__ void warp_topk(const float* row, int E, int K, Cand* cand, int* idx, float* w) {
+  switch (E >> 5) {
+    case 1: warp_topk_reg<1>(row, K, cand, idx, w); break;
+    case 2: warp_topk_reg<2>(row, K, cand, idx, w); break;
+    case 4: warp_topk_reg<4>(row, K, cand, idx, w); break;
+    case 8: warp_topk_reg<8>(row, K, cand, idx, w); break;
+    case 16: warp_topk_reg<16>(row, K, cand, idx, w); break;
+    case 32: warp_topk_reg<32>(row, K, cand, idx, w); break;
+    default: warp_topk_any(row, E, K, cand, idx, w);
   }
 }
 
@@ -381,6 +528,58 @@ __device__ __forceinline__ void gateup_row(const uint8_t* gc, const uint8_t* gs,
       h_fn(i, silu_f(gv) * uv);
     }
   }
+}
+
+// ------------------------------------------------------------------ NVFP4 x f16 on mma.sync
+// An expert dot product over K runs as m16n8k16 MMAs: A = 16 weight rows (NVFP4
+// decoded in registers, times the E4M3 block scale, exact in f16), B = up to 8
+// activation rows (f16), fp32 accumulators.  A dot product does not depend on the
+// order of its K terms, so K is taken in 32-column chunks with both operands read in
+// one fixed permutation: thread c of a quad holds the fragment columns 2c, 2c + 1,
+// 2c + 8, 2c + 9 of two MMAs, which are mapped to the chunk's physical columns
+// 8c .. 8c + 7 (first MMA 8c .. 8c + 3, second 8c + 4 .. 8c + 7).  The thread then
+// reads one 32-bit code word (8 codes, one 16-block scale) per A row and one 16-byte
+// activation vector per B row, instead of scattered bytes.
+struct MmaRows {
+  const uint8_t* code[2];   // A rows g and g + 8: code bytes of the row (K / 2)
+  const uint8_t* scale[2];  // their E4M3 scales (K / 16)
+};
+
+// acc[t] += A (rows g, g + 8) x B tile t over 32-column chunks [s0, s1).
+template <int NT>
+__device__ __forceinline__ void fp4_mma_chunks(const MmaRows& ar, const __half* const* brow, const bool* bval,
+                                               int s0, int s1, float (*acc)[4]) {
+  const int c = threadIdx.x & 3;
+  const uint8_t* ca = ar.code[0] + 4 * c;
+  const uint8_t* cb = ar.code[1] + 4 * c;
+  const uint8_t* sa = ar.scale[0] + (c >> 1);
+  const uint8_t* sb = ar.scale[1] + (c >> 1);
+#pragma unroll 2
+  for (int s = s0; s < s1; ++s) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(ca + 16 * s);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(cb + 16 * s);
+    const uint32_t ka = scale_f16x2(sa[2 * s]), kb = scale_f16x2(sb[2 * s]);
+    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+    e2m1x8_to_h2x4(wa, a0, a1, a2, a3);
+    e2m1x8_to_h2x4(wb, b0, b1, b2, b3);
+    a0 = hmul2_u32(a0, ka); a1 = hmul2_u32(a1, ka); a2 = hmul2_u32(a2, ka); a3 = hmul2_u32(a3, ka);
+    b0 = hmul2_u32(b0, kb); b1 = hmul2_u32(b1, kb); b2 = hmul2_u32(b2, kb); b3 = hmul2_u32(b3, kb);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (bval[t]) z = *reinterpret_cast<const uint4*>(brow[t] + 32 * s + 8 * c);
+      mma16816(acc[t], a0, b0, a1, b1, z.x, z.y);
+      mma16816(acc[t], a2, b2, a3, b3, z.z, z.w);
+    }
+  }
+}
+
+// Split of a task's chunks over ks warps (at most 16 warp tasks in all, ks <= kmax):
+// the partial accumulators of part p go to part_buf[(task * ks + p) * 32 + lane]
+// and are summed in part order afterwards.
+__device__ __forceinline__ int mma_ksplit(int ntask, int kmax) {
+  int ks = ntask >= 9 ? 1 : ntask >= 5 ? 2 : ntask >= 3 ? 4 : 8;
+  return ks < kmax ? ks : kmax;
 }
 
 }  // namespace
@@ -530,59 +729,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     // ================================================================ P1: routing, gate/up -> h
     {
       if (tid == 0) tb->task_ctr = 0;
-      // zh = f16(z * 2^-e) per token (warp t), and the chunk sorts of the top-k
-      const int nc = (E + 31) / 32;
-      Cand* cx0 = reinterpret_cast<Cand*>(act);                       // [T][nc][16]
-      Cand* cx1 = cx0 + size_t(T) * nc * 16;                          // [T][(nc+1)/2][16]
+      // the experts' f16 input zh, and the logits rows [T][E] into act
       for (int i = tid; i < T * L / 8; i += kDecThreads)
         cp_async16(reinterpret_cast<uint4*>(zh) + i, reinterpret_cast<const uint4*>(a.zh) + i);
       cp_async_commit();
-      for (int task = warp; task < T * nc; task += kDecWarps) {
-        const int t = task / nc, c = task % nc;
-        const int e = c * 32 + lane;
-        float v = e < E ? a.logits[size_t(t) * E + e] : -INFINITY;
-        if (isnan(v)) v = -INFINITY;        // any pick stays a valid expert
-        int ix = e < E ? e : 0x7fffffff;
-        warp_sort_desc(v, ix, lane);
-        if (lane < 16) cx0[(size_t(t) * nc + c) * 16 + lane] = Cand{v, ix};
-      }
+      float* lg = act;
+      for (int i = tid; i < T * E / 4; i += kDecThreads)
+        reinterpret_cast<float4*>(lg)[i] = reinterpret_cast<const float4*>(a.logits)[i];
       // U rows of this CTA into L2 for P3 (routing-independent), after the logits loads
       if (tid == 0 && j1 > j0) l2_prefetch_share(lw.U + size_t(j0) * L, size_t(j1 - j0) * L * 2, 0, 1);
       cp_async_wait_all();
       __syncthreads();
-      // merge levels: lists 2p, 2p+1 -> p (an odd last list passes through)
-      {
-        Cand* src = cx0;
-        Cand* dst = cx1;
-        for (int width = nc; width > 1; width = (width + 1) / 2) {
-          const int outw = (width + 1) / 2;
-          for (int task = warp; task < T * outw; task += kDecWarps) {
-            const int t = task / outw, p = task % outw;
-            const Cand* la = src + (size_t(t) * width + 2 * p) * 16;
-            Cand* lo = dst + (size_t(t) * outw + p) * 16;
-            if (2 * p + 1 < width) {
-              const Cand cv = lane < 16 ? la[lane] : la[16 + (31 - lane)];
-              float v = cv.v;
-              int ix = cv.i;
-              warp_merge_desc(v, ix, lane);
-              if (lane < 16) lo[lane] = Cand{v, ix};
-            } else if (lane < 16) {
-              lo[lane] = la[lane];
-            }
-          }
-          __syncthreads();
-          Cand* tmp = src; src = dst; dst = tmp;
-        }
-        // src holds [T][1][16]: the ranked candidates; weights = softmax over the k
-        for (int t = warp; t < T; t += kDecWarps) {
-          const Cand cv = src[size_t(t) * 16 + (lane < 16 ? lane : 0)];
-          const float top0 = __shfl_sync(kFull, cv.v, 0);
-          const float ev = lane < K ? expf(cv.v - top0) : 0.f;
-          float den = ev;
-          for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
-          if (lane < K) { tb->idx[t * K + lane] = cv.i; tb->w[t * K + lane] = ev / den; }
-        }
-      }
+      // top-k + weights: one warp per token
+      Cand* cbuf = reinterpret_cast<Cand*>(lg + size_t(T) * E) + warp * kTopkCap;
+      for (int t = warp; t < T; t += kDecWarps) warp_topk(lg + size_t(t) * E, E, K, cbuf, tb->idx + t * K, tb->w + t * K);
       __syncthreads();
       // permutation: stable order by (expert, slot)
       for (int s = tid; s < TK; s += kDecThreads) {
@@ -614,9 +774,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       __syncthreads();
       stamp0(li, kStRouted);
       const int nu = tb->nu;
-      // routed gate/up rows: q in [q0, q1) of nu * F (group-major)
-      const long nq = long(nu) * F;
-      const int q0 = int(nq * bid / G), q1 = int(nq * (bid + 1) / G);
+      // routed gate/up rows: q in [q0, q1) of nu * F (group-major), in whole tasks of 8
+      const long ntq = long(nu) * (F / 8);
+      const int q0 = 8 * int(ntq * bid / G), q1 = 8 * int(ntq * (bid + 1) / G);
       const int per_row = gu_row;
       // stage P2's down rows now when the whole P1 slab and the down slab both fit
       const int ngr = nu + 1;                          // routed groups + the shared expert
@@ -667,31 +827,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
       };
       const float sgg = tb->gsc[0].x, sgu = tb->gsc[0].y;
-      const __half* arow_all[TB];
-#pragma unroll
-      for (int i = 0; i < TB; ++i) arow_all[i] = zh + size_t(i < T ? i : 0) * L;
       const int* gexp = tb->gexp;
       const int* goff = tb->goff;
       const int* perm = tb->perm;
+      constexpr int NT = TB > 8 ? 2 : 1;                // 8-token MMA tiles
+      const int nst = (nsr + 7) / 8;                    // shared-expert tasks (8 row pairs each)
+      const int nch = L / 32;                           // 32-column chunks of a gate/up row
+      float4* part_buf = reinterpret_cast<float4*>(act);  // [warp task][lane][NT] partial sums
       int qa = q0;
       bool first_round = true;
-      while (qa < q1) {
-        // with the down rows staged behind it, every round stays inside gu_alloc
-        const int cap = min(256, (stage_down ? gu_alloc : a.dyn_bytes) / per_row);
-        if (cap < 1) {   // not even one row fits (the host rejects such shapes): stop, do not spin
-          if (tid == 0) atomicOr(a.err, kErrTimeout);
-          break;
-        }
-        const int nrow = min(cap, q1 - qa);
-        // batches of BR rows, one lane of warp 0 each (a batch may span a group boundary)
-        const int BR = (nrow + kMbRounds - 1) / kMbRounds;
-        const int nb = (nrow + BR - 1) / BR;          // every batch non-empty
-        if (warp == 0 && lane < nb) {
-          const int s0 = qa + lane * BR, s1 = min(s0 + BR, qa + nrow);
-          if (s1 > s0) {
+      while (qa < q1 || first_round) {
+        int nrow = 0, TPB = 1, nb = 0;
+        if (qa < q1) {
+          // with the down rows staged behind it, every round stays inside gu_alloc
+          const int cap = min(256, (stage_down ? gu_alloc : a.dyn_bytes) / per_row) & ~7;
+          if (cap < 8) {   // not even one 8-row task fits (the host rejects such shapes): stop, do not spin
+            if (tid == 0) atomicOr(a.err, kErrTimeout);
+            break;
+          }
+          nrow = min(cap, q1 - qa);                     // whole tasks: q0, q1 are multiples of 8
+          const int nt = nrow / 8;
+          TPB = (nt + kMbRounds - 1) / kMbRounds;       // tasks per batch, one lane of warp 0 each
+          nb = (nt + TPB - 1) / TPB;
+          if (warp == 0 && lane < nb) {
+            const int s0 = qa + lane * TPB * 8, s1 = min(s0 + TPB * 8, qa + nrow);
             const int b = lane;
             mbar_arrive_expect_tx(&tb->mbar[kMbRound + b], uint32_t(s1 - s0) * per_row);
-            uint32_t off = uint32_t(lane) * BR * per_row;
+            uint32_t off = uint32_t(s0 - qa) * per_row;
             for (int q = s0; q < s1;) {
               // rows of one expert are one byte range of its GU block
               const int g = q / F, fa = q % F;
@@ -705,67 +867,118 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
         __syncthreads();
         if (first_round) publish_scales();
-        if (first_round && nsr > 0) {
-          // shared-expert rows (staged in P0) while the routed rows land
-          wait_mb(cx, kMbShared);
-          for (;;) {
-            int r = 0;
-            if (lane == 0) r = atomicAdd(&tb->task_ctr, 1);
-            r = __shfl_sync(kFull, r, 0);
-            if (r >= nsr) break;
-            const uint8_t* row = shr + size_t(r) * gu_row;
-            gateup_row<TB>(row, row + sofs_g, row + cofs_up, row + sofs_u, L, arow_all, T, sgg, sgu, tb->zinv,
-                           [&](int i, float hv) { a.h[size_t(TK + i) * F + f0 + r] = hv; });
+        // tasks of 8 row pairs: A rows 0-7 the gate rows, 8-15 the up rows of the same
+        // f, so that each thread holds gate and up of (f, token) for the SwiGLU
+        const int ntr = nrow / 8;
+        const int ntask = ntr + (first_round ? nst : 0);
+        const int ks = mma_ksplit(ntask, 8);
+        const int g8 = lane >> 2, c4 = lane & 3;
+        // task i: routed (i < ntr: rows qa + 8 i ..) or shared (task i - ntr)
+        auto task_info = [&](int i, MmaRows& ar, const __half** brow, bool* bval, int& grp, int& fbase,
+                             int& ns) {
+          if (i < ntr) {
+            const int q = qa + 8 * i;
+            grp = q / F;
+            fbase = q % F;
+            ns = goff[grp + 1] - goff[grp];
+            const uint8_t* row = dyn + size_t(8 * i + g8) * gu_row;
+            ar.code[0] = row; ar.code[1] = row + cofs_up;
+            ar.scale[0] = row + sofs_g; ar.scale[1] = row + sofs_u;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const int n = 8 * t + g8;
+              bval[t] = n < ns;
+              brow[t] = zh + size_t(n < ns ? perm[goff[grp] + n] / K : 0) * L;
+            }
+          } else {
+            const int si = i - ntr;
+            grp = -1;
+            fbase = f0 + 8 * si;
+            ns = T;
+            const int r = 8 * si + g8;
+            const uint8_t* row = shr + size_t(r < nsr ? r : 0) * gu_row;
+            ar.code[0] = row; ar.code[1] = row + cofs_up;
+            ar.scale[0] = row + sofs_g; ar.scale[1] = row + sofs_u;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const int n = 8 * t + g8;
+              bval[t] = n < T;
+              brow[t] = zh + size_t(n < T ? n : 0) * L;
+            }
+          }
+        };
+        // SwiGLU of a finished task: thread (g8, c4) holds gate / up of row f = fbase + g8
+        // for the group's activation rows n = 8 t + 2 c4 + j
+        auto finish = [&](int i, float (*acc)[4]) {
+          MmaRows ar;
+          const __half* brow[NT];
+          bool bval[NT];
+          int grp, fbase, ns;
+          task_info(i, ar, brow, bval, grp, fbase, ns);
+          const int f = fbase + g8;
+          if (grp < 0 && 8 * (i - ntr) + g8 >= nsr) return;
+          const float gg = grp < 0 ? sgg : tb->gsc[grp + 1].x, gu = grp < 0 ? sgu : tb->gsc[grp + 1].y;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int n = 8 * t + 2 * c4 + j;
+              if (n < ns) {
+                const int slot = grp < 0 ? TK + n : perm[goff[grp] + n];
+                const float zi = tb->zinv[grp < 0 ? n : slot / K];
+                a.h[size_t(slot) * F + f] = silu_f(gg * acc[t][j] * zi) * (gu * acc[t][2 + j] * zi);
+              }
+            }
+          }
+        };
+        for (int wt = warp; wt < ntask * ks; wt += kDecWarps) {
+          const int i = wt / ks, part = wt - i * ks;
+          MmaRows ar;
+          const __half* brow[NT];
+          bool bval[NT];
+          int grp, fbase, ns;
+          task_info(i, ar, brow, bval, grp, fbase, ns);
+          if (i < ntr) {
+            wait_mb(cx, kMbRound + i / TPB);
+            wait_mb(cx, kMbScale);
+          } else {
+            wait_mb(cx, kMbShared);
+          }
+          float acc[NT][4];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+          fp4_mma_chunks<NT>(ar, brow, bval, nch * part / ks, nch * (part + 1) / ks, acc);
+          if (ks == 1) {
+            finish(i, acc);
+          } else {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+              part_buf[(size_t(wt) * 32 + lane) * NT + t] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
           }
         }
-        // one warp per row pair: lanes 0-15 gate, lanes 16-31 up
-        for (int r = warp; r < nrow; r += kDecWarps) {
-          // row r of the round sits at r * gu_row (pieces are packed back to back)
-          const int q = qa + r;
-          const int g = q / F, f = q % F;
-          wait_mb(cx, kMbRound + r / BR);
-          const uint8_t* gc = dyn + size_t(r) * gu_row;
-          const uint8_t* gs = gc + sofs_g;
-          const uint8_t* uc = gc + cofs_up;
-          const uint8_t* us = gc + sofs_u;
-          const int n = goff[g + 1] - goff[g];
-          const __half* arow[TB];
-          float ainv[TB];
+        if (ks > 1) {
+          __syncthreads();
+          for (int i = warp; i < ntask; i += kDecWarps) {
+            float acc[NT][4];
 #pragma unroll
-          for (int i = 0; i < TB; ++i) {
-            const int t = perm[goff[g] + (i < n ? i : 0)] / K;
-            arow[i] = zh + size_t(t) * L;
-            ainv[i] = tb->zinv[t];
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            for (int p = 0; p < ks; ++p) {
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                const float4 v = part_buf[(size_t(i * ks + p) * 32 + lane) * NT + t];
+                acc[t][0] += v.x; acc[t][1] += v.y; acc[t][2] += v.z; acc[t][3] += v.w;
+              }
+            }
+            finish(i, acc);
           }
-          wait_mb(cx, kMbScale);
-          const float4 gl = tb->gsc[g + 1];
-          gateup_row<TB>(gc, gs, uc, us, L, arow, n, gl.x, gl.y, ainv, [&](int i, float hv) {
-            const int slot = perm[goff[g] + i];
-            a.h[size_t(slot) * F + f] = hv;
-          });
         }
         for (int b = 0; b < nb; ++b) wait_mb(cx, kMbRound + b);
+        if (first_round && nsr > 0) wait_mb(cx, kMbShared);
         __syncthreads();
         release_mb(cx, (1u << nb) - 1u);
         if (first_round && nsr > 0) release_mb(cx, 1u << kMbShared);
         qa += nrow;
         first_round = false;
-      }
-      if (first_round) publish_scales();
-      if (first_round && nsr > 0) {
-        // no routed rows for this CTA: the shared rows still run
-        wait_mb(cx, kMbShared);
-        for (;;) {
-          int r = 0;
-          if (lane == 0) r = atomicAdd(&tb->task_ctr, 1);
-          r = __shfl_sync(kFull, r, 0);
-          if (r >= nsr) break;
-          const uint8_t* row = shr + size_t(r) * gu_row;
-          gateup_row<TB>(row, row + sofs_g, row + cofs_up, row + sofs_u, L, arow_all, T, sgg, sgu, tb->zinv,
-                         [&](int i, float hv) { a.h[size_t(TK + i) * F + f0 + r] = hv; });
-        }
-        __syncthreads();
-        release_mb(cx, 1u << kMbShared);
       }
       if (stage_down && warp == 1) {
         // down rows [r0, r1) of every used expert (shared first), for P2, issued once
@@ -842,6 +1055,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       float* ob = reinterpret_cast<float*>(region);
       const int ob_bytes = (nslot * nr * 4 + 127) & ~127;
+      constexpr int NTD = TB > 8 ? 2 : 1;             // 8-token MMA tiles
       const int hrow = F * 2;
       wait_mb(cx, kMbScale);
       // Slots in one order q: q < T the shared expert's slot of token q (slot TK + q),
@@ -944,41 +1158,97 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           }
         }
         __syncthreads();
-        // tasks (group, row): 8 lanes each, 4 per warp; the loop bound is uniform per warp
-        const int l8 = tid & 7;
-        for (int tbase = warp * 4; tbase < ng * nr; tbase += kDecThreads / 8) {
-          const int task = tbase + (lane >> 3);
-          const bool valid = task < ng * nr;
-          const int jj = valid ? task / nr : 0, r = valid ? task % nr : 0;
-          const int j = ja + jj;
-          const int qs = max(qa, qlo(j));                       // the group's slots in this round
-          const int ns = !valid ? 0 : min(qb, qhi(j)) - qs;
-          if (valid) {
-            if (down_staged) wait_mb(cx, kMbDown + j / per_b);
-            else wait_mb(cx, kMbRound + tb->task_aux[jj]);
-          }
+        // tasks (group, 16-row tile of this CTA's latent rows): MMAs over the F columns,
+        // A = the down rows (rho = tile row), B = the group's h rows of this round
+        const int g8 = lane >> 2, c4 = lane & 3;
+        const int rt = (nr + 15) / 16;
+        const int ntask2 = ng * rt;
+        const int ks2 = mma_ksplit(ntask2, 4);
+        const int nchd = F / 32;
+        float4* part_buf = reinterpret_cast<float4*>(act);
+        auto dtask = [&](int i, MmaRows& ar, const __half** brow, bool* bval, int& j, int& qs, int& ns,
+                         int& rbase) {
+          const int jj = i / rt;
+          rbase = 16 * (i - jj * rt);
+          j = ja + jj;
+          qs = max(qa, qlo(j));
+          ns = min(qb, qhi(j)) - qs;
           const uint8_t* gbase = wbase + size_t(down_staged ? j : jj) * down_grp;
-          const uint8_t* pr = gbase + size_t(r / 2) * d_pair;
-          const uint8_t* codes = pr + (r & 1) * (F / 2);
-          const uint8_t* scl = pr + F + (r & 1) * (F / 16);
-          const __half* arow[TB];
 #pragma unroll
-          for (int i = 0; i < TB; ++i) arow[i] = hs + size_t(qs - qa + (i < ns ? i : 0)) * F;
-          float acc[TB];
+          for (int h = 0; h < 2; ++h) {
+            int rho = rbase + g8 + 8 * h;
+            if (rho >= nr) rho = 0;
+            const uint8_t* pr = gbase + size_t(rho / 2) * d_pair;
+            ar.code[h] = pr + (rho & 1) * (F / 2);
+            ar.scale[h] = pr + F + (rho & 1) * (F / 16);
+          }
 #pragma unroll
-          for (int i = 0; i < TB; ++i) acc[i] = 0.f;
-          fp4_dot<TB>(codes, scl, F / 16, arow, ns, l8, 8, acc);
-          group_reduce<TB>(acc, 8);
-          if (valid && l8 == 0) {
-            const float gd = tb->gsc[j].z;
+          for (int t = 0; t < NTD; ++t) {
+            const int n = 8 * t + g8;
+            bval[t] = n < ns;
+            brow[t] = hs + size_t(qs - qa + (n < ns ? n : 0)) * F;
+          }
+        };
+        auto dfinish = [&](int i, float (*acc)[4]) {
+          MmaRows ar;
+          const __half* brow[NTD];
+          bool bval[NTD];
+          int j, qs, ns, rbase;
+          dtask(i, ar, brow, bval, j, qs, ns, rbase);
+          const float gd = tb->gsc[j].z;
 #pragma unroll
-            for (int i = 0; i < TB; ++i) {
-              if (i < ns) {
-                const int q = qs + i;
-                const int slot = (q < T) ? TK + q : tb->perm[q - T];
-                ob[size_t(slot) * nr + r] = gd * tb->hinv[slot] * acc[i];
+          for (int h = 0; h < 2; ++h) {
+            const int rho = rbase + g8 + 8 * h;
+            if (rho >= nr) continue;
+#pragma unroll
+            for (int t = 0; t < NTD; ++t) {
+#pragma unroll
+              for (int jx = 0; jx < 2; ++jx) {
+                const int n = 8 * t + 2 * c4 + jx;
+                if (n < ns) {
+                  const int q = qs + n;
+                  const int slot = (q < T) ? TK + q : tb->perm[q - T];
+                  ob[size_t(slot) * nr + rho] = gd * tb->hinv[slot] * acc[t][2 * h + jx];
+                }
               }
             }
+          }
+        };
+        for (int wt = warp; wt < ntask2 * ks2; wt += kDecWarps) {
+          const int i = wt / ks2, part = wt - i * ks2;
+          MmaRows ar;
+          const __half* brow[NTD];
+          bool bval[NTD];
+          int j, qs, ns, rbase;
+          dtask(i, ar, brow, bval, j, qs, ns, rbase);
+          if (down_staged) wait_mb(cx, kMbDown + j / per_b);
+          else wait_mb(cx, kMbRound + tb->task_aux[i / rt]);
+          float acc[NTD][4];
+#pragma unroll
+          for (int t = 0; t < NTD; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+          fp4_mma_chunks<NTD>(ar, brow, bval, nchd * part / ks2, nchd * (part + 1) / ks2, acc);
+          if (ks2 == 1) {
+            dfinish(i, acc);
+          } else {
+#pragma unroll
+            for (int t = 0; t < NTD; ++t)
+              part_buf[(size_t(wt) * 32 + lane) * NTD + t] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+          }
+        }
+        if (ks2 > 1) {
+          __syncthreads();
+          for (int i = warp; i < ntask2; i += kDecWarps) {
+            float acc[NTD][4];
+#pragma unroll
+            for (int t = 0; t < NTD; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            for (int pp = 0; pp < ks2; ++pp) {
+#pragma unroll
+              for (int t = 0; t < NTD; ++t) {
+                const float4 v = part_buf[(size_t(i * ks2 + pp) * 32 + lane) * NTD + t];
+                acc[t][0] += v.x; acc[t][1] += v.y; acc[t][2] += v.z; acc[t][3] += v.w;
+              }
+            }
+            dfinish(i, acc);
           }
         }
         if (!down_staged) {

@@ -31,6 +31,7 @@ constexpr int kMaxTopK = 16;
 constexpr int kDecodeMaxT = 16;
 constexpr int kMaxSlots = kDecodeMaxT * (kMaxTopK + 1);
 constexpr int kNumMbar = 16;
+constexpr int kTopkCand = 64;   // candidates per warp of the top-k (shared memory)
 // mbarrier roles
 constexpr int kMbRound = 0;      // 0..7: batches of the current round
 constexpr int kMbRounds = 8;

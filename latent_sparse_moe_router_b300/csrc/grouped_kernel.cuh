@@ -12,16 +12,6 @@ constexpr int kGgBBox = 64;       // rows of one B box (TMA)
 // result is rounded to bf16, far coarser than their error); v -> -inf gives -0.
 __device__ __forceinline__ float silu_gg(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-// Four E2M1 pairs (one 32-bit word, byte i = elements 2i, 2i+1, low nibble first)
-// -> four f16x2.
-__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
-                                               uint32_t& h3) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
-}
-
 // f16x2 holding E2M1 values -> bf16x2 times a block scale, exact.  sc2 holds the
 // scale times 2^112 in both bf16 halves: moving the f16 bits right by 3 puts the
 // exponent field in bf16 position (the value becomes 2^-112 too small) and drops
@@ -30,18 +20,6 @@ __device__ __forceinline__ uint32_t h2_to_bf2_scaled(uint32_t h, uint32_t sc2) {
   const uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
   __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
                              *reinterpret_cast<const __nv_bfloat162*>(&sc2));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// f16x2 (both halves) of an E4M3 scale (exact).
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e4m3) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(e4m3 | (e4m3 << 8))));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 

@@ -36,3 +36,23 @@ def check_layer(dev, lay, x_bits: np.ndarray, y_gpu_bits: np.ndarray, routing: d
     assert mx <= MAX_ABS, f"max abs / rms {mx:.3e}"
     return dict(rel_l2=rel, max_abs_over_rms=mx, flips=len(flipped), tokens=len(sel))
 
+
+
+def chain_amplification(lays, x_bits: np.ndarray, idx_per_layer, seed: int = 99):
+    """The oracle stack's own amplification of a rounding-level input change: one bf16
+    ulp moved in a seeded tenth of the input elements, routing forced to the given
+    indices in both runs.  Returns (relative output change) / (relative input change)."""
+    xp = np.array(x_bits, dtype=np.uint16)
+    xp[np.random.default_rng(seed).random(xp.shape) < 0.1] ^= np.uint16(1)
+    x0, x1 = moe.bf16_to_f64(x_bits), moe.bf16_to_f64(xp)
+    d_in = np.linalg.norm(x1 - x0) / np.linalg.norm(x0)
+    f0 = moe.bf16_to_f64(stack_chain(lays, x_bits, idx_per_layer)[0])
+    f1 = moe.bf16_to_f64(stack_chain(lays, xp, idx_per_layer)[0])
+    return float(np.linalg.norm(f1 - f0) / np.linalg.norm(f0) / d_in)
+
+
+def stack_e2e_bound(layer_rels, amplification: float) -> float:
+    """End-to-end error the per-layer checks imply: the measured per-layer errors (each
+    on the GPU's own input and routing) add in quadrature and are carried to the output
+    with at most the chain's own measured amplification."""
+    return float(np.sqrt(np.sum(np.square(layer_rels)))) * max(1.0, amplification)

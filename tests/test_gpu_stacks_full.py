@@ -29,7 +29,7 @@ def test_stack48_145b_decode_teacher_forced_and_end_to_end():
     GPU's routing at every layer, within the quadrature bound of 48 layers."""
     from synth import device
     import stack_oracle
-    from parity import MAX_ABS, REL_L2, stack_rel_l2
+    from parity import MAX_ABS, REL_L2, stack_e2e_bound
     L, E, K, F, n_layers, H = 1792, 512, 10, 640, 48, 2560
     pool = stack_oracle.make_pool()          # spawned workers: no CUDA context in them
     stride = ext.edge0_expert_record_stride(L, F)
@@ -62,11 +62,12 @@ def test_stack48_145b_decode_teacher_forced_and_end_to_end():
         nxt = moe.residual_rmsnorm(txb[:, l], tyb[:, l])
         assert np.mean(nxt == txb[:, l + 1]) > 0.99
     tasks = [(2, l, L, 0.0, txb[:, l], tyb[:, l], tib[:, l]) for l in range(n_layers)]
-    flips = 0
+    flips, rels = 0, []
     for l, rel, mx, nf, bad in pool.imap_unordered(stack_oracle.layer_task, tasks):
         assert not bad, f"layer {l}: routing differs beyond near-ties at tokens {bad}"
         assert rel <= REL_L2 and mx <= MAX_ABS, (l, rel, mx)
         flips += nf
+        rels.append(rel)
     chains = pool.map(stack_oracle.chain_task,
                       [(2, n_layers, L, (0.0,), x_all[j:j + 1], tib[i][:, None, :], i < 4)
                        for i, j in enumerate(toks)])
@@ -80,10 +81,10 @@ def test_stack48_145b_decode_teacher_forced_and_end_to_end():
     amp = max(c[3][1] / c[3][0] for c in chains if c[3] is not None)
     got, refv = moe.bf16_to_f64(yb), moe.bf16_to_f64(ref)
     e2e = np.linalg.norm(got - refv) / np.linalg.norm(refv)
-    # what the per-layer checks imply end to end: each layer's error (<= REL_L2 on the
+    # what the per-layer checks imply end to end: each layer's measured error (on the
     # same input and routing) is carried to the output with the chain's own measured
     # amplification of a rounding-level input change, and errors add in quadrature
-    bound = stack_rel_l2(n_layers) * max(1.0, amp)
+    bound = stack_e2e_bound(rels, amp)
     print(f"stack48: {n} tokens x 48 layers, near-tie flips {flips}; oracle chain vs forced routing "
           f"{chain_flips}; end-to-end rel L2 {e2e:.2e}; chain amplification {amp:.2f}; bound {bound:.2e}")
     assert e2e <= bound
@@ -98,7 +99,7 @@ def test_prefill4x145b_t16384_stack_sampled():
     layer (routing with near-tie flips counted, y teacher-forced); and the stack
     output on the sample against the oracle stack run on those rows."""
     from synth import device
-    from parity import check_layer, stack_chain, stack_rel_l2
+    from parity import chain_amplification, check_layer, stack_chain, stack_e2e_bound
     T, n_layers = 16384, 4
     zipf = (0.0, 1.1, 0.0, 1.1)
     inps = [synth.make_layer(synth.LayerSpec(seed=4, layer=l, latent=1792, zipf=zipf[l])) for l in range(n_layers)]
@@ -115,7 +116,7 @@ def test_prefill4x145b_t16384_stack_sampled():
     sel = np.unique(np.concatenate([np.random.default_rng(45).choice(T, 48, replace=False), [0, T - 1]]))
     cur = x
     flips = 0
-    idx_layers = []
+    idx_layers, rels = [], []
     for l, d in enumerate(devs):
         yl = torch.empty_like(cur)
         ext.edge0_moe_forward(d.handle, cur, yl, T)
@@ -125,6 +126,7 @@ def test_prefill4x145b_t16384_stack_sampled():
         idx_layers.append(r["idx"])
         m = check_layer(d, lays[l], _bits(cur), _bits(yl), r, tokens=sel, check_perm=(l == 0))
         flips += m["flips"]
+        rels.append(m["rel_l2"])
         print(f"prefill4x layer {l}: sampled rel L2 {m['rel_l2']:.2e}, max/rms {m['max_abs_over_rms']:.2e}, "
               f"flips {m['flips']}")
         nx = torch.empty_like(cur)
@@ -133,12 +135,16 @@ def test_prefill4x145b_t16384_stack_sampled():
     torch.cuda.synchronize()
     assert np.array_equal(_bits(cur), y_stack)
     # end to end on the sample: the oracle stack forced to the GPU's routing per layer
-    xf, chain_flips, bad = stack_chain(lays, x_bits[sel], [r[sel] for r in idx_layers])
-    assert not bad, bad
+    # (that chain runs on its own inputs: where its own top-k differs from the forced
+    # choice it is counted, not an error; the GPU's routing was checked per layer above)
+    idx_sel = [r[sel] for r in idx_layers]
+    xf, chain_flips, chain_bad = stack_chain(lays, x_bits[sel], idx_sel)
     got, ref = moe.bf16_to_f64(y_stack[sel]), moe.bf16_to_f64(xf)
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    print(f"prefill4x T=16384: sampled {len(sel)} tokens, end-to-end rel L2 {rel:.2e} "
-          f"(bound {stack_rel_l2(n_layers):.2e}), near-tie flips {flips} (oracle chain {chain_flips})")
-    assert rel <= stack_rel_l2(n_layers)
+    amp = chain_amplification(lays, x_bits[sel[:8]], [r[:8] for r in idx_sel])
+    bound = stack_e2e_bound(rels, amp)
+    print(f"prefill4x T=16384: sampled {len(sel)} tokens, end-to-end rel L2 {rel:.2e} (bound {bound:.2e}, "
+          f"chain amplification {amp:.2f}), near-tie flips {flips} (oracle chain {chain_flips + len(chain_bad)})")
+    assert rel <= bound
     for d in devs:
         d.close()

@@ -294,12 +294,15 @@ edge0_status edge0_moe_stage_times(void *handle, float *ms, int max, int *n_out)
  *   CTAs' P0 ends, 2 grid barrier 1, 3 routing (top-k, weights, permutation) on
  *   CTA 0, 4 rest of P1 (gate/up) to the last CTA's end, 5 spread of P1 ends,
  *   6 barrier 2, 7 P2 (down + combine), 8 spread, 9 barrier 3, 10 P3 (U), 11
- *   spread, 12 barrier 4 (stacks; 0 otherwise), 13 the layer's total.
+ *   spread, 12 barrier 4 (stacks; 0 otherwise), 13 the layer's total; and on
+ *   CTA 0's clock: 14 routing's loads of the logits and z, 15 the top-k and
+ *   weights, 16 issue of the first expert copies after routing, 17 P2's first
+ *   staging of h, 18 P2's down MMAs of all rounds.
  * n = min(max, layers * EDGE0_DECODE_PHASES); *n_out = n.  UNSUPPORTED if no
  * profiled decode launch ran.  Profiling adds one memset per launch and a few
  * stores per CTA and phase.
  */
-#define EDGE0_DECODE_PHASES 14
+#define EDGE0_DECODE_PHASES 19
 edge0_status edge0_moe_profile_decode(void *handle, int enable);
 edge0_status edge0_moe_decode_phase_times(void *handle, float *us, int max, int *n_out);
 

@@ -245,9 +245,10 @@ def edge0_moe_stage_times(handle):
     return [float(buf[i]) for i in range(n.value)]
 
 
-EDGE0_DECODE_PHASES = 14
+EDGE0_DECODE_PHASES = 19
 DECODE_PHASE_NAMES = ("p0", "p0_spread", "barrier1", "routing", "p1_gate_up", "p1_spread", "barrier2",
-                      "p2_down_combine", "p2_spread", "barrier3", "p3_u", "p3_spread", "barrier4", "layer_total")
+                      "p2_down_combine", "p2_spread", "barrier3", "p3_u", "p3_spread", "barrier4", "layer_total",
+                      "routing_loads", "routing_topk", "p1_issue", "p2_h_staging", "p2_down_mma")
 
 
 def edge0_moe_profile_decode(handle, enable: bool):

@@ -697,7 +697,9 @@ edge0_status edge0_moe_decode_phase_times(void* handle, float* us, int max, int*
         d(t[kStP1EndMax], t[kStBar2]), d(t[kStBar2], t[kStP2EndMax]), d(e2, t[kStP2EndMax]),
         d(t[kStP2EndMax], t[kStBar3]), d(t[kStBar3], t[kStP3EndMax]), d(e3, t[kStP3EndMax]),
         t[kStBar4] ? d(t[kStP3EndMax], t[kStBar4]) : 0.f,
-        d(t[kStP0Start], t[kStBar4] ? t[kStBar4] : t[kStP3EndMax])};
+        d(t[kStP0Start], t[kStBar4] ? t[kStBar4] : t[kStP3EndMax]),
+        d(t[kStBar1], t[kStRouteLoaded]), d(t[kStRouteLoaded], t[kStTopk]), d(t[kStRouted], t[kStP1Issued]),
+        d(t[kStBar2], t[kStP2Staged]), d(t[kStP2Staged], t[kStP2Tasks])};
     for (int i = 0; i < EDGE0_DECODE_PHASES && n < max; ++i) us[n++] = v[i];
   }
   if (n_out) *n_out = n;

@@ -740,10 +740,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       if (tid == 0 && j1 > j0) l2_prefetch_share(lw.U + size_t(j0) * L, size_t(j1 - j0) * L * 2, 0, 1);
       cp_async_wait_all();
       __syncthreads();
+      stamp0(li, kStRouteLoaded);
       // top-k + weights: one warp per token
       Cand* cbuf = reinterpret_cast<Cand*>(lg + size_t(T) * E) + warp * kTopkCap;
       for (int t = warp; t < T; t += kDecWarps) warp_topk(lg + size_t(t) * E, E, K, cbuf, tb->idx + t * K, tb->w + t * K);
       __syncthreads();
+      stamp0(li, kStTopk);
       // permutation: stable order by (expert, slot)
       for (int s = tid; s < TK; s += kDecThreads) {
         const int key = tb->idx[s];
@@ -866,6 +868,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           }
         }
         __syncthreads();
+        if (first_round) stamp0(li, kStP1Issued);
         if (first_round) publish_scales();
         // tasks of 8 row pairs: A rows 0-7 the gate rows, 8-15 the up rows of the same
         // f, so that each thread holds gate and up of (f, token) for the SwiGLU
@@ -1158,6 +1161,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           }
         }
         __syncthreads();
+        if (qa == 0) stamp0(li, kStP2Staged);
         // tasks (group, 16-row tile of this CTA's latent rows): MMAs over the F columns,
         // A = the down rows (rho = tile row), B = the group's h rows of this round
         const int g8 = lane >> 2, c4 = lane & 3;
@@ -1258,6 +1262,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         if (!down_staged) release_mb(cx, (1u << nb) - 1u);
         qa = qb;
       }
+      stamp0(li, kStP2Tasks);
       if (!u_issued) issue_u();
       if (down_staged) {
         for (int b = 0; b < n_down_b; ++b) wait_mb(cx, kMbDown + b);

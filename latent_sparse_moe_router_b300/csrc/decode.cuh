@@ -53,7 +53,12 @@ enum DecStamp {
   kStP1EndMax, kStP1EndMin, kStBar2,
   kStP2EndMax, kStP2EndMin, kStBar3,
   kStP3EndMax, kStP3EndMin, kStBar4,        // barrier 4: stacks only
-  kStampSlots = 16
+  kStRouteLoaded,                           // CTA 0: logits and zh in shared memory
+  kStTopk,                                  // CTA 0: top-k and weights done
+  kStP1Issued,                              // CTA 0: first round of expert copies issued
+  kStP2Staged,                              // CTA 0: first round of h rows staged
+  kStP2Tasks,                               // CTA 0: down tasks of all rounds done
+  kStampSlots = 24
 };
 
 // One layer's weights as the decode kernel sees them.

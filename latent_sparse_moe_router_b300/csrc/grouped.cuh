@@ -57,8 +57,8 @@ struct GgSmem {
   static constexpr int kB = kGgBN / 2 * 64 * 2;  // 16 KB: this CTA's half of the token rows
   static constexpr int kRaw = 128 * 32;          // 4 KB
   static constexpr int kSc = 16384;              // scales of one tile (<= 128 rows x 128 B)
-  static constexpr int kEpiT = 9216;             // epilogue transpose buffers
-  static constexpr int kEpi = kEpiT + kGgBN * 4; // + the tile's token scales (mode 1)
+  static constexpr int kEpiPitch = 80;           // bytes per token row of an epilogue warp's staging
+  static constexpr int kEpi = 8 * 32 * kEpiPitch;  // 8 epilogue warps x 32 token rows
   static constexpr int offA = 0;
   static constexpr int offB = offA + kGgSA * kA;
   static constexpr int offRaw = offB + kGgSB * kB;

@@ -174,16 +174,17 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
     }
   } else if (warp == kGgBWarp) {
     if (lane == 0) {
-      // ---- B producer: this CTA's half of the tile's token rows (MMA columns
-      // rank * N/2 ..), one k-slice per stage, completing on rank 0's barrier
+      // ---- token producer: this CTA's 128 token rows of the tile (MMA rows 128 rank ..,
+      // the M side), one k-slice per stage, completing on rank 0's barrier.  Boxes
+      // wholly past the tile's rows are not loaded: those accumulator rows are never read
       const uint32_t bfull0 = mapa_shared(smem_u32(b_full), 0);
       int it = 0;
       for (int tile = pair; ok && tile < total; tile += npairs) {
         const GgTile t = gg_tile(p, tile, rank);
         const CUtensorMap* mb = (t.shared && p.mode == 1) ? &maps.b_shared : &maps.b_routed;
-        const int half = t.n_mma >> 1;
-        const int row0 = t.pos0 + rank * half;
-        const int nbox = (half + kGgBBox - 1) / kGgBBox;
+        const int mine = min(128, max(0, t.n_rows - 128 * rank));
+        const int row0 = t.pos0 + rank * 128;
+        const int nbox = (mine + kGgBBox - 1) / kGgBBox;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kGgSB;
           if (!mbar_wait_abort(&b_empty[s], ((it / kGgSB) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
@@ -201,7 +202,9 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       int it = 0, ti = 0;
       for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
         const GgTile t = gg_tile(p, tile, 0);
-        const uint32_t idesc = p.mode == 1 ? idesc_f16_f32(256, t.n_mma) : idesc_bf16_f32(256, t.n_mma);
+        // M = 256 token rows (128 per CTA), N = 256 weight rows (the two CTAs' tiles)
+        const uint32_t idesc = p.mode == 1 ? idesc_f16_f32(256, 256) : idesc_bf16_f32(256, 256);
+        (void)t;
         const int ab = ti & 1;
         if (!mbar_wait_abort(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, p.err, p.abort)) { ok = false; break; }
         tc_fence_after();
@@ -218,7 +221,7 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
           const uint32_t sbb = smem_u32(smem + GgSmem::offB + sb_i * GgSmem::kB);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_pair_f16(acc, sw128_desc(sa + k * 32), sw128_desc(sbb + k * 32), idesc, (kb | k) != 0);
+            mma_pair_f16(acc, sw128_desc(sbb + k * 32), sw128_desc(sa + k * 32), idesc, (kb | k) != 0);
           mma_pair_commit_both(&a_empty[sa_i]);
           mma_pair_commit_both(&b_empty[sb_i]);
         }
@@ -301,81 +304,89 @@ grouped_nvfp4_kernel(const __grid_constant__ GgMaps maps, const __grid_constant_
       if (lane == 0) mbar_arrive(&sc_empty[sb]);
     }
   } else {
-    // ---- epilogue: warp q = warp % 4 reads TMEM lanes 32q .. 32q + 31 (A rows), and
-    // half ch of every 32-column chunk (columns 16 ch .. 16 ch + 15).  Neighbouring
-    // lanes hold the row pair (2i, 2i+1); after one shuffle per column pair the even
-    // lane finishes the half's first 8 token columns, the odd lane the last 8.
+    // ---- epilogue: TMEM lane = token row 128 rank + lane of the pair tile.  Warp q =
+    // warp % 4 reads lanes 32q .. 32q + 31, and half ch of the 256 columns: the weight
+    // rows of CTA ch's tile (mode 1: columns 2i, 2i + 1 = gate, up of f = 64 mt + i;
+    // mode 2: column i = latent row 128 mt + i), 32 columns per TMEM load.  Each
+    // thread then stores its token's values as whole 16-byte pieces of its output row.
     const int q = warp & 3;
-    const int te = threadIdx.x - kGgEpWarp0 * 32;   // 0..255
-    const int ch = te >> 7;
-    const int odd = lane & 1, pr = q * 16 + (lane >> 1);   // row pair in the tile
-    // mode 1: [32 tokens][72] bf16 (64 f used); mode 2: [32 tokens][68] u32 (64 latent pairs used)
-    __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(smem + GgSmem::offEpi);
-    uint32_t* obuf = reinterpret_cast<uint32_t*>(smem + GgSmem::offEpi);
-    float* zbuf = reinterpret_cast<float*>(smem + GgSmem::offEpi + GgSmem::kEpiT);   // [256] token scales
+    const int ch = (warp - kGgEpWarp0) >> 2;
     const uint32_t accempty0 = mapa_shared(smem_u32(acc_empty), 0);
     int ti = 0;
     for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
       const GgTile t = gg_tile(p, tile, rank);
       const int ab = ti & 1;
+      const int tok = 128 * rank + 32 * q + lane;
+      const bool valid = tok < t.n_rows;
+      const int mtc = t.mt - rank + ch;           // the weight tile whose columns this half holds
       // the tile's global reads go out before the accumulator wait: the record's fp32
-      // scales, and (mode 1) one column's token scale per thread into the shared table
-      // (the previous tile's last named barrier has passed: no thread still reads it)
+      // scales (of CTA ch's expert: the pair shares the group) and this token's scale
       const uint8_t* rec = t.shared ? p.shared : p.experts + size_t(t.g) * p.stride;
       const float* gl = reinterpret_cast<const float*>(rec + size_t(27) * p.F * p.L / 16);
       const float g0 = p.mode == 1 ? gl[0] : gl[2], g1 = gl[1];
-      if (p.mode == 1) zbuf[te] = te < t.n_rows ? __ldg(&p.pos_inv[t.out0 + te]) : 1.0f;
-      // uniform across the epilogue warps: all agree the accumulator is complete (this
-      // barrier also publishes the token-scale table)
+      const float zi = (p.mode == 1 && valid) ? __ldg(&p.pos_inv[t.out0 + tok]) : 1.0f;
+      // uniform across the epilogue warps: all agree the accumulator is complete
       ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, p.err, p.abort);
       if (!named_and(1, kGgEpThreads, ok)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256 + ch * 16;
-      const int tr = te >> 3, part = te & 7;
-      for (int c = 0; c * 32 < t.n_rows; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tbase + c * 32, v);
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + ab * 256 + ch * 128;
+      // this warp's 32 token rows go through a padded staging buffer (one row per
+      // thread, written conflict-free), then out as row-contiguous 16-byte pieces
+      uint8_t* stg = smem + GgSmem::offEpi + (warp - kGgEpWarp0) * 32 * GgSmem::kEpiPitch;
+      const int tok0 = 128 * rank + 32 * q;          // the warp's first token row
+      const int nvalid = min(32, max(0, t.n_rows - tok0));
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
         tmem_ld_wait();
-        const int col0 = ch * 16 + odd * 8;   // first token column this lane finishes
+        uint4* my = reinterpret_cast<uint4*>(stg + lane * GgSmem::kEpiPitch);
         if (p.mode == 1) {
+          // 16 f values: f = 64 mtc + 16 c + i, gate in column 2i, up in 2i + 1
+          uint32_t o[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t va = v[j], vb = v[8 + j];
-            const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
-            const float gate = odd ? x : __uint_as_float(va);
-            const float up = odd ? __uint_as_float(vb) : x;
-            // undo the token's power-of-two scale of z (exact)
-            const float zi = zbuf[c * 32 + col0 + j];
-            hbuf[(col0 + j) * 72 + pr] = __float2bfloat16_rn(silu_gg(g0 * zi * gate) * (g1 * zi * up));
+          for (int i = 0; i < 8; ++i) {
+            const float h0 = silu_gg(g0 * zi * __uint_as_float(v[4 * i])) * (g1 * zi * __uint_as_float(v[4 * i + 1]));
+            const float h1 =
+                silu_gg(g0 * zi * __uint_as_float(v[4 * i + 2])) * (g1 * zi * __uint_as_float(v[4 * i + 3]));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+            o[i] = *reinterpret_cast<const uint32_t*>(&b);
           }
-          named_sync(1, kGgEpThreads);
-          // 32 token rows x 64 f (128 B): 8 threads per row, 16 B each
-          if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(hbuf + tr * 72 + part * 8);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 64 + part * 8);
-            dst[0] = src[0];
+          my[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          my[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          __syncwarp();
+          // 32 rows x 32 bytes: two threads per row
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int i = lane + 32 * k, r = i >> 1, pc = i & 1;
+            if (r < nvalid) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * GgSmem::kEpiPitch + pc * 16);
+              *reinterpret_cast<uint4*>(p.out + size_t(t.out0 + tok0 + r) * p.out_ld + 64 * mtc + 16 * c + 8 * pc) = val;
+            }
           }
         } else {
+          // 32 latent rows 128 mtc + 32 c + j
+          uint32_t o[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t va = v[j], vb = v[8 + j];
-            const float x = __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, odd ? va : vb, 1));
-            const float lo = odd ? x : __uint_as_float(va);            // latent row 2i
-            const float hi = odd ? __uint_as_float(vb) : x;            // latent row 2i + 1
-            const __nv_bfloat162 b = __floats2bfloat162_rn(g0 * lo, g0 * hi);
-            obuf[(col0 + j) * 68 + pr] = *reinterpret_cast<const uint32_t*>(&b);
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b =
+                __floats2bfloat162_rn(g0 * __uint_as_float(v[2 * i]), g0 * __uint_as_float(v[2 * i + 1]));
+            o[i] = *reinterpret_cast<const uint32_t*>(&b);
           }
-          named_sync(1, kGgEpThreads);
-          // 32 token rows x 128 latent rows (256 B): 8 threads per row, 32 B each
-          if (c * 32 + tr < t.n_rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(obuf + tr * 68 + part * 8);
-            uint4* dst =
-                reinterpret_cast<uint4*>(p.out + size_t(t.out0 + c * 32 + tr) * p.out_ld + t.mt * 128 + part * 16);
-            dst[0] = src[0];
-            dst[1] = src[1];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) my[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          __syncwarp();
+          // 32 rows x 64 bytes: four threads per row
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i = lane + 32 * k, r = i >> 2, pc = i & 3;
+            if (r < nvalid) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + r * GgSmem::kEpiPitch + pc * 16);
+              *reinterpret_cast<uint4*>(p.out + size_t(t.out0 + tok0 + r) * p.out_ld + 128 * mtc + 32 * c + 8 * pc) = val;
+            }
           }
         }
-        named_sync(1, kGgEpThreads);
+        __syncwarp();   // the staging rows are rewritten by the next chunk
       }
       // the accumulator's TMEM columns are free for the tile after next
       tc_fence_before();

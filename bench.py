@@ -38,6 +38,9 @@ WORKLOADS = {
     "layer145b_t4096_zipf": dict(kind="prefill", latent=1792, T=4096, seed=3, layers=1, zipf=(1.1,),
                                  instances=2,
                                  desc="one Edge0-145B layer, prefill T=4096, Zipf(1.1) router bias"),
+    # one layer of the 16K workload (its uniform-routing first layer): a size for profiling captures
+    "layer145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=1, zipf=(0.0,), instances=1,
+                             desc="one Edge0-145B layer, prefill T=16384, uniform routing (profiling size)"),
     "prefill4x145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=4,
                                  zipf=(0.0, 1.1, 0.0, 1.1), instances=1,
                                  desc="4 Edge0-145B layers, prefill T=16384, uniform/Zipf(1.1) alternating"),

@@ -144,7 +144,7 @@ void fill_decode_args(const Handle* hd, DecodeArgs& a, const void* x, void* y, i
   a.y = static_cast<__nv_bfloat16*>(y);
   a.T = T;
   a.H = hd->d.hidden; a.L = hd->d.latent; a.E = hd->d.n_experts; a.K = hd->d.top_k; a.F = hd->d.ffn;
-  a.z = hd->z; a.zh = hd->zh; a.logits = hd->logits; a.h = hd->h; a.c = hd->c;
+  a.z = hd->z; a.zh = hd->zh; a.logits = hd->logits; a.h = reinterpret_cast<__nv_bfloat16*>(hd->h); a.c = hd->c;
   a.ybuf = hd->ybuf; a.xbuf = hd->xbuf;
   a.idx = hd->idx; a.w = hd->w; a.counts = hd->counts; a.offsets = hd->offsets;
   a.perm = hd->perm; a.pos = hd->pos;

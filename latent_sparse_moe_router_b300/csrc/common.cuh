@@ -291,6 +291,24 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// f16x2 holding E2M1 values -> bf16x2 times a block scale, exact.  sc2 holds the
+// scale times 2^112 in both bf16 halves: moving the f16 bits right by 3 puts the
+// exponent field in bf16 position (the value becomes 2^-112 too small) and drops
+// three mantissa bits the E2M1 values never use; the sign bits are kept as they are.
+__device__ __forceinline__ uint32_t h2_to_bf2_scaled(uint32_t h, uint32_t sc2) {
+  const uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
+                             *reinterpret_cast<const __nv_bfloat162*>(&sc2));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// bf16x2 (both halves) of an E4M3 scale times 2^112.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t e4m3) {
+  const float s = e4m3_to_f32(e4m3) * 5.192296858534828e33f;  // 2^112
+  __nv_bfloat162 r = __floats2bfloat162_rn(s, s);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // D += A B (m16n8k16, f16 inputs, fp32 accumulate), warp-wide.  Fragments per
 // thread (g = lane / 4, c = lane % 4): a0 (row g, k 2c, 2c+1), a1 (row g + 8, same
 // k), a2 (row g, k 2c + 8, 2c + 9), a3 (row g + 8, same); b0 (k 2c, 2c+1, column g),
@@ -299,6 +317,14 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same MMA with bf16 inputs.
+__device__ __forceinline__ void mma16816_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }

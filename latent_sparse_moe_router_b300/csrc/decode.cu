@@ -574,6 +574,39 @@ __device__ __forceinline__ void fp4_mma_chunks(const MmaRows& ar, const __half* 
   }
 }
 
+// The same with bf16 operands (the down projection: B = SwiGLU activations in bf16).
+// NVFP4 -> f16 by cvt, then to the bf16 exponent range and times the block scale
+// (exact: E2M1 x E4M3 has at most 5 significant bits).
+template <int NT>
+__device__ __forceinline__ void fp4_mma_chunks_bf16(const MmaRows& ar, const __nv_bfloat16* const* brow,
+                                                    const bool* bval, int s0, int s1, float (*acc)[4]) {
+  const int c = threadIdx.x & 3;
+  const uint8_t* ca = ar.code[0] + 4 * c;
+  const uint8_t* cb = ar.code[1] + 4 * c;
+  const uint8_t* sa = ar.scale[0] + (c >> 1);
+  const uint8_t* sb = ar.scale[1] + (c >> 1);
+#pragma unroll 2
+  for (int s = s0; s < s1; ++s) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(ca + 16 * s);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(cb + 16 * s);
+    const uint32_t ka = scale_bf16x2(sa[2 * s]), kb = scale_bf16x2(sb[2 * s]);
+    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+    e2m1x8_to_h2x4(wa, a0, a1, a2, a3);
+    e2m1x8_to_h2x4(wb, b0, b1, b2, b3);
+    a0 = h2_to_bf2_scaled(a0, ka); a1 = h2_to_bf2_scaled(a1, ka);
+    a2 = h2_to_bf2_scaled(a2, ka); a3 = h2_to_bf2_scaled(a3, ka);
+    b0 = h2_to_bf2_scaled(b0, kb); b1 = h2_to_bf2_scaled(b1, kb);
+    b2 = h2_to_bf2_scaled(b2, kb); b3 = h2_to_bf2_scaled(b3, kb);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (bval[t]) z = *reinterpret_cast<const uint4*>(brow[t] + 32 * s + 8 * c);
+      mma16816_bf16(acc[t], a0, b0, a1, b1, z.x, z.y);
+      mma16816_bf16(acc[t], a2, b2, a3, b3, z.z, z.w);
+    }
+  }
+}
+
 // Split of a task's chunks over ks warps (at most 16 warp tasks in all, ks <= kmax):
 // the partial accumulators of part p go to part_buf[(task * ks + p) * 32 + lane]
 // and are summed in part order afterwards.
@@ -867,6 +900,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             }
           }
         }
+        if (first_round && stage_down && warp == 1) {
+          // down rows [r0, r1) of every used expert (shared first), for P2, issued right
+          // behind the gate/up rows (staging means one round, so the regions are disjoint):
+          // the batch leader arms the barrier, then one lane per expert issues its copy
+          uint8_t* dd = dyn + gu_alloc;
+          const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
+          for (int gbase = 0; gbase < ngr; gbase += 32) {
+            const int gi = gbase + lane;
+            if (gi < ngr && gi % per_b == 0) {
+              const int n_in = min(per_b, ngr - gi);
+              mbar_arrive_expect_tx(&tb->mbar[kMbDown + gi / per_b], uint32_t(n_in) * down_grp);
+            }
+            __syncwarp();
+            if (gi < ngr) {
+              // this CTA's row pairs of one expert's D block: one byte range
+              const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
+              bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
+                       uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
+            }
+          }
+        }
         __syncthreads();
         if (first_round) stamp0(li, kStP1Issued);
         if (first_round) publish_scales();
@@ -929,7 +983,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
               if (n < ns) {
                 const int slot = grp < 0 ? TK + n : perm[goff[grp] + n];
                 const float zi = tb->zinv[grp < 0 ? n : slot / K];
-                a.h[size_t(slot) * F + f] = silu_f(gg * acc[t][j] * zi) * (gu * acc[t][2 + j] * zi);
+                a.h[size_t(slot) * F + f] = __float2bfloat16_rn(silu_f(gg * acc[t][j] * zi) * (gu * acc[t][2 + j] * zi));
               }
             }
           }
@@ -982,27 +1036,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         if (first_round && nsr > 0) release_mb(cx, 1u << kMbShared);
         qa += nrow;
         first_round = false;
-      }
-      if (stage_down && warp == 1) {
-        // down rows [r0, r1) of every used expert (shared first), for P2, issued once
-        // the gate/up rows have landed so that they do not share the bandwidth: the
-        // batch leader arms the barrier, then one lane per expert issues its copy
-        uint8_t* dd = dyn + gu_alloc;
-        const int per_b = (ngr + kMbDownN - 1) / kMbDownN;
-        for (int gbase = 0; gbase < ngr; gbase += 32) {
-          const int gi = gbase + lane;
-          if (gi < ngr && gi % per_b == 0) {
-            const int n_in = min(per_b, ngr - gi);
-            mbar_arrive_expect_tx(&tb->mbar[kMbDown + gi / per_b], uint32_t(n_in) * down_grp);
-          }
-          __syncwarp();
-          if (gi < ngr) {
-            // this CTA's row pairs of one expert's D block: one byte range
-            const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
-            bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
-                     uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
-          }
-        }
       }
       if (tid == 0 && li + 1 < a.n_layers) {
         // next layer's D and R D into L2 while this layer finishes
@@ -1106,59 +1139,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             }
           }
         }
-        // h rows of the round's slots, scaled to f16 (row i = slot q = qa + i)
-        __half* hs = reinterpret_cast<__half*>(region + ob_bytes);
-        for (int i = warp; i < nq; i += kDecWarps) {
-          // one warp per slot: the row in registers (one round trip), max |h|, scaled f16 copy
-          const int q = qa + i;
-          const int slot = (q < T) ? TK + q : tb->perm[q - T];
-          const float4* src = reinterpret_cast<const float4*>(a.h + size_t(slot) * F);
-          __half2* dst = reinterpret_cast<__half2*>(hs + size_t(i) * F);
-          for (int k0 = 0; k0 < F / 4; k0 += 32 * 8) {
-            float4 v[8];
-            float m = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int k = k0 + lane + 32 * j;
-              v[j] = k < F / 4 ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              m = fmaxf(fmaxf(m, fmaxf(fabsf(v[j].x), fabsf(v[j].y))), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-            if (k0 == 0 && F / 4 <= 32 * 8) {
-              float sc, inv;
-              pow2_scale(m, &sc, &inv);
-              if (lane == 0) tb->hinv[slot] = inv;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int k = k0 + lane + 32 * j;
-                if (k < F / 4) {
-                  dst[2 * k] = __floats2half2_rn(v[j].x * sc, v[j].y * sc);
-                  dst[2 * k + 1] = __floats2half2_rn(v[j].z * sc, v[j].w * sc);
-                }
-              }
-            } else {
-              // rows longer than 1024: a second pass (max first over all chunks)
-              float mm = m;
-              for (int k1 = k0 + 32 * 8; k1 < F / 4; k1 += 32) {
-                for (int k = k1 + lane; k < min(k1 + 32, F / 4); k += 32) {
-                  const float4 w4 = src[k];
-                  mm = fmaxf(fmaxf(mm, fmaxf(fabsf(w4.x), fabsf(w4.y))), fmaxf(fabsf(w4.z), fabsf(w4.w)));
-                }
-              }
-              for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
-              float sc, inv;
-              pow2_scale(mm, &sc, &inv);
-              if (lane == 0) tb->hinv[slot] = inv;
-              for (int k = lane; k < F / 4; k += 32) {
-                const float4 w4 = src[k];
-                dst[2 * k] = __floats2half2_rn(w4.x * sc, w4.y * sc);
-                dst[2 * k + 1] = __floats2half2_rn(w4.z * sc, w4.w * sc);
-              }
-              break;
-            }
+        // h rows of the round's slots (bf16, row i = slot q = qa + i), copied as they are
+        __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(region + ob_bytes);
+        {
+          const int cpr = F / 8;                   // 16-byte pieces per row
+          for (int i = tid; i < nq * cpr; i += kDecThreads) {
+            const int r = i / cpr, k = i - r * cpr;
+            const int q = qa + r;
+            const int slot = (q < T) ? TK + q : tb->perm[q - T];
+            cp_async16(reinterpret_cast<uint4*>(hs + size_t(r) * F) + k,
+                       reinterpret_cast<const uint4*>(a.h + size_t(slot) * F) + k);
           }
+          cp_async_commit();
+          cp_async_wait_all();
         }
         __syncthreads();
         if (qa == 0) stamp0(li, kStP2Staged);
@@ -1170,7 +1163,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         const int ks2 = mma_ksplit(ntask2, 4);
         const int nchd = F / 32;
         float4* part_buf = reinterpret_cast<float4*>(act);
-        auto dtask = [&](int i, MmaRows& ar, const __half** brow, bool* bval, int& j, int& qs, int& ns,
+        auto dtask = [&](int i, MmaRows& ar, const __nv_bfloat16** brow, bool* bval, int& j, int& qs, int& ns,
                          int& rbase) {
           const int jj = i / rt;
           rbase = 16 * (i - jj * rt);
@@ -1195,7 +1188,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         };
         auto dfinish = [&](int i, float (*acc)[4]) {
           MmaRows ar;
-          const __half* brow[NTD];
+          const __nv_bfloat16* brow[NTD];
           bool bval[NTD];
           int j, qs, ns, rbase;
           dtask(i, ar, brow, bval, j, qs, ns, rbase);
@@ -1212,7 +1205,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
                 if (n < ns) {
                   const int q = qs + n;
                   const int slot = (q < T) ? TK + q : tb->perm[q - T];
-                  ob[size_t(slot) * nr + rho] = gd * tb->hinv[slot] * acc[t][2 * h + jx];
+                  ob[size_t(slot) * nr + rho] = gd * acc[t][2 * h + jx];
                 }
               }
             }
@@ -1221,7 +1214,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         for (int wt = warp; wt < ntask2 * ks2; wt += kDecWarps) {
           const int i = wt / ks2, part = wt - i * ks2;
           MmaRows ar;
-          const __half* brow[NTD];
+          const __nv_bfloat16* brow[NTD];
           bool bval[NTD];
           int j, qs, ns, rbase;
           dtask(i, ar, brow, bval, j, qs, ns, rbase);
@@ -1230,7 +1223,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           float acc[NTD][4];
 #pragma unroll
           for (int t = 0; t < NTD; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-          fp4_mma_chunks<NTD>(ar, brow, bval, nchd * part / ks2, nchd * (part + 1) / ks2, acc);
+          fp4_mma_chunks_bf16<NTD>(ar, brow, bval, nchd * part / ks2, nchd * (part + 1) / ks2, acc);
           if (ks2 == 1) {
             dfinish(i, acc);
           } else {

@@ -87,7 +87,7 @@ struct DecodeArgs {
   float* z;                 // [T][L]
   __half* zh;               // [T][L] f16 copy of z * 2^-e_t (the experts' input)
   float* logits;            // [T][E]
-  float* h;                 // [T*K + T][F]  routed slots, then the shared slot of each token
+  __nv_bfloat16* h;         // [T*K + T][F]  SwiGLU output: routed slots, then the shared slot of each token
   float* c;                 // [T][L]
   __nv_bfloat16* ybuf;      // [2][T][H] layer outputs inside a stack
   __nv_bfloat16* xbuf;      // [2][T][H] normalised layer inputs inside a stack
@@ -127,7 +127,6 @@ struct alignas(16) DecTables {
   float zsc[kDecodeMaxT], zinv[kDecodeMaxT];
   float4 gsc[kDecodeMaxT * kMaxTopK + 1];  // (gate, up, down, -) fp32 scales of group j:
                                          // j = 0 the shared expert, j >= 1 expert gexp[j - 1]
-  float hinv[kMaxSlots];                 // 2^e of each slot's f16 h copy
   float red[kDecWarps * kDecodeMaxT];
   float inv_rms[kDecodeMaxT];
   // per-round task tables

@@ -12,24 +12,6 @@ constexpr int kGgBBox = 64;       // rows of one B box (TMA)
 // result is rounded to bf16, far coarser than their error); v -> -inf gives -0.
 __device__ __forceinline__ float silu_gg(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-// f16x2 holding E2M1 values -> bf16x2 times a block scale, exact.  sc2 holds the
-// scale times 2^112 in both bf16 halves: moving the f16 bits right by 3 puts the
-// exponent field in bf16 position (the value becomes 2^-112 too small) and drops
-// three mantissa bits the E2M1 values never use; the sign bits are kept as they are.
-__device__ __forceinline__ uint32_t h2_to_bf2_scaled(uint32_t h, uint32_t sc2) {
-  const uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t),
-                             *reinterpret_cast<const __nv_bfloat162*>(&sc2));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// bf16x2 (both halves) of an E4M3 scale times 2^112.
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t e4m3) {
-  const float s = e4m3_to_f32(e4m3) * 5.192296858534828e33f;  // 2^112
-  __nv_bfloat162 r = __floats2bfloat162_rn(s, s);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }

@@ -307,6 +307,56 @@ edge0_status edge0_moe_profile_decode(void *handle, int enable);
 edge0_status edge0_moe_decode_phase_times(void *handle, float *us, int max, int *n_out);
 
 /*
+ * Expert residency tiering (decode forwards).  The pages' engine keeps the hot
+ * experts on the GPU and the rest of the expert library in host RAM ("Edge0-145B
+ * en local", introduction: VRAM / RAM / SSD tiers; "Edge0-145B hardware
+ * requirements", flags table: resident budget, memory-mapped experts).  Here the
+ * layer's routed records live in host memory and n_slots of them are cached in
+ * device memory:
+ *   - each decode forward reads a resident expert from its cache slot; after its
+ *     routing, the records of the chosen experts that are not resident are copied
+ *     from host memory (over the host link, by all CTAs, plain loads through the
+ *     device mapping) into a staging area, then the forward continues as usual;
+ *   - the kernel counts how often each expert is chosen; edge0_moe_tier_rebalance
+ *     moves the most-used experts into the slots (edge0_tier_plan, below).
+ * The result of a forward does not depend on which experts are resident.
+ *
+ * edge0_moe_tier_attach: host_records = the layer's n_experts records at the
+ *   handle's expert_stride, in pinned host memory mapped for device access
+ *   (cudaHostAlloc / cudaMallocHost with unified addressing, or cudaHostRegister
+ *   with the mapped flag), 256-byte aligned; caller-owned, valid until detach.
+ *   Allocates n_slots device slots (all empty at first) and a staging area of
+ *   16 * top_k records.  From then on the handle ignores desc.experts.  Requires a
+ *   handle created with max_tokens <= 16 (prefill forwards read every record from
+ *   device memory: UNSUPPORTED); a second attach is UNSUPPORTED.  Synchronises.
+ * edge0_moe_tier_place: puts expert slot_expert[k] (host int [n_slots], -1 =
+ *   empty, no expert twice) into slot k, copying the records on `stream` and
+ *   updating the table; synchronises `stream`.
+ * edge0_moe_tier_rebalance: reads the use counts (synchronises `stream`), places
+ *   the edge0_tier_plan choice and clears the counts.
+ * edge0_moe_tier_stats: out host [4]: tiered forwards, non-resident experts
+ *   copied, bytes copied from host memory, experts now resident.  Synchronises.
+ * edge0_moe_tier_detach: frees the slots and staging (synchronises); the handle
+ *   reads desc.experts again.
+ */
+edge0_status edge0_moe_tier_attach(void *handle, const void *host_records, int n_slots,
+                                   edge0_stream_t stream);
+edge0_status edge0_moe_tier_place(void *handle, const int *slot_expert, edge0_stream_t stream);
+edge0_status edge0_moe_tier_rebalance(void *handle, edge0_stream_t stream);
+edge0_status edge0_moe_tier_stats(void *handle, unsigned long long *out);
+edge0_status edge0_moe_tier_detach(void *handle);
+
+/*
+ * The residency policy (host code, no device access): the n_slots experts with the
+ * most uses (use host uint [n_experts]; ties to the lower index; an unused expert is
+ * never promoted) are resident in `next`.  An expert already in a slot (cur host int
+ * [n_slots], -1 empty) and still chosen keeps its slot; the other chosen experts fill
+ * the remaining slots in rank order; a slot left over keeps its current expert.
+ * Returns the number of slots whose expert changes, or -1 on bad arguments.
+ */
+int edge0_tier_plan(const unsigned int *use, int n_experts, int n_slots, const int *cur, int *next);
+
+/*
  * Failure-path check: launch one block on `stream` that waits on an mbarrier
  * no one arrives at, through the same bounded wait every kernel of the library
  * uses (limit 1 s of %globaltimer).  The wait runs out, sets the handle's

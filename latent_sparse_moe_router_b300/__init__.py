@@ -28,7 +28,9 @@ EXPORTED = (
     "edge0_moe_stack_forward", "edge0_moe_stack_forward_trace", "edge0_moe_get_error",
     "edge0_status_string", "edge0_moe_destroy", "edge0_moe_forward_noalloc", "edge0_gemm_bf16_tn",
     "edge0_moe_profile_stages", "edge0_moe_stage_times", "edge0_moe_debug_wait_probe",
-    "edge0_moe_profile_decode", "edge0_moe_decode_phase_times",
+    "edge0_moe_profile_decode", "edge0_moe_decode_phase_times", "edge0_moe_tier_attach",
+    "edge0_moe_tier_place", "edge0_moe_tier_rebalance", "edge0_moe_tier_stats", "edge0_moe_tier_detach",
+    "edge0_tier_plan",
 )
 
 EDGE0_PREFILL_STAGES = 10
@@ -89,6 +91,12 @@ def lib() -> ctypes.CDLL:
             "edge0_moe_stage_times": (i, [vp, vp, i, vp]),
             "edge0_moe_profile_decode": (i, [vp, i]),
             "edge0_moe_decode_phase_times": (i, [vp, vp, i, vp]),
+            "edge0_moe_tier_attach": (i, [vp, vp, i, vp]),
+            "edge0_moe_tier_place": (i, [vp, vp, vp]),
+            "edge0_moe_tier_rebalance": (i, [vp, vp]),
+            "edge0_moe_tier_stats": (i, [vp, vp]),
+            "edge0_moe_tier_detach": (i, [vp]),
+            "edge0_tier_plan": (i, [vp, i, i, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -266,6 +274,46 @@ def edge0_moe_decode_phase_times(handle, n_layers: int = 1):
     vals = [float(buf[i]) for i in range(n.value)]
     return [dict(zip(DECODE_PHASE_NAMES, vals[l * EDGE0_DECODE_PHASES:(l + 1) * EDGE0_DECODE_PHASES]))
             for l in range(n.value // EDGE0_DECODE_PHASES)]
+
+
+# ------------------------------------------------------------------ residency tiering
+def edge0_moe_tier_attach(handle, host_records, n_slots, stream=None):
+    """host_records: pinned host tensor (or address) of the layer's records at the handle's stride."""
+    _check(lib().edge0_moe_tier_attach(handle, _ptr(host_records), int(n_slots), _stream(stream)),
+           "edge0_moe_tier_attach")
+
+
+def edge0_moe_tier_place(handle, slot_expert, stream=None):
+    import numpy as np
+    arr = np.ascontiguousarray(slot_expert, dtype=np.int32)
+    _check(lib().edge0_moe_tier_place(handle, arr.ctypes.data, _stream(stream)), "edge0_moe_tier_place")
+
+
+def edge0_moe_tier_rebalance(handle, stream=None):
+    _check(lib().edge0_moe_tier_rebalance(handle, _stream(stream)), "edge0_moe_tier_rebalance")
+
+
+def edge0_moe_tier_stats(handle):
+    """dict(forwards, misses, host_bytes, resident)."""
+    buf = (ctypes.c_ulonglong * 4)()
+    _check(lib().edge0_moe_tier_stats(handle, ctypes.cast(buf, ctypes.c_void_p)), "edge0_moe_tier_stats")
+    return dict(forwards=buf[0], misses=buf[1], host_bytes=buf[2], resident=buf[3])
+
+
+def edge0_moe_tier_detach(handle):
+    _check(lib().edge0_moe_tier_detach(handle), "edge0_moe_tier_detach")
+
+
+def edge0_tier_plan(use, n_slots, cur):
+    """The residency policy on the host: returns (slot -> expert array, slots changed)."""
+    import numpy as np
+    use = np.ascontiguousarray(use, dtype=np.uint32)
+    cur = np.ascontiguousarray(cur, dtype=np.int32)
+    nxt = np.full(int(n_slots), -1, dtype=np.int32)
+    n = lib().edge0_tier_plan(use.ctypes.data, use.size, int(n_slots), cur.ctypes.data, nxt.ctypes.data)
+    if n < 0:
+        raise Edge0Error(EDGE0_ERR_INVALID_ARG, "edge0_tier_plan")
+    return nxt, n
 
 
 def edge0_moe_get_error(handle) -> int:

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -48,6 +49,19 @@ struct Handle {
   std::vector<LayerW> stack_tab;  // the layer table last uploaded to d_stack
   int last_T = 0;
   int last_path = 0;          // 0 none, 1 decode, 2 prefill
+  // residency tiering of the routed records (decode forwards; off by default)
+  bool tiered = false;
+  const uint8_t* host_records = nullptr;  // the caller's host records (pinned)
+  const uint8_t* host_dev = nullptr;      // their device alias (mapped host memory)
+  int n_slots = 0;
+  uint8_t* slots = nullptr;               // device [n_slots][stride]
+  uint8_t* staging = nullptr;             // device [kDecodeMaxT * top_k][stride]
+  char* tier_ws = nullptr;                // device: table, resident flags, use counts, stats
+  const uint8_t** d_table = nullptr;      // [E] record of each expert
+  uint8_t* d_resident = nullptr;          // [E]
+  unsigned int* d_use = nullptr;          // [E]
+  unsigned long long* d_stats = nullptr;  // [3]
+  std::vector<int> slot_expert;           // [n_slots] expert in each slot, -1 empty
   // decode phase profiling (off by default)
   bool dec_profile = false;
   unsigned long long* stamps = nullptr;   // [kStackMax][kStampSlots], own allocation
@@ -131,6 +145,11 @@ LayerW layer_of(const Handle* hd) {
   l.shared = static_cast<const uint8_t*>(hd->d.shared_expert);
   l.stride = hd->d.expert_stride;
   l.dnorm = hd->dnorm;
+  l.rec_table = hd->tiered ? hd->d_table : nullptr;
+  l.resident = hd->tiered ? hd->d_resident : nullptr;
+  l.staging = hd->tiered ? hd->staging : nullptr;
+  l.use = hd->tiered ? hd->d_use : nullptr;
+  l.tier_stats = hd->tiered ? hd->d_stats : nullptr;
   return l;
 }
 
@@ -505,6 +524,7 @@ edge0_status edge0_moe_forward(void* handle, const void* x, void* y, int T, edge
     return EDGE0_OK;
   }
   if (T > hd->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
+  if (hd->tiered) return EDGE0_ERR_UNSUPPORTED;   // prefill reads every record from device memory
   const edge0_status st = prefill_forward(hd->d, &hd->pf, hd->num_sms,
                                           static_cast<const __nv_bfloat16*>(x),
                                           static_cast<__nv_bfloat16*>(y), T, (cudaStream_t)stream);
@@ -566,7 +586,8 @@ static bool same_layers(const std::vector<LayerW>& a, const std::vector<LayerW>&
   for (size_t i = 0; i < a.size(); ++i)
     if (a[i].D != b[i].D || a[i].U != b[i].U || a[i].RD != b[i].RD || a[i].bias != b[i].bias ||
         a[i].experts != b[i].experts || a[i].shared != b[i].shared || a[i].stride != b[i].stride ||
-        a[i].dnorm != b[i].dnorm)
+        a[i].dnorm != b[i].dnorm || a[i].rec_table != b[i].rec_table || a[i].resident != b[i].resident ||
+        a[i].staging != b[i].staging || a[i].use != b[i].use || a[i].tier_stats != b[i].tier_stats)
       return false;
   return true;
 }
@@ -586,6 +607,8 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
   }
   if (T > kDecodeMaxT || n_layers > kStackMax) {
     if (trace_x || trace_y || trace_idx) return EDGE0_ERR_UNSUPPORTED;
+    for (int i = 0; i < n_layers; ++i)
+      if (static_cast<const Handle*>(handles[i])->tiered) return EDGE0_ERR_UNSUPPORTED;
     // chain: layer forward into the prefill scratch of handle 0, then the residual norm
     if (T > h0->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
     __nv_bfloat16* tmp = prefill_stack_scratch(&h0->pf);
@@ -722,6 +745,183 @@ edge0_status edge0_moe_get_error(void* handle) {
   return EDGE0_OK;
 }
 
+// ------------------------------------------------------------------ residency tiering
+int edge0_tier_plan(const unsigned int* use, int n_experts, int n_slots, const int* cur, int* next) {
+  if (!use || !cur || !next || n_experts < 0 || n_slots < 0 || n_slots > n_experts) return -1;
+  // the n_slots most-used experts (ties: lower index first); an expert not used at all
+  // is not promoted, so a slot it would take keeps its current expert
+  std::vector<int> order(n_experts);
+  for (int e = 0; e < n_experts; ++e) order[e] = e;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return use[a] > use[b]; });
+  std::vector<char> want(n_experts, 0), placed(n_experts, 0);
+  int n_want = 0;
+  for (int i = 0; i < n_slots && i < n_experts && use[order[i]] > 0; ++i) { want[order[i]] = 1; ++n_want; }
+  // experts already in a slot and still wanted stay where they are
+  for (int s = 0; s < n_slots; ++s) {
+    const int e = cur[s];
+    next[s] = (e >= 0 && e < n_experts && want[e] && !placed[e]) ? e : -1;
+    if (next[s] >= 0) placed[next[s]] = 1;
+  }
+  // the other wanted experts take the freed slots in rank order; slots left over keep
+  // their current expert if it is not placed elsewhere
+  int i = 0, changed = 0;
+  for (int s = 0; s < n_slots; ++s) {
+    if (next[s] >= 0) continue;
+    while (i < n_experts && !(want[order[i]] && !placed[order[i]])) ++i;
+    if (i < n_experts) {
+      next[s] = order[i];
+      placed[order[i]] = 1;
+    } else {
+      const int e = cur[s];
+      next[s] = (e >= 0 && e < n_experts && !placed[e]) ? e : -1;
+      if (next[s] >= 0) placed[next[s]] = 1;
+    }
+  }
+  for (int s = 0; s < n_slots; ++s) changed += next[s] != cur[s];
+  (void)n_want;
+  return changed;
+}
+
+static edge0_status tier_upload(Handle* hd, cudaStream_t s) {
+  const int E = hd->d.n_experts;
+  const size_t stride = hd->d.expert_stride;
+  std::vector<const uint8_t*> table(E);
+  std::vector<uint8_t> res(E, 0);
+  for (int e = 0; e < E; ++e) table[e] = hd->host_dev + size_t(e) * stride;
+  for (int k = 0; k < hd->n_slots; ++k) {
+    const int e = hd->slot_expert[k];
+    if (e >= 0) { table[e] = hd->slots + size_t(k) * stride; res[e] = 1; }
+  }
+  // pageable sources: staged before the calls return, stream-ordered on the device
+  if (cudaMemcpyAsync(hd->d_table, table.data(), sizeof(void*) * E, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(hd->d_resident, res.data(), E, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA;
+}
+
+edge0_status edge0_moe_tier_attach(void* handle, const void* host_records, int n_slots, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !host_records || n_slots < 0 || n_slots > hd->d.n_experts) return EDGE0_ERR_INVALID_ARG;
+  if (hd->tiered) return EDGE0_ERR_UNSUPPORTED;
+  if (hd->d.max_tokens > kDecodeMaxT) return EDGE0_ERR_UNSUPPORTED;   // tiering serves decode forwards
+  void* dev = nullptr;
+  if (cudaHostGetDevicePointer(&dev, const_cast<void*>(host_records), 0) != cudaSuccess || !dev) {
+    cudaGetLastError();
+    return EDGE0_ERR_INVALID_ARG;                    // not pinned host memory mapped for the device
+  }
+  if (!aligned(dev, 256)) return EDGE0_ERR_INVALID_ARG;
+  const int E = hd->d.n_experts;
+  const size_t stride = hd->d.expert_stride;
+  const size_t o_tab = 0, o_res = align_up(sizeof(void*) * E, 256), o_use = o_res + align_up(E, 256);
+  const size_t o_st = o_use + align_up(sizeof(unsigned int) * E, 256), ws = o_st + 256;
+  uint8_t* slots = nullptr;
+  uint8_t* staging = nullptr;
+  char* tws = nullptr;
+  if ((n_slots > 0 && cudaMalloc(&slots, size_t(n_slots) * stride) != cudaSuccess) ||
+      cudaMalloc(&staging, size_t(kDecodeMaxT) * hd->d.top_k * stride) != cudaSuccess ||
+      cudaMalloc(&tws, ws) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(slots); cudaFree(staging); cudaFree(tws);
+    return EDGE0_ERR_OOM;
+  }
+  hd->host_records = static_cast<const uint8_t*>(host_records);
+  hd->host_dev = static_cast<const uint8_t*>(dev);
+  hd->n_slots = n_slots;
+  hd->slots = slots;
+  hd->staging = staging;
+  hd->tier_ws = tws;
+  hd->d_table = reinterpret_cast<const uint8_t**>(tws + o_tab);
+  hd->d_resident = reinterpret_cast<uint8_t*>(tws + o_res);
+  hd->d_use = reinterpret_cast<unsigned int*>(tws + o_use);
+  hd->d_stats = reinterpret_cast<unsigned long long*>(tws + o_st);
+  hd->slot_expert.assign(n_slots, -1);
+  hd->tiered = true;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(hd->d_use, 0, sizeof(unsigned int) * E, s) != cudaSuccess ||
+      cudaMemsetAsync(hd->d_stats, 0, 256, s) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  return tier_upload(hd, s);
+}
+
+edge0_status edge0_moe_tier_place(void* handle, const int* slot_expert, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !slot_expert) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->tiered) return EDGE0_ERR_UNSUPPORTED;
+  const int E = hd->d.n_experts;
+  std::vector<char> seen(E, 0);
+  for (int k = 0; k < hd->n_slots; ++k) {
+    const int e = slot_expert[k];
+    if (e < -1 || e >= E || (e >= 0 && seen[e])) return EDGE0_ERR_INVALID_ARG;
+    if (e >= 0) seen[e] = 1;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t stride = hd->d.expert_stride;
+  // the table first points every leaving expert back at host memory, then the slots
+  // are refilled (stream order: forwards already enqueued finish with the old slots)
+  std::vector<int> cur = hd->slot_expert;
+  for (int k = 0; k < hd->n_slots; ++k)
+    if (cur[k] != slot_expert[k]) hd->slot_expert[k] = -1;
+  edge0_status st = tier_upload(hd, s);
+  if (st != EDGE0_OK) return st;
+  for (int k = 0; k < hd->n_slots; ++k) {
+    const int e = slot_expert[k];
+    if (e >= 0 && cur[k] != e &&
+        cudaMemcpyAsync(hd->slots + size_t(k) * stride, hd->host_records + size_t(e) * stride, stride,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return EDGE0_ERR_CUDA;
+    hd->slot_expert[k] = e;
+  }
+  return tier_upload(hd, s);
+}
+
+edge0_status edge0_moe_tier_rebalance(void* handle, edge0_stream_t stream) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->tiered) return EDGE0_ERR_UNSUPPORTED;
+  const int E = hd->d.n_experts;
+  cudaStream_t s = (cudaStream_t)stream;
+  std::vector<unsigned int> use(E);
+  if (cudaMemcpyAsync(use.data(), hd->d_use, sizeof(unsigned int) * E, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  std::vector<int> next(hd->n_slots);
+  if (edge0_tier_plan(use.data(), E, hd->n_slots, hd->slot_expert.data(), next.data()) < 0) return EDGE0_ERR_CUDA;
+  const edge0_status st = edge0_moe_tier_place(handle, next.data(), stream);
+  if (st != EDGE0_OK) return st;
+  return cuda_status(cudaMemsetAsync(hd->d_use, 0, sizeof(unsigned int) * E, s));
+}
+
+edge0_status edge0_moe_tier_stats(void* handle, unsigned long long* out) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd || !out) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->tiered) return EDGE0_ERR_UNSUPPORTED;
+  unsigned long long st[3];
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(st, hd->d_stats, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EDGE0_ERR_CUDA;
+  int resident = 0;
+  for (int e : hd->slot_expert) resident += e >= 0;
+  out[0] = st[0]; out[1] = st[1]; out[2] = st[2]; out[3] = (unsigned long long)resident;
+  return EDGE0_OK;
+}
+
+edge0_status edge0_moe_tier_detach(void* handle) {
+  Handle* hd = static_cast<Handle*>(handle);
+  if (!hd) return EDGE0_ERR_INVALID_ARG;
+  if (!hd->tiered) return EDGE0_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return EDGE0_ERR_CUDA;
+  cudaFree(hd->slots);
+  cudaFree(hd->staging);
+  cudaFree(hd->tier_ws);
+  hd->tiered = false;
+  hd->slots = hd->staging = nullptr;
+  hd->tier_ws = nullptr;
+  hd->d_table = nullptr; hd->d_resident = nullptr; hd->d_use = nullptr; hd->d_stats = nullptr;
+  hd->slot_expert.clear();
+  hd->n_slots = 0;
+  return EDGE0_OK;
+}
+
 const char* edge0_status_string(edge0_status s) {
   switch (s) {
     case EDGE0_OK: return "ok";
@@ -740,6 +940,11 @@ void edge0_moe_destroy(void* handle) {
   cudaDeviceSynchronize();
   prefill_destroy(&hd->pf);
   if (hd->stamps) cudaFree(hd->stamps);
+  if (hd->tiered) {
+    cudaFree(hd->slots);
+    cudaFree(hd->staging);
+    cudaFree(hd->tier_ws);
+  }
   cudaFree(hd->ws);
   delete hd;
 }

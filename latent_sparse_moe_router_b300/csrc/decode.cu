@@ -809,6 +809,53 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       __syncthreads();
       stamp0(li, kStRouted);
       const int nu = tb->nu;
+      // the record of every distinct expert: its place in the layer's array, or with
+      // residency tiering its device slot or, for an expert not resident, a staging
+      // record that all CTAs first fill from host memory (one more grid barrier)
+      if (!lw.rec_table) {
+        for (int g = tid; g < nu; g += kDecThreads) tb->gptr[g] = lw.experts + size_t(tb->gexp[g]) * lw.stride;
+        __syncthreads();
+      } else {
+        if (warp == 0) {
+          int base = 0;
+          for (int g0 = 0; g0 < nu; g0 += 32) {
+            const int g = g0 + lane;
+            const bool miss = g < nu && !lw.resident[tb->gexp[g]];
+            const unsigned bal = __ballot_sync(kFull, miss);
+            const int m = base + __popc(bal & ((1u << lane) - 1u));
+            if (g < nu) tb->gmiss[g] = miss ? m : -1;
+            if (miss) tb->mgrp[m] = g;
+            base += __popc(bal);
+          }
+          if (lane == 0) tb->n_miss = base;
+        }
+        __syncthreads();
+        const int n_miss = tb->n_miss;
+        if (n_miss > 0) {
+          // records [0, n_miss) of the staging area from host memory, 16 bytes per
+          // thread-step over the whole grid (plain loads through the device mapping)
+          const size_t per = lw.stride / 16, total = size_t(n_miss) * per;
+          for (size_t i = size_t(bid) * kDecThreads + tid; i < total; i += size_t(G) * kDecThreads) {
+            const int m = int(i / per);
+            const uint4* src = reinterpret_cast<const uint4*>(lw.rec_table[tb->gexp[tb->mgrp[m]]]) + (i - size_t(m) * per);
+            reinterpret_cast<uint4*>(lw.staging)[i] = *src;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          if (!grid_sync(a.bar, a.err)) return;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        for (int g = tid; g < nu; g += kDecThreads)
+          tb->gptr[g] = tb->gmiss[g] >= 0 ? lw.staging + size_t(tb->gmiss[g]) * lw.stride : lw.rec_table[tb->gexp[g]];
+        if (bid == 0) {
+          for (int g = tid; g < nu; g += kDecThreads) atomicAdd(&lw.use[tb->gexp[g]], unsigned(tb->goff[g + 1] - tb->goff[g]));
+          if (tid == 0) {
+            atomicAdd(&lw.tier_stats[0], 1ull);
+            atomicAdd(&lw.tier_stats[1], (unsigned long long)n_miss);
+            atomicAdd(&lw.tier_stats[2], (unsigned long long)n_miss * lw.stride);
+          }
+        }
+        __syncthreads();
+      }
       // routed gate/up rows: q in [q0, q1) of nu * F (group-major), in whole tasks of 8
       const long ntq = long(nu) * (F / 8);
       const int q0 = 8 * int(ntq * bid / G), q1 = 8 * int(ntq * (bid + 1) / G);
@@ -843,14 +890,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           if (e < E) a.counts[e] = cnt;
         }
       }
-      const uint8_t* experts = lw.experts;
-      const size_t stride = lw.stride;
       // fp32 scales of the selected records, one per lane of warps 8..15: the loads
       // stay in flight across the next barrier; stored and announced on kMbScale after it
       float3 rsc = make_float3(0.f, 0.f, 0.f);
       const int sj = tid - kScaleWarp0 * 32;            // routed group of this lane
       if (sj >= 0 && sj < nu) {
-        const float* gs = reinterpret_cast<const float*>(experts + size_t(tb->gexp[sj]) * stride + rec_body);
+        const float* gs = reinterpret_cast<const float*>(tb->gptr[sj] + rec_body);
         const float2 gu = *reinterpret_cast<const float2*>(gs);
         rsc = make_float3(gu.x, gu.y, gs[2]);
       }
@@ -893,7 +938,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
               // rows of one expert are one byte range of its GU block
               const int g = q / F, fa = q % F;
               const int n = min(s1, (g + 1) * F) - q;
-              const uint8_t* rec = experts + size_t(gexp[g]) * stride;
+              const uint8_t* rec = tb->gptr[g];
               bulk_g2s(dyn + off, rec + size_t(fa) * gu_row, uint32_t(n) * gu_row, &tb->mbar[kMbRound + b]);
               off += uint32_t(n) * gu_row;
               q += n;
@@ -915,7 +960,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             __syncwarp();
             if (gi < ngr) {
               // this CTA's row pairs of one expert's D block: one byte range
-              const uint8_t* rec = (gi == 0) ? lw.shared : experts + size_t(gexp[gi - 1]) * stride;
+              const uint8_t* rec = (gi == 0) ? lw.shared : tb->gptr[gi - 1];
               bulk_g2s(dd + size_t(gi) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
                        uint32_t(down_grp), &tb->mbar[kMbDown + gi / per_b]);
             }
@@ -1132,7 +1177,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             mbar_arrive_expect_tx(&tb->mbar[kMbRound + b], uint32_t(gb - ga) * down_grp);
             for (int jj = ga; jj < gb; ++jj) {
               const int j = ja + jj;
-              const uint8_t* rec = (j == 0) ? lw.shared : lw.experts + size_t(tb->gexp[j - 1]) * lw.stride;
+              const uint8_t* rec = (j == 0) ? lw.shared : tb->gptr[j - 1];
               bulk_g2s(wbase + size_t(jj) * down_grp, rec + rec_dblk + size_t(r0 / 2) * d_pair,
                        uint32_t(down_grp), &tb->mbar[kMbRound + b]);
               tb->task_aux[jj] = b;

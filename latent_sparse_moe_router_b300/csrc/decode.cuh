@@ -71,6 +71,14 @@ struct LayerW {
   const uint8_t* shared;    // 1 record
   unsigned long long stride;
   float dnorm;              // max_r sum_h |D[r][h]|: bounds |z| / max|x|
+  // residency tiering (all null when the layer's records are all in device memory):
+  // record e is at rec_table[e], in device memory when resident[e] != 0, else in
+  // host memory mapped into the device address space
+  const uint8_t* const* rec_table;
+  const uint8_t* resident;
+  uint8_t* staging;         // device, >= T K records at `stride`: this forward's misses
+  unsigned int* use;        // [E] selections per expert (the residency policy reads them)
+  unsigned long long* tier_stats;  // [0] forwards, [1] misses, [2] bytes read from host memory
 };
 
 struct DecodeArgs {
@@ -116,6 +124,10 @@ struct alignas(16) DecTables {
   int perm[kDecodeMaxT * kMaxTopK];     // grouped position -> slot
   int posn[kDecodeMaxT * kMaxTopK];     // slot -> grouped position
   int gexp[kDecodeMaxT * kMaxTopK];     // distinct experts, ascending
+  const uint8_t* gptr[kDecodeMaxT * kMaxTopK];  // record of each distinct expert for this forward
+  int gmiss[kDecodeMaxT * kMaxTopK];    // tiering: staging index of a non-resident expert, else -1
+  int mgrp[kDecodeMaxT * kMaxTopK];     // tiering: group of staging record m
+  int n_miss;                            // tiering: non-resident experts of this forward
   int goff[kDecodeMaxT * kMaxTopK + 1]; // group g = perm[goff[g] .. goff[g+1])
   int nu;                                // number of distinct experts
   int stuck;                             // bit b: a wait on mbar[b] ran out

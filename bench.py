@@ -770,6 +770,78 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
                 stages=stages, layer_tok_s=value * n_layers, jobs=jobs)
 
 
+def run_tiered(args, rank, world, local, n_slots=128, n_warm=64, n_tok=256):
+    """Expert residency tiering: one Edge0-145B layer with Zipf(1.1) routing, its 512
+    records in pinned host memory and n_slots of them cached in device memory after a
+    warm-up and a rebalance; T=1 forwards timed back to back against the handle that
+    reads every record from device memory, and the host link's copy bandwidth."""
+    import numpy as np
+    import torch
+    import synth
+    import latent_sparse_moe_router_b300 as ext
+    from synth import device
+    torch.cuda.set_device(local)
+    spec = synth.LayerSpec(seed=3, layer=0, latent=1792, zipf=1.1)
+    dl = device.DeviceLayer(synth.make_layer(spec), max_tokens=16)
+    host = torch.empty(dl.records.numel(), dtype=torch.uint8, pin_memory=True)
+    host.copy_(dl.records.cpu())
+    tl = ext.MoELayer(hidden=spec.hidden, latent=spec.latent, n_experts=spec.n_experts, top_k=spec.top_k,
+                      ffn=spec.ffn, max_tokens=16, D=dl.D, U=dl.U, router=dl.R, router_bias=dl.bias,
+                      experts=dl.records, expert_stride=dl.stride, shared_expert=dl.shared)
+    stream = torch.cuda.Stream()
+    ext.edge0_moe_tier_attach(tl.handle, host, n_slots, stream)
+    xs = [device.bf16_tensor(synth.tokens_bf16(9000 + rank * 1000 + j, 1, HIDDEN)) for j in range(n_warm + n_tok)]
+    ys = [torch.empty_like(x) for x in xs]
+    for j in range(n_warm):
+        ext.edge0_moe_forward(tl.handle, xs[j], ys[j], 1, stream)
+    ext.edge0_moe_tier_rebalance(tl.handle, stream)
+    st0 = ext.edge0_moe_tier_stats(tl.handle)
+
+    def timed(handle):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        e0.record(stream)
+        for j in range(n_warm, n_warm + n_tok):
+            ext.edge0_moe_forward(handle, xs[j], ys[j], 1, stream)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    t_tier = timed(tl.handle)
+    st1 = ext.edge0_moe_tier_stats(tl.handle)
+    y_tier = [device.bf16_bits(ys[j]) for j in range(n_warm, n_warm + 8)]
+    t_res = timed(dl.handle)
+    same = all(np.array_equal(a, device.bf16_bits(ys[n_warm + i])) for i, a in enumerate(y_tier))
+    # the host link: one 256 MB pinned -> device copy
+    src = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    dst.copy_(src, non_blocking=True)
+    e1.record()
+    e1.synchronize()
+    link_gbs = (256 << 20) / (e0.elapsed_time(e1) / 1e3) / 1e9
+    misses = st1["misses"] - st0["misses"]
+    hbytes = st1["host_bytes"] - st0["host_bytes"]
+    out = {"workload": "layer145b_t1_zipf_tiered",
+           "desc": "one Edge0-145B layer, Zipf(1.1) routing, records in pinned host memory, "
+                   f"{n_slots} of 512 cached in device memory after {n_warm} warm-up tokens and a rebalance",
+           "value": round(n_tok / t_tier, 1), "unit": "tok/s", "tokens": n_tok,
+           "resident_value": round(n_tok / t_res, 1), "n_slots": n_slots, "resident_experts": st1["resident"],
+           "misses_per_token": round(misses / n_tok, 3), "routed_per_token": spec.top_k,
+           "host_bytes_per_token": round(hbytes / n_tok), "host_read_gbs": round(hbytes / t_tier / 1e9, 2),
+           "host_link_copy_gbs": round(link_gbs, 1),
+           "bitwise_equal_to_resident": bool(same),
+           "note": "host_read_gbs = bytes copied from host memory over the whole timed interval; "
+                   "host_link_copy_gbs = one pinned 256 MB host-to-device copy"}
+    assert ext.edge0_moe_get_error(tl.handle) == ext.EDGE0_OK
+    tl.close()
+    dl.close()
+    return out
+
+
 def config_of(name, wl, world):
     if wl["kind"] == "prefill":
         l2 = (f"inputs larger than L2: x {wl['T'] * HIDDEN * 2 / 1e6:.0f} MB per layer input, "
@@ -862,6 +934,9 @@ def main():
             extra[key] = sub_line(name, o, world)
             if o.get("sweep"):
                 extra["verify_sweep"] = {"workload": name, "layer": "Edge0-145B", "points": o["sweep"]}
+        if not args.only or "tiered" in args.only.split(","):
+            torch.cuda.empty_cache()
+            extra["tiered_decode"] = run_tiered(args, rank, world, local)
     if rank != 0:
         return
     if pool is not None:

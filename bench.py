@@ -842,6 +842,48 @@ def run_tiered(args, rank, world, local, n_slots=128, n_warm=64, n_tok=256):
     return out
 
 
+def run_noalloc(args, rank, world, local, n=40):
+    """The allocation-free decode entry against the handle forward on one Edge0-145B
+    layer at T=1: the difference is what each of its calls adds (R D and the |z|
+    bound recomputed into the library's static scratch)."""
+    import numpy as np
+    import torch
+    import synth
+    import latent_sparse_moe_router_b300 as ext
+    from synth import device
+    torch.cuda.set_device(local)
+    spec = synth.LayerSpec(seed=0, layer=0, latent=1792)
+    dl = device.DeviceLayer(synth.make_layer(spec), max_tokens=16)
+    x = device.bf16_tensor(synth.tokens_bf16(5, 1, HIDDEN))
+    y0, y1 = torch.empty_like(x), torch.empty_like(x)
+    s = torch.cuda.Stream()
+
+    def na():
+        ext.edge0_moe_forward_noalloc(spec.hidden, spec.latent, spec.n_experts, spec.top_k, spec.ffn, dl.D, dl.U,
+                                      dl.R, dl.bias, dl.records, dl.stride, dl.shared, x, y1, 1, None, s)
+
+    def hf():
+        ext.edge0_moe_forward(dl.handle, x, y0, 1, s)
+
+    out = {}
+    for name, f in (("noalloc_us", na), ("handle_us", hf)):
+        for _ in range(5):
+            f()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(n):
+            f()
+        e1.record(s)
+        e1.synchronize()
+        out[name] = round(e0.elapsed_time(e1) * 1e3 / n, 2)
+    out["same_output"] = bool(np.array_equal(device.bf16_bits(y0), device.bf16_bits(y1)))
+    out["note"] = ("one Edge0-145B layer at T=1, the same token and weights, calls back to back on one stream "
+                   "(same L2 state for both); the difference is the per-call R D and |z|-bound recomputation")
+    dl.close()
+    return out
+
+
 def config_of(name, wl, world):
     if wl["kind"] == "prefill":
         l2 = (f"inputs larger than L2: x {wl['T'] * HIDDEN * 2 / 1e6:.0f} MB per layer input, "
@@ -937,6 +979,8 @@ def main():
         if not args.only or "tiered" in args.only.split(","):
             torch.cuda.empty_cache()
             extra["tiered_decode"] = run_tiered(args, rank, world, local)
+        if not args.only or "noalloc" in args.only.split(","):
+            extra["noalloc_decode"] = run_noalloc(args, rank, world, local)
     if rank != 0:
         return
     if pool is not None:

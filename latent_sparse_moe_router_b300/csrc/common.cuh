@@ -173,6 +173,12 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
   unsigned int v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -189,10 +195,12 @@ __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
     unsigned long long tk;
     asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(tk) : "l"(&bar->ticket) : "memory");
     const unsigned long long target = (tk / gridDim.x + 1) * gridDim.x;
-    if (ld_relaxed_u64(&bar->ticket) < target) {
+    // acquire loads: the load that sees the round complete orders this CTA after
+    // every other CTA's release (its arrival); the __syncthreads below passes that on
+    if (ld_acquire_u64(&bar->ticket) < target) {
       const unsigned long long t0 = globaltimer_ns();
       unsigned int spins = 0;
-      while (ld_relaxed_u64(&bar->ticket) < target) {
+      while (ld_acquire_u64(&bar->ticket) < target) {
         if ((++spins & 31u) == 0) {
           if (ld_relaxed_u32(&bar->abort)) { ok = 0; break; }
           if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -204,7 +212,6 @@ __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
         }
       }
     }
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     s_ok = ok;
   }
   __syncthreads();

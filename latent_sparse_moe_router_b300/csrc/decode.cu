@@ -646,6 +646,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   const int j0 = int(long(bid) * H / G), j1 = int(long(bid + 1) * H / G);      // hidden rows
   const int nr = r1 - r0, nsr = f1 - f0;
 
+  // launched as a programmatic dependent of the preceding kernel on the stream: its
+  // results (this launch's input, the workspace) are complete from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // a launch after one whose wait ran out finds the grid barrier mid-round (reset
   // by edge0_moe_get_error): it does no work and leaves the error word set
   if (ld_relaxed_u32(&a.bar->abort)) {
@@ -1320,6 +1323,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     if (!grid_sync(a.bar, a.err)) return;
     stamp0(li, kStBar3);
     // ================================================================ P3: y = U c
+    // the next kernel on the stream may be scheduled from here (it waits for this
+    // grid's completion before reading anything)
+    if (last) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
       for (int i = tid; i < T * L / 4; i += kDecThreads)
         reinterpret_cast<float4*>(act)[i] = reinterpret_cast<const float4*>(a.c)[i];
@@ -1389,12 +1395,24 @@ static cudaError_t launch_tb(const DecodeArgs& a, int grid, int smem, cudaStream
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<TB>, a);
+  // programmatic serialization lets the launch overlap the tail of the preceding
+  // kernel; where the runtime refuses it with a cooperative launch, launch without
+  static int pdl = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_kernel<TB>, a);
+  if (e != cudaSuccess && pdl) {
+    cudaGetLastError();
+    pdl = 0;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, moe_decode_kernel<TB>, a);
+  }
+  return e;
 }
 
 template <int TB>

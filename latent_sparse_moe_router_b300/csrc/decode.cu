@@ -877,14 +877,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         tb->down_staged = stage_down ? 1 : 0;
         tb->down_off = gu_alloc;
       }
-      if (bid == 0 && a.trace_idx)
-        for (int s = tid; s < TK; s += kDecThreads) a.trace_idx[size_t(li) * TK + s] = tb->idx[s];
-      // bid 0 publishes the routing of the last layer
-      if (bid == 0 && last) {
-        for (int s = tid; s < TK; s += kDecThreads) {
+      // the routing tables for the caller (trace, and the last layer's copy read by
+      // edge0_moe_debug_routing), written after the expert copies are issued and
+      // spread over the CTAs: each writes a slice
+      auto publish_routing = [&]() {
+        const int s0 = int(long(TK) * bid / G), s1 = int(long(TK) * (bid + 1) / G);
+        if (a.trace_idx)
+          for (int s = s0 + tid; s < s1; s += kDecThreads) a.trace_idx[size_t(li) * TK + s] = tb->idx[s];
+        if (!last) return;
+        for (int s = s0 + tid; s < s1; s += kDecThreads) {
           a.idx[s] = tb->idx[s]; a.w[s] = tb->w[s]; a.perm[s] = tb->perm[s]; a.pos[s] = tb->posn[s];
         }
-        for (int e = tid; e <= E; e += kDecThreads) {
+        const int ea = int(long(E + 1) * bid / G), eb = int(long(E + 1) * (bid + 1) / G);
+        for (int e = ea + tid; e < eb; e += kDecThreads) {
           int off = TK, cnt = 0;
           for (int g = 0; g < nu; ++g) {
             if (tb->gexp[g] >= e) { off = tb->goff[g]; if (tb->gexp[g] == e) cnt = tb->goff[g + 1] - tb->goff[g]; break; }
@@ -892,7 +897,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           a.offsets[e] = off;
           if (e < E) a.counts[e] = cnt;
         }
-      }
+      };
       // fp32 scales of the selected records, one per lane of warps 8..15: the loads
       // stay in flight across the next barrier; stored and announced on kMbScale after it
       float3 rsc = make_float3(0.f, 0.f, 0.f);
@@ -910,7 +915,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
       };
       const float sgg = tb->gsc[0].x, sgu = tb->gsc[0].y;
-      const int* gexp = tb->gexp;
       const int* goff = tb->goff;
       const int* perm = tb->perm;
       constexpr int NT = TB > 8 ? 2 : 1;                // 8-token MMA tiles
@@ -972,6 +976,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         __syncthreads();
         if (first_round) stamp0(li, kStP1Issued);
         if (first_round) publish_scales();
+        if (first_round) publish_routing();
         // tasks of 8 row pairs: A rows 0-7 the gate rows, 8-15 the up rows of the same
         // f, so that each thread holds gate and up of (f, token) for the SwiGLU
         const int ntr = nrow / 8;

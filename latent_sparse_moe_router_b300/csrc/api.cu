@@ -94,41 +94,55 @@ __host__ __device__ inline size_t record_src(size_t o, size_t L, size_t F, bool*
   return 2 * F * (L / 16) + pr * (F / 8) + (w - F);
 }
 
-// Shared-memory plan of the decode kernel for token bucket TB.
+// Shared-memory plan of the decode kernel for a bucket of TB tokens: the tables, the
+// shared expert's gate/up rows, the phase-local arrays, then the ring area (to the end).
 void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
-  const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts, F = hd->d.ffn;
+  const int H = hd->d.hidden, L = hd->d.latent, F = hd->d.ffn, K = hd->d.top_k, G = hd->num_sms;
+  const int NT = TB > 8 ? 2 : 1;
   size_t off = decode_tables_bytes();
-  // x (P0 only) and the fp32 activations (P1, P3) are never live together
-  size_t act = TB * (size_t)(L > E ? L : E) * 4;
-  // P0 of a stacked layer: x [T][H] bf16 and the norm's group sums [T][H/8] fp32
-  if (TB * (size_t)H * 5 / 2 > act) act = TB * (size_t)H * 5 / 2;
-  const size_t cand = TB * (size_t)E * 4 + size_t(kDecWarps) * kTopkCand * 8;   // logits + top-k candidates
-  if (cand > act) act = cand;
-  a.off_xs = (int)off;
-  a.off_act = (int)off;
-  a.act_bytes = (int)align_up(act, 128);
-  off += a.act_bytes;
-  a.off_zh = (int)off;
-  off += align_up(TB * (size_t)L * 2, 128);
-  const int shared_rows = (F + hd->num_sms - 1) / hd->num_sms;
+  const int shared_rows = (F + G - 1) / G;
   a.off_sh = (int)off;
-  a.sh_bytes = (int)align_up((size_t)shared_rows * 2 * (L / 2 + L / 16), 128);
+  a.sh_bytes = (int)align_up((size_t)shared_rows * pitch_gu_row(L), 128);
   off += a.sh_bytes;
-  a.off_res = (int)off;
-  a.res_rows = 0;
-  off = align_up(off, 1024);
-  a.off_dyn = (int)off;
-  a.dyn_bytes = (int)((hd->smem_total - off) & ~size_t(1023));
+  // x [T][H + pad] (P0); zh [T][L + pad] and the partial sums (P1); the per-slot down
+  // outputs (P2); c [T][L + pad] (P3)
+  const int nr_max = 2 * ((L / 2 + G - 1) / G);
+  const size_t xs = size_t(TB) * (H + kPadElems) * 2;
+  const size_t zs = align_up(size_t(TB) * (L + kPadElems) * 2, 128);
+  const size_t p1 = zs + size_t(kPartCap) * 32 * NT * 16;
+  const size_t p2 = size_t(TB) * (K + 1) * nr_max * 4;
+  size_t ar = xs > p1 ? xs : p1;
+  if (p2 > ar) ar = p2;
+  a.off_a = (int)off;
+  a.a_bytes = (int)align_up(ar, 128);
+  off = align_up(off + a.a_bytes, 1024);
+  a.off_ring = (int)off;
+  a.ring_bytes = hd->smem_total > (int)off ? (int)((hd->smem_total - off) & ~size_t(127)) : 0;
+  const int unit1 = (int)align_up(size_t(8) * pitch_gu_row(L), 128);
+  int S = a.ring_bytes / unit1;
+  if (S > kRingMax) S = kRingMax;
+  a.ring_slots = S;
+  a.slot_bytes = S > 0 ? (a.ring_bytes / S) & ~127 : 0;
 }
 
-// Every decode bucket leaves room in the staged-weight region for at least an fp32
-// R D row pair and a gate/up row pair (the smallest unit each phase stages).
+// Every decode bucket's plan holds what each phase stages: at least two ring slots, the
+// P0 rows of a CTA, the logits and top-k candidates, a P2 unit of one expert's down
+// rows and one h row, and the U rows of P3.
 bool decode_fits(const Handle* hd) {
+  const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts, F = hd->d.ffn, G = hd->num_sms;
+  const int ne = (E + G - 1) / G, nr = 2 * ((L / 2 + G - 1) / G), nsr = (F + G - 1) / G, nur = (H + G - 1) / G;
+  if ((ne + 7) / 8 + (nr + 15) / 16 > kP0Tiles || ne + nr > 32 || nsr > 32 || (nur + 15) / 16 > kDecWarps) return false;
   for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
     DecodeArgs a;
     decode_plan(hd, TB, a);
-    const int need = 4 * hd->d.hidden * 2 + 8192;
-    if (a.dyn_bytes < need) return false;
+    const int NT = TB > 8 ? 2 : 1;
+    const size_t ring = (size_t)a.ring_bytes;
+    if (a.ring_slots < 2 || (nsr + 7) / 8 > a.ring_slots) return false;
+    if (size_t(ne) * pitch_f32_row(H) + size_t(nr) * pitch_bf16_row(H) > ring) return false;
+    if (size_t(kDecWarps) * 32 * NT * 16 > ring) return false;
+    if (size_t(TB) * E * 4 + size_t(kDecWarps) * kTopkCand * 8 > ring) return false;
+    if (size_t(nr / 2) * (9 * F / 8) + size_t(F) * 2 > (size_t)a.slot_bytes) return false;
+    if (size_t(nur) * pitch_bf16_row(L) > ring) return false;
   }
   return true;
 }

@@ -4,21 +4,23 @@
 // hardware requirements", section "Edge0-145B latent MoE architecture"):
 //   z = D x;  l = R z + b;  top-k + renormalised softmax;  o_e = W_d (silu(W_g z) * W_up z);
 //   c = o_shared + sum_k w_k o_k;  y = U c.
-// At T <= 16 every step is a GEMV bound by HBM bandwidth and each step needs all of
-// the previous one.  One CTA per SM runs four phases separated by software grid
-// barriers (the minimum for this dependency chain):
+// At T <= 16 every step is a matrix-vector product bound by HBM bandwidth and each
+// step needs all of the previous one.  One CTA per SM runs four phases separated by
+// software grid barriers (the minimum for this dependency chain):
 //   P0  z = D x and l = (R D) x + b     R D is folded once, in fp32, when the handle
 //                                        is created, so the router needs no phase of its own
-//   P1  top-k + weights + permutation   redundantly per CTA, in shared memory, while
-//       shared-expert gate/up           other warps run the shared expert (staged in P0)
-//       routed gate/up -> h             rows of the union of the selected experts;
-//                                        the down rows of P2 are staged at the same time
-//   P2  down projections + combine -> c (U rows of P3 staged at the start)
-//   P3  y = U c
-// Weights move with bulk copies (cp.async.bulk) into shared memory, completion on
-// mbarriers, one phase ahead where shared memory allows; NVFP4 is dequantised in
-// registers.  A stack of layers (residual + RMSNorm between them) runs in the same
-// launch, each layer prefetching the next one's D and R D into L2.
+//   P1  top-k + weights + permutation   redundantly per CTA, in shared memory
+//       gate/up -> h                    rows of the union of the selected experts and
+//                                        of the shared expert (staged during P0)
+//   P2  down projections + combine -> c (the down rows are fetched during P1)
+//   P3  y = U c                          (U rows fetched at the end of P2)
+// Every product runs on m16n8k16 mma.sync with the tokens on N.  The expert rows move
+// through a ring of shared-memory slots: each slot is one bulk-copied unit of work
+// (8 gate/up row pairs in P1, a few experts' down rows and their h rows in P2), the
+// warp that finishes the last part of a unit refills its slot with the unit S places
+// further on, and units of P1 and P2 form one stream, so that the first down units are
+// in flight before P1 ends.  A stack of layers (residual + RMSNorm between them) runs
+// in the same launch, each layer prefetching the next one's D and R D into L2.
 #pragma once
 
 #include "common.cuh"
@@ -30,18 +32,25 @@ constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxTopK = 16;
 constexpr int kDecodeMaxT = 16;
 constexpr int kMaxSlots = kDecodeMaxT * (kMaxTopK + 1);
-constexpr int kNumMbar = 16;
+constexpr int kNumMbar = 20;
 constexpr int kTopkCand = 64;   // candidates per warp of the top-k (shared memory)
 // mbarrier roles
-constexpr int kMbRound = 0;      // 0..7: batches of the current round
-constexpr int kMbRounds = 8;
-constexpr int kMbShared = 8;     // shared-expert gate/up rows (P0 -> P1)
-constexpr int kMbDown = 9;       // 9..12: down rows staged in P1 for P2
-constexpr int kMbDownN = 4;
-constexpr int kMbU = 13;         // U rows staged in P2 for P3
-constexpr int kMbScale = 14;     // fp32 scales of the selected records (P1 -> P1, P2)
-constexpr int kScaleWarp0 = 8;   // warps 8..15 load them, one record per lane
-constexpr int kScaleWarps = 8;
+constexpr int kMbRing = 0;       // 0..11: ring slots (P1 gate/up units, P2 down units)
+constexpr int kRingMax = 12;
+constexpr int kMbShared = 12;    // shared-expert gate/up rows (P0 -> P1)
+constexpr int kMbP0 = 13;        // 13..16: P0 row tiles
+constexpr int kP0Tiles = 4;
+constexpr int kMbU = 17;         // U rows (end of P2 -> P3)
+constexpr int kMbScale = 18;     // fp32 scales of the selected records (P1 -> P1, P2)
+constexpr int kScaleWarp = 2;    // the warp that copies them (one arrival per lane)
+constexpr int kPartCap = 24;     // P1 partial-sum entries (ring slots x parts of a unit)
+constexpr int kPadElems = 32;    // row padding (16-bit elements) of x, zh and c in shared memory
+
+// Row pitches (bytes) of rows staged in shared memory: the padding puts rows g and
+// g + 1 of an MMA fragment load in different bank groups.
+__host__ __device__ constexpr int pitch_bf16_row(int K) { return K * 2 + 64; }
+__host__ __device__ constexpr int pitch_f32_row(int K) { return K * 4 + 16; }
+__host__ __device__ constexpr int pitch_gu_row(int L) { return 9 * L / 8 + 16; }
 
 // Phase stamps of a profiled launch, per layer (ns of %globaltimer): CTA 0's time at
 // each point, and the latest (max) / earliest (stored as ~t, max) phase end over all
@@ -55,9 +64,9 @@ enum DecStamp {
   kStP3EndMax, kStP3EndMin, kStBar4,        // barrier 4: stacks only
   kStRouteLoaded,                           // CTA 0: logits and zh in shared memory
   kStTopk,                                  // CTA 0: top-k and weights done
-  kStP1Issued,                              // CTA 0: first round of expert copies issued
-  kStP2Staged,                              // CTA 0: first round of h rows staged
-  kStP2Tasks,                               // CTA 0: down tasks of all rounds done
+  kStP1Issued,                              // CTA 0: first gate/up units issued
+  kStP2Staged,                              // CTA 0: h rows of the first down units requested
+  kStP2Tasks,                               // CTA 0: all down units done
   kStampSlots = 24
 };
 
@@ -95,7 +104,7 @@ struct DecodeArgs {
   float* z;                 // [T][L]
   __half* zh;               // [T][L] f16 copy of z * 2^-e_t (the experts' input)
   float* logits;            // [T][E]
-  __nv_bfloat16* h;         // [T*K + T][F]  SwiGLU output: routed slots, then the shared slot of each token
+  __nv_bfloat16* h;         // [T*K + T][F]  SwiGLU output: grouped positions, then the shared slot of each token
   float* c;                 // [T][L]
   __nv_bfloat16* ybuf;      // [2][T][H] layer outputs inside a stack
   __nv_bfloat16* xbuf;      // [2][T][H] normalised layer inputs inside a stack
@@ -108,12 +117,12 @@ struct DecodeArgs {
   GridBarrier* bar;
   int* err;
   // shared-memory plan (bytes from the 128-aligned dynamic base)
-  int off_xs;               // x bf16 [T][H] (P0; shares its bytes with act)
-  int off_act, act_bytes;   // top-k candidates (P1), c fp32 [T][L] (P3)
-  int off_zh;               // zh f16 [T][L]
-  int off_sh, sh_bytes;     // shared-expert gate/up rows of this CTA
-  int off_res, res_rows;    // gate/up dot results: 2 x res_rows x TB fp32
-  int off_dyn, dyn_bytes;   // staged weights, per phase
+  int off_sh, sh_bytes;     // shared-expert gate/up rows of this CTA (pitch pitch_gu_row)
+  int off_a, a_bytes;       // phase-local arrays: x (P0), zh + partial sums (P1),
+                            // per-slot down outputs (P2), c in bf16 (P3)
+  int off_ring, ring_bytes; // staged weights: P0 rows, the P1/P2 ring, U rows; the
+                            // logits during routing
+  int ring_slots, slot_bytes;
 };
 
 // Tables at the start of dynamic shared memory.
@@ -131,19 +140,21 @@ struct alignas(16) DecTables {
   int goff[kDecodeMaxT * kMaxTopK + 1]; // group g = perm[goff[g] .. goff[g+1])
   int nu;                                // number of distinct experts
   int stuck;                             // bit b: a wait on mbar[b] ran out
-  int task_ctr;                          // dynamic task counter
-  int down_staged;                       // P1 staged the down rows (P2 uses them)
-  int down_off;                          // their offset in the dynamic region
-  int u_staged;                          // P2 staged the U rows (P3 uses them)
-  int pad0, pad1;
+  int pair_ctr[2];                       // next (unit, part) of P1 / P2
+  int ring_cnt[kRingMax];                // parts of units finished on each slot (this phase)
+  int ring_gen[kRingMax];                // units finished on each slot (this layer)
+  int p2_ready;                          // the P2 unit table is built
+  int n2;                                // P2 units of this CTA
   float zsc[kDecodeMaxT], zinv[kDecodeMaxT];
   float4 gsc[kDecodeMaxT * kMaxTopK + 1];  // (gate, up, down, -) fp32 scales of group j:
                                          // j = 0 the shared expert, j >= 1 expert gexp[j - 1]
   float red[kDecWarps * kDecodeMaxT];
   float inv_rms[kDecodeMaxT];
-  // per-round task tables
-  int task_row[512];
-  int task_aux[512];
+  // P2 units: unit k takes the slots q in [p2_qa[k], p2_qa[k + 1]) of the order
+  // (shared slots of tokens 0..T-1, then grouped positions), groups [p2_ja[k], p2_jb[k])
+  short p2_qa[kMaxSlots + 1];
+  short p2_ja[kMaxSlots];
+  short p2_jb[kMaxSlots];
 };
 
 size_t decode_tables_bytes();

@@ -127,7 +127,7 @@ void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
 
 // Every decode bucket's plan holds what each phase stages: at least two ring slots, the
 // P0 rows of a CTA, the logits and top-k candidates, a P2 unit of one expert's down
-// rows and one h row, and the U rows of P3.
+// rows and one h row, and the U rows of P3 in at most one piece per slot.
 bool decode_fits(const Handle* hd) {
   const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts, F = hd->d.ffn, G = hd->num_sms;
   const int ne = (E + G - 1) / G, nr = 2 * ((L / 2 + G - 1) / G), nsr = (F + G - 1) / G, nur = (H + G - 1) / G;
@@ -142,7 +142,8 @@ bool decode_fits(const Handle* hd) {
     if (size_t(kDecWarps) * 32 * NT * 16 > ring) return false;
     if (size_t(TB) * E * 4 + size_t(kDecWarps) * kTopkCand * 8 > ring) return false;
     if (size_t(nr / 2) * (9 * F / 8) + size_t(F) * 2 > (size_t)a.slot_bytes) return false;
-    if (size_t(nur) * pitch_bf16_row(L) > ring) return false;
+    const int rpp = std::max(1, a.slot_bytes / (L * 2));
+    if ((nur + rpp - 1) / rpp > a.ring_slots) return false;           // the U pieces of P3
   }
   return true;
 }

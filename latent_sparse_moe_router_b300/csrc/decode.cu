@@ -362,62 +362,6 @@ __device__ __forceinline__ void fp4_mma_chunks(const MmaRows& ar, const __half* 
   }
 }
 
-// The same with bf16 operands (the down projection: B = SwiGLU activations in bf16).
-// NVFP4 -> f16 by cvt, then to the bf16 exponent range and times the block scale
-// (exact: E2M1 x E4M3 has at most 5 significant bits).
-template <int NT>
-__device__ __forceinline__ void fp4_mma_chunks_bf16(const MmaRows& ar, const __nv_bfloat16* const* brow,
-                                                    const bool* bval, int s0, int s1, float (*acc)[4]) {
-  if (s0 >= s1) return;
-  const int c = threadIdx.x & 3;
-  const uint8_t* ca = ar.code[0] + 4 * c;
-  const uint8_t* cb = ar.code[1] + 4 * c;
-  const uint8_t* sa = ar.scale[0] + (c >> 1);
-  const uint8_t* sb = ar.scale[1] + (c >> 1);
-  float acc2[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc2[t][0] = acc2[t][1] = acc2[t][2] = acc2[t][3] = 0.f;
-  uint32_t wa = *reinterpret_cast<const uint32_t*>(ca + 16 * s0);
-  uint32_t wb = *reinterpret_cast<const uint32_t*>(cb + 16 * s0);
-  uint32_t xa = sa[2 * s0], xb = sb[2 * s0];
-  uint4 z[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-    z[t] = bval[t] ? *reinterpret_cast<const uint4*>(brow[t] + 32 * s0 + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-  for (int s = s0; s < s1; ++s) {
-    const uint32_t cwa = wa, cwb = wb, cxa = xa, cxb = xb;
-    uint4 cz[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) cz[t] = z[t];
-    if (s + 1 < s1) {
-      wa = *reinterpret_cast<const uint32_t*>(ca + 16 * (s + 1));
-      wb = *reinterpret_cast<const uint32_t*>(cb + 16 * (s + 1));
-      xa = sa[2 * (s + 1)];
-      xb = sb[2 * (s + 1)];
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (bval[t]) z[t] = *reinterpret_cast<const uint4*>(brow[t] + 32 * (s + 1) + 8 * c);
-    }
-    const uint32_t ka = scale_bf16x2(cxa), kb = scale_bf16x2(cxb);
-    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-    e2m1x8_to_h2x4(cwa, a0, a1, a2, a3);
-    e2m1x8_to_h2x4(cwb, b0, b1, b2, b3);
-    a0 = h2_to_bf2_scaled(a0, ka); a1 = h2_to_bf2_scaled(a1, ka);
-    a2 = h2_to_bf2_scaled(a2, ka); a3 = h2_to_bf2_scaled(a3, ka);
-    b0 = h2_to_bf2_scaled(b0, kb); b1 = h2_to_bf2_scaled(b1, kb);
-    b2 = h2_to_bf2_scaled(b2, kb); b3 = h2_to_bf2_scaled(b3, kb);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      mma16816_bf16(acc[t], a0, b0, a1, b1, cz[t].x, cz[t].y);
-      mma16816_bf16(acc2[t], a2, b2, a3, b3, cz[t].z, cz[t].w);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    acc[t][0] += acc2[t][0]; acc[t][1] += acc2[t][1]; acc[t][2] += acc2[t][2]; acc[t][3] += acc2[t][3];
-  }
-}
-
 // The same scheme for bf16 weight rows held in shared memory (D, U): ra and rb are A
 // rows g and g + 8, one 16-byte load each per 32-column chunk.
 template <int NT>
@@ -935,6 +879,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       const int ra = max(qa, T);                        // grouped positions: h rows q - T
       if (qb > ra) bulk_g2s(dst + size_t(ra - qa) * hrow, a.h + size_t(ra - T) * F, uint32_t(qb - ra) * hrow, bar);
     };
+    // the stream ends with the U rows of P3: nU pieces of up to rpp contiguous rows,
+    // each one copy into a slot, issued as the last down units free their slots
+    const int rpp = max(1, SB / (L * 2)), nU = (nur + rpp - 1) / rpp;
+    auto issue_u = [&](int v, int n2) {
+      const int i = v - (n1 + n2), ra = i * rpp, rb = min(nur, ra + rpp);
+      uint64_t* bar = slot_bar(v);
+      mbar_arrive_expect_tx(bar, uint32_t(rb - ra) * L * 2);
+      bulk_g2s(slot_ptr(v), lw.U + size_t(j0 + ra) * L, uint32_t(rb - ra) * L * 2, bar);
+      mbar_arrive(bar);
+    };
     // P2 units: consecutive slots q packed into a slot's bytes (down rows of each group
     // touched, then the h rows); a group too large for one unit continues in the next
     auto build_p2 = [&]() {
@@ -960,8 +914,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           qa = qb;
         }
       }
+      int gmax = 1;
+      for (int i = 0; i < k; ++i) gmax = max(gmax, tb->p2_jb[i] - tb->p2_ja[i]);
       tb->p2_qa[k] = short(nslot);
       tb->n2 = k;
+      tb->p2_gmax = gmax;
       __threadfence_block();
       *reinterpret_cast<volatile int*>(&tb->p2_ready) = 1;
     };
@@ -1021,6 +978,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           build_p2();
           const int n2 = tb->n2;
           for (int u = n1; u < min(S + nst, n1 + n2); ++u) issue_p2_down(u);
+          for (int u = n1 + n2; u < min(S + nst, n1 + n2 + nU); ++u) issue_u(u, n2);
         }
         __syncwarp();
       }
@@ -1088,8 +1046,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         // are read too (the next unit on the slot writes them)
         if (lane == 0) {
           const int v = u + S;
-          if (u >= nst && v < n1) issue_p1(v);
-          else if (u >= nst && v < n1 + p2_table()) issue_p2_down(v);
+          if (u >= nst) {
+            if (v < n1) {
+              issue_p1(v);
+            } else {
+              const int n2v = p2_table();
+              if (v < n1 + n2v) issue_p2_down(v);
+              else if (v < n1 + n2v + nU) issue_u(v, n2v);
+            }
+          }
         }
         if (ks > 1) partial_sum<NT>(part1, (u % S) * ks, ks, acc);
         __syncwarp();
@@ -1141,9 +1106,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       stamp0(li, kStP2Staged);
       wait_mb(cx, kMbScale);
       // units of one or more groups; part p of a unit takes its groups p, p + ks2, ...
-      // whole (all F columns), A = the down rows (rho = tile row), B = the group's h rows
-      const int ks2 = min(8, (kDecWarps + max(1, min(S, n2)) - 1) / max(1, min(S, n2)));
-      const int rt = (nr + 15) / 16, nchd = F / 32;
+      // (ks2: the most groups in a unit, at most 8)
+      // whole (all F columns, every 16-row tile), A = the down rows (rho = tile row),
+      // B = the group's h rows, first turned in place from bf16 into f16 times 2^-e_r
+      // (e_r from row r's max |h|): exact for every element above 2^-24 of the row's
+      // maximum, so the down products run on the f16 path
+      const int ks2 = min(8, tb->p2_gmax);
+      const int rt = (nr + 15) / 16, nchd = F / 32, f8 = F / 8;
       const int np2 = n2 * ks2;
       for (;;) {
         int pi = 0;
@@ -1153,47 +1122,77 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         const int k = pi / ks2, part = pi - k * ks2, u = n1 + k;
         ring_wait(u);
         const int qa = tb->p2_qa[k], qb = tb->p2_qa[k + 1], ja = tb->p2_ja[k], jb = tb->p2_jb[k];
-        const uint8_t* sbase = slot_ptr(u);
-        const __nv_bfloat16* hbase = reinterpret_cast<const __nv_bfloat16*>(sbase + size_t(jb - ja) * down_grp);
-        for (int ti = part; ti < (jb - ja) * rt; ti += ks2) {
-          const int jj = ti / rt, rbase = 16 * (ti - jj * rt), j = ja + jj;
+        uint8_t* sbase = slot_ptr(u);
+        uint8_t* hbase = sbase + size_t(jb - ja) * down_grp;
+        for (int jj = part; jj < jb - ja; jj += ks2) {
+          const int j = ja + jj;
           const int qs = max(qa, qlo(j)), ns = min(qb, qhi(j)) - qs;
-          MmaRows ar;
-          const __nv_bfloat16* brow[NT];
-          bool bval[NT];
+          float inv_row = 1.f;                          // lane r < ns: 2^e_r of row r
+          for (int r = 0; r < ns; ++r) {
+            uint4* rp = reinterpret_cast<uint4*>(hbase + size_t(qs - qa + r) * hrow);
+            float m = 0.f;
+            for (int ix = lane; ix < f8; ix += 32) {
+              const uint4 v = rp[ix];
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            int rho = rbase + g8 + 8 * hh;
-            if (rho >= nr) rho = 0;
-            const uint8_t* pr = sbase + size_t(jj) * down_grp + size_t(rho / 2) * d_pair;
-            ar.code[hh] = pr + (rho & 1) * (F / 2);
-            ar.scale[hh] = pr + F + (rho & 1) * (F / 16);
+              for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w4[e])), fabsf(bf16_hi(w4[e]))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+            float sc, inv;
+            pow2_scale(m, &sc, &inv);
+            if (lane == r) inv_row = inv;
+            for (int ix = lane; ix < f8; ix += 32) {
+              const uint4 v = rp[ix];
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+              uint32_t o4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __half2 hv = __floats2half2_rn(bf16_lo(w4[e]) * sc, bf16_hi(w4[e]) * sc);
+                o4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              rp[ix] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
           }
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const int n = 8 * t + g8;
-            bval[t] = n < ns;
-            brow[t] = hbase + size_t(qs - qa + (n < ns ? n : 0)) * F;
-          }
-          float acc[NT][4];
-#pragma unroll
-          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-          if (NT == 1 || ns <= 8) fp4_mma_chunks_bf16<1>(ar, brow, bval, 0, nchd, acc);
-          else fp4_mma_chunks_bf16<NT>(ar, brow, bval, 0, nchd, acc);
+          __syncwarp();
           const float gd = tb->gsc[j].z;
+          for (int rbase = 0; rbase < nr; rbase += 16) {
+            MmaRows ar;
+            const __half* brow[NT];
+            bool bval[NT];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int rho = rbase + g8 + 8 * hh;
-            if (rho >= nr) continue;
+            for (int hh = 0; hh < 2; ++hh) {
+              int rho = rbase + g8 + 8 * hh;
+              if (rho >= nr) rho = 0;
+              const uint8_t* pr = sbase + size_t(jj) * down_grp + size_t(rho / 2) * d_pair;
+              ar.code[hh] = pr + (rho & 1) * (F / 2);
+              ar.scale[hh] = pr + F + (rho & 1) * (F / 16);
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const int n = 8 * t + g8;
+              bval[t] = n < ns;
+              brow[t] = reinterpret_cast<const __half*>(hbase + size_t(qs - qa + (n < ns ? n : 0)) * hrow);
+            }
+            float acc[NT][4];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            if (NT == 1 || ns <= 8) fp4_mma_chunks<1>(ar, brow, bval, 0, nchd, acc);
+            else fp4_mma_chunks<NT>(ar, brow, bval, 0, nchd, acc);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
               for (int jx = 0; jx < 2; ++jx) {
                 const int n = 8 * t + 2 * c4 + jx;
-                if (n < ns) {
-                  const int q = qs + n;
-                  const int slot = (q < T) ? TK + q : tb->perm[q - T];
-                  ob[size_t(slot) * nr + rho] = gd * acc[t][2 * hh + jx];
+                const float inv_n = __shfl_sync(kFull, inv_row, n & 31);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const int rho = rbase + g8 + 8 * hh;
+                  if (rho < nr && n < ns) {
+                    const int q = qs + n;
+                    const int slot = (q < T) ? TK + q : tb->perm[q - T];
+                    ob[size_t(slot) * nr + rho] = gd * (acc[t][2 * hh + jx] * inv_n);
+                  }
                 }
               }
           }
@@ -1201,7 +1200,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         if (!part_done(u, ks2)) continue;
         if (lane == 0) {
           const int v = u + S;
-          if (v < n1 + n2) {
+          if (v >= n1 + n2) {
+            if (v < n1 + n2 + nU) issue_u(v, n2);
+          } else {
             issue_p2_down(v);
             issue_p2_h(v);
           }
@@ -1211,21 +1212,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       __syncthreads();
       stamp0(li, kStP2Tasks);
-      // every ring slot's copies of this layer have been waited for: advance its parity
-      for (int s = 0; s < S; ++s) {
-        const int n_all = n1 + n2;
-        const int units = s < n_all ? (n_all - 1 - s) / S + 1 : 0;
-        const int csh = s < nst ? (nst - 1 - s) / S + 1 : 0;
-        if ((units - csh) & 1) release_mb(cx, 1u << (kMbRing + s));
-      }
-      // U rows of P3 into the ring area, in flight across the combine and the barrier
-      if (warp == 0 && nur > 0) {
-        const int pu = pitch_bf16_row(L);
-        if (lane == 0) mbar_arrive_expect_tx(&tb->mbar[kMbU], uint32_t(nur) * L * 2);
-        __syncwarp();
-        for (int i = lane; i < nur; i += 32)
-          bulk_g2s(ring + size_t(i) * pu, lw.U + size_t(j0 + i) * L, uint32_t(L) * 2, &tb->mbar[kMbU]);
-      }
       // combine: c[t][r] = o_shared + sum_k w[t][k] o[t*K + k], k ascending
       for (int p = tid; p < T * nr; p += kDecThreads) {
         const int t = p / nr, r = p % nr;
@@ -1243,6 +1229,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     // grid's completion before reading anything)
     if (last) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
+      // U rows: the last nU units of the ring stream (each MMA warp waits for the pieces
+      // holding its tile's rows)
+      const int n2 = tb->n2, ubase = n1 + n2;
+      const int nut = (nur + 15) / 16, wpt = nut > 0 ? kDecWarps / nut : kDecWarps;
+      const int tile = warp / wpt, part = warp - tile * wpt;
+      const int nchl = L / 32, s0 = nchl * part / wpt, s1 = nchl * (part + 1) / wpt;
+      const bool mma_warp = tile < nut;
+      auto u_row = [&](int r) {
+        return reinterpret_cast<const __nv_bfloat16*>(slot_ptr(ubase + r / rpp) + size_t(r % rpp) * L * 2);
+      };
       // c (all CTAs' rows) into shared memory in bf16, padded rows
       const int l8 = L / 8;
       for (int i = tid; i < T * l8; i += kDecThreads) {
@@ -1258,17 +1254,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       __syncthreads();
       __nv_bfloat16* yo = (last && !a.final_norm) ? a.y : a.ybuf + size_t(li & 1) * T * H;
       __nv_bfloat16* ty = a.trace_y ? a.trace_y + size_t(li) * T * H : nullptr;
-      const int nut = (nur + 15) / 16, wpt = nut > 0 ? kDecWarps / nut : kDecWarps;
-      const int tile = warp / wpt, part = warp - tile * wpt;
-      const int pu = pitch_bf16_row(L), nchl = L / 32;
       float acc[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-      if (tile < nut) {
-        wait_mb(cx, kMbU);
-        int ra = 16 * tile + g8, rb = 16 * tile + g8 + 8;
-        if (ra >= nur) ra = 16 * tile;
-        if (rb >= nur) rb = 16 * tile;
+      if (mma_warp) {
         const __nv_bfloat16* brow[NT];
         bool bval[NT];
 #pragma unroll
@@ -1277,9 +1266,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           bval[t] = n < T;
           brow[t] = cs + size_t(n < T ? n : 0) * zp;
         }
-        bf16_mma_chunks<NT>(reinterpret_cast<const __nv_bfloat16*>(ring + size_t(ra) * pu),
-                            reinterpret_cast<const __nv_bfloat16*>(ring + size_t(rb) * pu), brow, bval,
-                            nchl * part / wpt, nchl * (part + 1) / wpt, acc);
+        const int ra0 = 16 * tile, ra1 = min(nur, ra0 + 16);
+        for (int pc = ra0 / rpp; pc <= (ra1 - 1) / rpp; ++pc) ring_wait(ubase + pc);
+        int ra = ra0 + g8, rb = ra0 + g8 + 8;
+        if (ra >= nur) ra = ra0;
+        if (rb >= nur) rb = ra0;
+        bf16_mma_chunks<NT>(u_row(ra), u_row(rb), brow, bval, s0, s1, acc);
       }
       __syncthreads();                 // the U rows are read: the partial sums overwrite them
       partial_store<NT>(partw, acc);
@@ -1303,7 +1295,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             }
         }
       }
-      if (nur > 0) release_mb(cx, 1u << kMbU);
+    }
+    // every ring slot's copies of this layer have been waited for: advance its parity
+    {
+      const int n_all = n1 + tb->n2 + nU;
+      for (int s = 0; s < S; ++s) {
+        const int units = s < n_all ? (n_all - 1 - s) / S + 1 : 0;
+        const int csh = s < nst ? (nst - 1 - s) / S + 1 : 0;
+        if ((units - csh) & 1) release_mb(cx, 1u << (kMbRing + s));
+      }
     }
     stamp_end(li, kStP3EndMax);
     if (!last || a.final_norm) {

@@ -13,10 +13,11 @@
 //       gate/up -> h                    rows of the union of the selected experts and
 //                                        of the shared expert (staged during P0)
 //   P2  down projections + combine -> c (the down rows are fetched during P1)
-//   P3  y = U c                          (U rows fetched at the end of P2)
+//   P3  y = U c                          (U rows: the end of the ring stream)
 // Every product runs on m16n8k16 mma.sync with the tokens on N.  The expert rows move
 // through a ring of shared-memory slots: each slot is one bulk-copied unit of work
-// (8 gate/up row pairs in P1, a few experts' down rows and their h rows in P2), the
+// (8 gate/up row pairs in P1, a few experts' down rows and their h rows in P2, U rows
+// for P3), the
 // warp that finishes the last part of a unit refills its slot with the unit S places
 // further on, and units of P1 and P2 form one stream, so that the first down units are
 // in flight before P1 ends.  A stack of layers (residual + RMSNorm between them) runs
@@ -40,7 +41,6 @@ constexpr int kRingMax = 12;
 constexpr int kMbShared = 12;    // shared-expert gate/up rows (P0 -> P1)
 constexpr int kMbP0 = 13;        // 13..16: P0 row tiles
 constexpr int kP0Tiles = 4;
-constexpr int kMbU = 17;         // U rows (end of P2 -> P3)
 constexpr int kMbScale = 18;     // fp32 scales of the selected records (P1 -> P1, P2)
 constexpr int kScaleWarp = 2;    // the warp that copies them (one arrival per lane)
 constexpr int kPartCap = 24;     // P1 partial-sum entries (ring slots x parts of a unit)
@@ -120,8 +120,8 @@ struct DecodeArgs {
   int off_sh, sh_bytes;     // shared-expert gate/up rows of this CTA (pitch pitch_gu_row)
   int off_a, a_bytes;       // phase-local arrays: x (P0), zh + partial sums (P1),
                             // per-slot down outputs (P2), c in bf16 (P3)
-  int off_ring, ring_bytes; // staged weights: P0 rows, the P1/P2 ring, U rows; the
-                            // logits during routing
+  int off_ring, ring_bytes; // staged weights: P0 rows, the P1/P2 ring; the logits during
+                            // routing; per-warp partial sums (P0, P3)
   int ring_slots, slot_bytes;
 };
 
@@ -145,6 +145,7 @@ struct alignas(16) DecTables {
   int ring_gen[kRingMax];                // units finished on each slot (this layer)
   int p2_ready;                          // the P2 unit table is built
   int n2;                                // P2 units of this CTA
+  int p2_gmax;                           // the most groups in one P2 unit
   float zsc[kDecodeMaxT], zinv[kDecodeMaxT];
   float4 gsc[kDecodeMaxT * kMaxTopK + 1];  // (gate, up, down, -) fp32 scales of group j:
                                          // j = 0 the shared expert, j >= 1 expert gexp[j - 1]

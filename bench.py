@@ -38,6 +38,9 @@ WORKLOADS = {
     "layer145b_t4096_zipf": dict(kind="prefill", latent=1792, T=4096, seed=3, layers=1, zipf=(1.1,),
                                  instances=2,
                                  desc="one Edge0-145B layer, prefill T=4096, Zipf(1.1) router bias"),
+    # one layer at the widest verify window: a size for profiling captures of the decode kernel
+    "layer145b_t16": dict(kind="decode", latent=1792, T=16, seed=0, layers=1, zipf=(0.0,), instances=16,
+                          desc="one Edge0-145B layer, decode verify window T=16 (profiling size)"),
     # one layer of the 16K workload (its uniform-routing first layer): a size for profiling captures
     "layer145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=1, zipf=(0.0,), instances=1,
                              desc="one Edge0-145B layer, prefill T=16384, uniform routing (profiling size)"),
@@ -54,9 +57,11 @@ HIDDEN, E, K, F = 2560, 512, 10, 640
 METRIC = "latent-MoE layer tok/s at T=1 and T=16K; % of HBM / bf16 tensor roofline"
 MIN_TIMED_S = 2.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from one
-# ncu capture of the current kernels (profiles/dram_traffic_grouped_decode.md)
-TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1522560256,
-           ("layer145b_t1", "moe_decode_kernel"): 45097984}
+# ncu capture of the current kernels: the gate/up grouped GEMM on the uniform-routing
+# layer of the 16K workload (profiles/ncu_grouped_nvfp4_layer145b_t16384.md), the decode
+# kernel on one layer at T=1 (profiles/ncu_moe_decode_layer145b_t1.md)
+TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1524064000,
+           ("layer145b_t1", "moe_decode_kernel"): None}
 
 
 def flops_per_token_layer(latent):
@@ -362,7 +367,8 @@ def timed_region(step, args, stream, world, local, min_s=MIN_TIMED_S, steps=None
             for i in range(steps):
                 step(args.warmup + i, stream)
         stream.synchronize()
-        graph.replay()                      # one untimed replay (the graph's first launch)
+        with torch.cuda.stream(stream):
+            graph.replay()                  # one untimed replay (the graph's first launch)
         stream.synchronize()
     except Exception as e:                  # graph capture unavailable: launch directly
         print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
@@ -409,16 +415,19 @@ def serial_e2e(stream, graphs, n_steps, world):
     """Steps one after another, the host reading each step's result before the next
     (autoregressive decode); CUDA events around the loop on the launching stream."""
     import torch
-    for g in graphs:
-        g.replay()
+    # a graph replays on the current stream: every replay is made on the launching stream
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
     stream.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(n_steps):
-        graphs[i % len(graphs)].replay()
-        stream.synchronize()                  # the host reads the step's result
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_steps):
+            graphs[i % len(graphs)].replay()
+            stream.synchronize()              # the host reads the step's result
+        e1.record(stream)
     stream.synchronize()
     return max_over_ranks(e0.elapsed_time(e1), world) / n_steps
 

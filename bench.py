@@ -59,9 +59,9 @@ MIN_TIMED_S = 2.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from one
 # ncu capture of the current kernels: the gate/up grouped GEMM on the uniform-routing
 # layer of the 16K workload (profiles/ncu_grouped_nvfp4_layer145b_t16384.md), the decode
-# kernel on one layer at T=1 (profiles/ncu_moe_decode_layer145b_t1.md)
+# kernel on one layer at T=1 (profiles/ncu_moe_decode_layer145b_t1_t16.md)
 TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1524064000,
-           ("layer145b_t1", "moe_decode_kernel"): None}
+           ("layer145b_t1", "moe_decode_kernel"): 45104128}
 
 
 def flops_per_token_layer(latent):

@@ -938,6 +938,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       __threadfence_block();
       return tb->n2;
     };
+    // warp-wide refills (every lane calls): lane 0 arms the slot's barrier and the copies
+    // go out from different lanes, which the copy engine accepts faster than from one
+    auto refill_p1 = [&](int v) {
+      const int q = q0 + 8 * (v - nst), g = q / F, fa = q - g * F;
+      uint64_t* bar = slot_bar(v);
+      if (lane == 0) mbar_arrive_expect_tx(bar, 8u * uint32_t(gu_row));
+      __syncwarp();
+      if (lane < 2)
+        bulk_g2s(slot_ptr(v) + size_t(lane) * (4 * gu_row + 16), tb->gptr[g] + size_t(fa + 4 * lane) * gu_row,
+                 4u * uint32_t(gu_row), bar);
+      if (lane == 0) mbar_arrive(bar);
+    };
+    auto refill_p2 = [&](int v, bool with_h) {
+      const int k = v - n1, ja = tb->p2_ja[k], jb = tb->p2_jb[k];
+      uint8_t* dst = slot_ptr(v);
+      uint64_t* bar = slot_bar(v);
+      if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(jb - ja) * uint32_t(down_grp));
+      __syncwarp();
+      for (int j = ja + lane; j < jb; j += 32)
+        bulk_g2s(dst + size_t(j - ja) * down_grp, p2_rec(j) + rec_dblk + size_t(r0 / 2) * d_pair, uint32_t(down_grp),
+                 bar);
+      if (!with_h) return;
+      const int qa = tb->p2_qa[k], qb = tb->p2_qa[k + 1];
+      uint8_t* hd = dst + size_t(jb - ja) * down_grp;
+      if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(qb - qa) * uint32_t(hrow));
+      __syncwarp();
+      const int sb = min(qb, T), ra = max(qa, T);
+      if (lane == 1 && sb > qa) bulk_g2s(hd, a.h + size_t(TK + qa) * F, uint32_t(sb - qa) * hrow, bar);
+      if (lane == 2 && qb > ra) bulk_g2s(hd + size_t(ra - qa) * hrow, a.h + size_t(ra - T) * F, uint32_t(qb - ra) * hrow, bar);
+    };
+    auto refill_u = [&](int v, int n2) {
+      if (lane == 0) issue_u(v, n2);
+    };
     {
       // the first units of the ring, and the fp32 scales of the selected records (16
       // bytes from each record's scale block: gate, up, down and the record's padding);
@@ -1044,15 +1077,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         // every part has read the slot: refill it with the unit S places on (a down
         // unit: its first part); the slot's unit count moves on once the partial sums
         // are read too (the next unit on the slot writes them)
-        if (lane == 0) {
+        {
           const int v = u + S;
           if (u >= nst) {
             if (v < n1) {
-              issue_p1(v);
+              refill_p1(v);
             } else {
               const int n2v = p2_table();
-              if (v < n1 + n2v) issue_p2_down(v);
-              else if (v < n1 + n2v + nU) issue_u(v, n2v);
+              if (v < n1 + n2v) refill_p2(v, false);
+              else if (v < n1 + n2v + nU) refill_u(v, n2v);
             }
           }
         }
@@ -1112,7 +1145,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       // (e_r from row r's max |h|): exact for every element above 2^-24 of the row's
       // maximum, so the down products run on the f16 path
       const int ks2 = min(8, tb->p2_gmax);
-      const int rt = (nr + 15) / 16, nchd = F / 32, f8 = F / 8;
+      const int nchd = F / 32, f8 = F / 8;
       const int np2 = n2 * ks2;
       for (;;) {
         int pi = 0;
@@ -1198,16 +1231,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           }
         }
         if (!part_done(u, ks2)) continue;
-        if (lane == 0) {
+        {
           const int v = u + S;
           if (v >= n1 + n2) {
-            if (v < n1 + n2 + nU) issue_u(v, n2);
+            if (v < n1 + n2 + nU) refill_u(v, n2);
           } else {
-            issue_p2_down(v);
-            issue_p2_h(v);
+            refill_p2(v, true);
           }
-          atomicAdd(&tb->ring_gen[u % S], 1);
         }
+        __syncwarp();
+        if (lane == 0) atomicAdd(&tb->ring_gen[u % S], 1);
         __syncwarp();
       }
       __syncthreads();

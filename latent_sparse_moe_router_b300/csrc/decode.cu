@@ -483,10 +483,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   const size_t rec_body = rec_dblk + size_t(L / 2) * d_pair;
   const int cofs_up = L / 2, sofs_g = L, sofs_u = L + L / 16;   // offsets inside a GU row
   // this CTA's row ranges (latent rows in whole pairs)
-  const int r0 = 2 * int(long(bid) * (L / 2) / G), r1 = 2 * int(long(bid + 1) * (L / 2) / G);
-  const int e0 = int(long(bid) * E / G), e1 = int(long(bid + 1) * E / G);      // router rows
-  const int f0 = int(long(bid) * F / G), f1 = int(long(bid + 1) * F / G);      // shared rows
-  const int j0 = int(long(bid) * H / G), j1 = int(long(bid + 1) * H / G);      // hidden rows
+  // (32-bit: every product below is under 2^31 for the shapes the host accepts)
+  const int r0 = 2 * (bid * (L / 2) / G), r1 = 2 * ((bid + 1) * (L / 2) / G);
+  const int e0 = bid * E / G, e1 = (bid + 1) * E / G;                          // router rows
+  const int f0 = bid * F / G, f1 = (bid + 1) * F / G;                          // shared rows
+  const int j0 = bid * H / G, j1 = (bid + 1) * H / G;                          // hidden rows
   const int nr = r1 - r0, nsr = f1 - f0, ne = e1 - e0, nur = j1 - j0;
   // the ring: S slots of SB bytes; a unit is split into ks parts (P1: K ranges)
   const int S = a.ring_slots, SB = a.slot_bytes;
@@ -547,7 +548,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
     }
     __syncwarp();
-    const int csh = s < nst ? (nst - 1 - s) / S + 1 : 0;       // copy-less units on slot s
+    const int csh = s < nst ? 1 : 0;                           // copy-less units on slot s (nst <= S)
     const uint32_t par = ((cx.mbp >> (kMbRing + s)) ^ uint32_t(need - csh)) & 1u;
     if (!mbar_wait_sleep(&tb->mbar[kMbRing + s], par, a.err)) atomicOr(&tb->stuck, 1 << (kMbRing + s));
   };
@@ -767,6 +768,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
         tb->posn[s] = r;
         tb->perm[r] = s;
+        tb->tokp[r] = short(s / K);
       }
       __syncthreads();
       if (warp == 0) {
@@ -840,8 +842,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     // the stream: units [0, nst) the shared expert's rows, [nst, n1) the routed rows,
     // [n1, n1 + n2) the down units of P2
     const int ngr = nu + 1;                             // groups: the shared expert, then the routed experts
-    const long ntq = long(nu) * (F / 8);
-    const int q0 = 8 * int(ntq * bid / G), q1 = 8 * int(ntq * (bid + 1) / G);
+    const int ntq = nu * (F / 8);
+    const int q0 = 8 * (ntq * bid / G), q1 = 8 * (ntq * (bid + 1) / G);
     n1 = nst + (q1 - q0) / 8;
     // P2 slots in one order q: q < T the shared expert's slot of token q, q >= T grouped
     // position q - T; group j covers [qlo(j), qhi(j)) (j = 0 the shared expert)
@@ -988,14 +990,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       // the routing tables for the caller (trace, and the last layer's copy read by
       // edge0_moe_debug_routing), each CTA a slice
       {
-        const int s0 = int(long(TK) * bid / G), s1 = int(long(TK) * (bid + 1) / G);
+        const int s0 = TK * bid / G, s1 = TK * (bid + 1) / G;
         if (a.trace_idx)
           for (int s = s0 + tid; s < s1; s += kDecThreads) a.trace_idx[size_t(li) * TK + s] = tb->idx[s];
         if (last) {
           for (int s = s0 + tid; s < s1; s += kDecThreads) {
             a.idx[s] = tb->idx[s]; a.w[s] = tb->w[s]; a.perm[s] = tb->perm[s]; a.pos[s] = tb->posn[s];
           }
-          const int ea = int(long(E + 1) * bid / G), eb = int(long(E + 1) * (bid + 1) / G);
+          const int ea = (E + 1) * bid / G, eb = (E + 1) * (bid + 1) / G;
           for (int e = ea + tid; e < eb; e += kDecThreads) {
             int off = TK, cnt = 0;
             for (int g = 0; g < nu; ++g) {
@@ -1055,7 +1057,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           for (int t = 0; t < NT; ++t) {
             const int n = 8 * t + g8;
             bval[t] = n < ns;
-            brow[t] = zs + size_t(n < ns ? tb->perm[tb->goff[grp] + n] / K : 0) * zp;
+            brow[t] = zs + size_t(n < ns ? tb->tokp[tb->goff[grp] + n] : 0) * zp;
           }
           ring_wait(u);
         }
@@ -1105,7 +1107,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
               const int n = 8 * t + 2 * c4 + j;
               if (n < ns) {
                 const int hr = grp < 0 ? TK + n : tb->goff[grp] + n;
-                const float zi = tb->zinv[grp < 0 ? n : tb->perm[tb->goff[grp] + n] / K];
+                const float zi = tb->zinv[grp < 0 ? n : tb->tokp[tb->goff[grp] + n]];
                 a.h[size_t(hr) * F + f] = __float2bfloat16_rn(silu_f(gg * acc[t][j] * zi) * (gu * acc[t][2 + j] * zi));
               }
             }
@@ -1329,14 +1331,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         }
       }
     }
-    // every ring slot's copies of this layer have been waited for: advance its parity
+    // every ring slot's copies of this layer have been waited for: advance its parity by
+    // the number of copies it took (its units, less the copy-less shared unit; nst <= S)
     {
-      const int n_all = n1 + tb->n2 + nU;
-      for (int s = 0; s < S; ++s) {
-        const int units = s < n_all ? (n_all - 1 - s) / S + 1 : 0;
-        const int csh = s < nst ? (nst - 1 - s) / S + 1 : 0;
-        if ((units - csh) & 1) release_mb(cx, 1u << (kMbRing + s));
-      }
+      const int n_all = n1 + tb->n2 + nU, q = n_all / S, r = n_all - q * S;
+      uint32_t flip = 0;
+      for (int s = 0; s < S; ++s) flip |= uint32_t((q + (s < r) - (s < nst)) & 1) << (kMbRing + s);
+      release_mb(cx, flip);
     }
     stamp_end(li, kStP3EndMax);
     if (!last || a.final_norm) {
@@ -1347,7 +1348,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       // stack output: RMSNorm(x_last + y_last); every CTA normalises, each writes its slice
       residual_norm(tb, xcur, a.ybuf + size_t(li & 1) * T * H, xs, xp, T, H, a.eps, [] {});
       const int h8 = H / 8, n8 = T * h8;
-      const int i0 = int(long(bid) * n8 / G), i1 = int(long(bid + 1) * n8 / G);
+      const int i0 = bid * n8 / G, i1 = (bid + 1) * n8 / G;
       for (int i = i0 + tid; i < i1; i += kDecThreads) {
         const int t = i / h8;
         reinterpret_cast<uint4*>(a.y)[i] = *reinterpret_cast<const uint4*>(xs + size_t(t) * xp + 8 * (i - t * h8));

@@ -132,6 +132,7 @@ struct alignas(16) DecTables {
   float w[kDecodeMaxT * kMaxTopK];
   int perm[kDecodeMaxT * kMaxTopK];     // grouped position -> slot
   int posn[kDecodeMaxT * kMaxTopK];     // slot -> grouped position
+  short tokp[kDecodeMaxT * kMaxTopK];   // grouped position -> token
   int gexp[kDecodeMaxT * kMaxTopK];     // distinct experts, ascending
   const uint8_t* gptr[kDecodeMaxT * kMaxTopK];  // record of each distinct expert for this forward
   int gmiss[kDecodeMaxT * kMaxTopK];    // tiering: staging index of a non-resident expert, else -1

@@ -495,15 +495,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   const int nst = (nsr + 7) / 8;                                 // shared-expert gate/up units
   const int down_grp = (nr / 2) * d_pair, hrow = F * 2;
 
-  // launched as a programmatic dependent of the preceding kernel on the stream: its
-  // results (this launch's input, the workspace) are complete from here on
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // a launch after one whose wait ran out finds the grid barrier mid-round (reset
-  // by edge0_moe_get_error): it does no work and leaves the error word set
-  if (ld_relaxed_u32(&a.bar->abort)) {
-    if (tid == 0) atomicOr(a.err, kErrTimeout);
-    return;
-  }
   if (tid == 0) {
     // ring slots complete on two arrivals (a unit's copies may be issued in two parts)
     for (int b = 0; b < kNumMbar; ++b)
@@ -512,6 +503,46 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
     tb->stuck = 0;
   }
   __syncthreads();
+  // P0's rows: router tiles of 8 fp32 rows (high / low bf16 terms in A rows g / g + 8),
+  // D tiles of 16 bf16 rows; every row bulk-copied to its padded place in the ring area
+  const int nrt = (ne + 7) / 8, ndt = (nr + 15) / 16, ntile = nrt + ndt;
+  const int pf = pitch_f32_row(H), pb = pitch_bf16_row(H);
+  uint8_t* rows_d = ring + size_t(ne) * pf;
+  auto issue_d_rows = [&](const LayerW& w) {           // warp 0
+    if (lane < ndt) mbar_arrive_expect_tx(&tb->mbar[kMbP0 + nrt + lane], uint32_t(min(16, nr - 16 * lane)) * H * 2);
+    __syncwarp();
+    for (int r = lane; r < nr; r += 32)
+      bulk_g2s(rows_d + size_t(r) * pb, w.D + size_t(r0 + r) * H, uint32_t(H) * 2, &tb->mbar[kMbP0 + nrt + r / 16]);
+  };
+  auto issue_rd_rows = [&](const LayerW& w) {          // warp 0
+    if (lane < nrt) mbar_arrive_expect_tx(&tb->mbar[kMbP0 + lane], uint32_t(min(8, ne - 8 * lane)) * H * 4);
+    __syncwarp();
+    for (int i = lane; i < ne; i += 32)
+      bulk_g2s(ring + size_t(i) * pf, w.RD + size_t(e0 + i) * H, uint32_t(H) * 4, &tb->mbar[kMbP0 + i / 8]);
+  };
+  auto issue_shared_rows = [&](const LayerW& w) {      // warp 1
+    if (nsr <= 0) return;
+    if (lane == 0) mbar_arrive_expect_tx(&tb->mbar[kMbShared], uint32_t(nsr) * gu_row);
+    __syncwarp();
+    if (lane < nsr)
+      bulk_g2s(shr + size_t(lane) * gu_pitch, w.shared + size_t(f0 + lane) * gu_row, uint32_t(gu_row),
+               &tb->mbar[kMbShared]);
+  };
+  // the first layer's D rows and shared-expert rows are weights no kernel writes: their
+  // copies go out before the wait on the preceding kernel (R D may come from it)
+  if (warp == 0) issue_d_rows(a.l0);
+  if (warp == 1) issue_shared_rows(a.l0);
+
+  // launched as a programmatic dependent of the preceding kernel on the stream: its
+  // results (this launch's input, the workspace) are complete from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a launch after one whose wait ran out finds the grid barrier mid-round (reset
+  // by edge0_moe_get_error): it does no work and leaves the error word set
+  if (ld_relaxed_u32(&a.bar->abort)) {
+    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    drain_copies();
+    return;
+  }
 
   // profiling stamps (no-ops unless the launch carries a stamp buffer)
   auto stamp0 = [&](int li, int slot) {
@@ -585,40 +616,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         sh_gu = *reinterpret_cast<const float2*>(gs);
         sh_d = gs[2];
       }
-      // row tiles: router tiles of 8 fp32 rows (high / low bf16 terms in A rows g / g + 8),
-      // D tiles of 16 bf16 rows; every row bulk-copied to its padded place in the ring area
-      const int nrt = (ne + 7) / 8, ndt = (nr + 15) / 16, ntile = nrt + ndt;
-      const int pf = pitch_f32_row(H), pb = pitch_bf16_row(H);
-      uint8_t* rows_d = ring + size_t(ne) * pf;
       // this CTA's router bias entries, in flight while x is read
       const int bj = tid - (kDecThreads - 32);          // lanes of the last warp
       const float bv = (bj >= 0 && bj < ne && lw.bias) ? lw.bias[e0 + bj] : 0.f;
-      // the weight rows and the shared expert's gate/up rows go out right after x's loads
+      // the weight rows go out right after x's loads (layer 0: the router rows only)
       auto stage = [&]() {
         if (warp == 0) {
-          if (lane < ntile) {
-            const uint32_t bytes = lane < nrt ? uint32_t(min(8, ne - 8 * lane)) * H * 4
-                                              : uint32_t(min(16, nr - 16 * (lane - nrt))) * H * 2;
-            mbar_arrive_expect_tx(&tb->mbar[kMbP0 + lane], bytes);
-          }
-          __syncwarp();
-          for (int i = lane; i < ne + nr; i += 32) {
-            if (i < ne) {
-              bulk_g2s(ring + size_t(i) * pf, lw.RD + size_t(e0 + i) * H, uint32_t(H) * 4, &tb->mbar[kMbP0 + i / 8]);
-            } else {
-              const int r = i - ne;
-              bulk_g2s(rows_d + size_t(r) * pb, lw.D + size_t(r0 + r) * H, uint32_t(H) * 2,
-                       &tb->mbar[kMbP0 + nrt + r / 16]);
-            }
-          }
+          issue_rd_rows(lw);
+          if (li > 0) issue_d_rows(lw);
         }
-        if (warp == 1 && nsr > 0) {
-          if (lane == 0) mbar_arrive_expect_tx(&tb->mbar[kMbShared], uint32_t(nsr) * gu_row);
-          __syncwarp();
-          if (lane < nsr)
-            bulk_g2s(shr + size_t(lane) * gu_pitch, lw.shared + size_t(f0 + lane) * gu_row, uint32_t(gu_row),
-                     &tb->mbar[kMbShared]);
-        }
+        if (warp == 1 && li > 0) issue_shared_rows(lw);
       };
       const int h8 = H / 8;
       if (li == 0) {

@@ -105,12 +105,12 @@ void decode_plan(const Handle* hd, int TB, DecodeArgs& a) {
   a.sh_bytes = (int)align_up((size_t)shared_rows * pitch_gu_row(L), 128);
   off += a.sh_bytes;
   // x [T][H + pad] (P0); zh [T][L + pad] and the partial sums (P1); the per-slot down
-  // outputs (P2); c [T][L + pad] (P3)
+  // outputs of both halves of F (P2); c [T][L + pad] (P3)
   const int nr_max = 2 * ((L / 2 + G - 1) / G);
   const size_t xs = size_t(TB) * (H + kPadElems) * 2;
   const size_t zs = align_up(size_t(TB) * (L + kPadElems) * 2, 128);
   const size_t p1 = zs + size_t(kPartCap) * 32 * NT * 16;
-  const size_t p2 = size_t(TB) * (K + 1) * nr_max * 4;
+  const size_t p2 = 2 * size_t(TB) * (K + 1) * nr_max * 4;        // two halves of F
   size_t ar = xs > p1 ? xs : p1;
   if (p2 > ar) ar = p2;
   a.off_a = (int)off;

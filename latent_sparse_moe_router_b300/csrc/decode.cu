@@ -169,6 +169,7 @@ __device__ void warp_topk_reg(const float* row, int K, Cand* cand, int* idx, flo
     for (int i = lane; i < total; i += 32) {
       const Cand c = cand[i];
       int r = 0;
+#pragma unroll 8
       for (int q = 0; q < total; ++q) {
         const Cand o = cand[q];
         r += cand_first(o.v, o.i, c.v, c.i);
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(areg);    // P0: x [T][xp]
   __half* zs = reinterpret_cast<__half*>(areg);                  // P1: zh [T][zp]
   float4* part1 = reinterpret_cast<float4*>(areg + ((size_t(T) * zp * 2 + 127) & ~size_t(127)));
-  float* ob = reinterpret_cast<float*>(areg);                    // P2: down outputs [slot][nr]
+  float* ob = reinterpret_cast<float*>(areg);                    // P2: down outputs [half][slot][nr]
   __nv_bfloat16* cs = reinterpret_cast<__nv_bfloat16*>(areg);    // P3: c [T][zp] in bf16
   float4* partw = reinterpret_cast<float4*>(ring);               // P0 / P3: per-warp partial sums
   // record layout: GU block of F rows (gate codes | up codes | gate scales | up
@@ -769,6 +770,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       for (int s = tid; s < TK; s += kDecThreads) {
         const int key = tb->idx[s];
         int r = 0;
+#pragma unroll 8
         for (int u = 0; u < TK; ++u) {
           const int k2 = tb->idx[u];
           r += (k2 < key) || (k2 == key && u < s);
@@ -1147,14 +1149,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       if (warp == 0 && lane < min(S, n2)) issue_p2_h(n1 + lane);
       stamp0(li, kStP2Staged);
       wait_mb(cx, kMbScale);
-      // units of one or more groups; part p of a unit takes its groups p, p + ks2, ...
-      // (ks2: the most groups in a unit, at most 8)
-      // whole (all F columns, every 16-row tile), A = the down rows (rho = tile row),
-      // B = the group's h rows, first turned in place from bf16 into f16 times 2^-e_r
-      // (e_r from row r's max |h|): exact for every element above 2^-24 of the row's
-      // maximum, so the down products run on the f16 path
-      const int ks2 = min(8, tb->p2_gmax);
-      const int nchd = F / 32, f8 = F / 8;
+      // units of one or more groups; in the 16-token bucket each group's F columns are
+      // split in two halves (more, shorter items for the warps; below it a group is one
+      // item), and part p of a unit takes the items p, p + ks2, ... (ks2: the most items
+      // in a unit, at most 8): every 16-row tile, A = the down rows (rho =
+      // tile row), B = the half's h columns, first turned in place from bf16 into f16
+      // times 2^-e_r (e_r from the max |h| of row r's half: exact for every element above
+      // 2^-24 of it), so the down products run on the f16 path; each half writes its own
+      // outputs, added in a fixed order by the combine
+      constexpr int NH = NT == 2 ? 2 : 1;              // halves of F per group
+      const int ks2 = min(8, NH * tb->p2_gmax);
+      const int nchd = F / 32, f8 = F / 8, hch = nchd / NH;
       const int np2 = n2 * ks2;
       for (;;) {
         int pi = 0;
@@ -1166,14 +1171,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
         const int qa = tb->p2_qa[k], qb = tb->p2_qa[k + 1], ja = tb->p2_ja[k], jb = tb->p2_jb[k];
         uint8_t* sbase = slot_ptr(u);
         uint8_t* hbase = sbase + size_t(jb - ja) * down_grp;
-        for (int jj = part; jj < jb - ja; jj += ks2) {
-          const int j = ja + jj;
+        for (int it = part; it < NH * (jb - ja); it += ks2) {
+          const int jj = it / NH, half = it - jj * NH, j = ja + jj;
           const int qs = max(qa, qlo(j)), ns = min(qb, qhi(j)) - qs;
+          const int x0 = half * hch * 4, x1 = half == NH - 1 ? f8 : (half + 1) * hch * 4;  // 16-byte pieces of a row
+          float* obh = ob + size_t(half) * nslot * nr;
           float inv_row = 1.f;                          // lane r < ns: 2^e_r of row r
           for (int r = 0; r < ns; ++r) {
             uint4* rp = reinterpret_cast<uint4*>(hbase + size_t(qs - qa + r) * hrow);
             float m = 0.f;
-            for (int ix = lane; ix < f8; ix += 32) {
+            for (int ix = x0 + lane; ix < x1; ix += 32) {
               const uint4 v = rp[ix];
               const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -1184,7 +1191,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             float sc, inv;
             pow2_scale(m, &sc, &inv);
             if (lane == r) inv_row = inv;
-            for (int ix = lane; ix < f8; ix += 32) {
+            for (int ix = x0 + lane; ix < x1; ix += 32) {
               const uint4 v = rp[ix];
               const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
               uint32_t o4[4];
@@ -1219,8 +1226,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
             float acc[NT][4];
 #pragma unroll
             for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-            if (NT == 1 || ns <= 8) fp4_mma_chunks<1>(ar, brow, bval, 0, nchd, acc);
-            else fp4_mma_chunks<NT>(ar, brow, bval, 0, nchd, acc);
+            const int c0 = half * hch, c1 = half == NH - 1 ? nchd : (half + 1) * hch;
+            if (NT == 1 || ns <= 8) fp4_mma_chunks<1>(ar, brow, bval, c0, c1, acc);
+            else fp4_mma_chunks<NT>(ar, brow, bval, c0, c1, acc);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -1233,7 +1241,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
                   if (rho < nr && n < ns) {
                     const int q = qs + n;
                     const int slot = (q < T) ? TK + q : tb->perm[q - T];
-                    ob[size_t(slot) * nr + rho] = gd * (acc[t][2 * hh + jx] * inv_n);
+                    obh[size_t(slot) * nr + rho] = gd * (acc[t][2 * hh + jx] * inv_n);
                   }
                 }
               }
@@ -1254,11 +1262,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
       }
       __syncthreads();
       stamp0(li, kStP2Tasks);
-      // combine: c[t][r] = o_shared + sum_k w[t][k] o[t*K + k], k ascending
+      // combine: c[t][r] = o_shared + sum_k w[t][k] o[t*K + k], k ascending, each o the
+      // sum of its halves of F (16-token bucket)
+      const float* ob1 = ob + size_t(nslot) * nr;
       for (int p = tid; p < T * nr; p += kDecThreads) {
         const int t = p / nr, r = p % nr;
-        float cv = ob[size_t(TK + t) * nr + r];
-        for (int j = 0; j < K; ++j) cv = fmaf(tb->w[t * K + j], ob[size_t(t * K + j) * nr + r], cv);
+        const size_t sh = size_t(TK + t) * nr + r;
+        float cv = NT == 2 ? ob[sh] + ob1[sh] : ob[sh];
+        for (int j = 0; j < K; ++j) {
+          const size_t o = size_t(t * K + j) * nr + r;
+          cv = fmaf(tb->w[t * K + j], NT == 2 ? ob[o] + ob1[o] : ob[o], cv);
+        }
         a.c[size_t(t) * L + r0 + r] = cv;
       }
       release_mb(cx, 1u << kMbScale);

@@ -129,6 +129,10 @@ __device__ void warp_topk_any(const float* row, int E, int K, Cand* cand, int* i
 }
 
 // NJ = E / 32 logits per lane, held in registers (one load each, issued together).
+// The candidates >= tau are compacted by ballots (in j-major order; their order does not
+// matter); up to 32 of them are ranked across the lanes by shuffles, lane l holding
+// candidate l, and the weights computed in place (the largest logit, top0, is the first
+// of the sorted lane maxima).
 template <int NJ>
 __device__ void warp_topk_reg(const float* row, int K, Cand* cand, int* idx, float* w) {
   const int lane = threadIdx.x & 31;
@@ -150,22 +154,40 @@ __device__ void warp_topk_reg(const float* row, int K, Cand* cand, int* idx, flo
     }
   }
   const float tau = __shfl_sync(kFull, s, K - 1);
-  int cnt = 0;
+  const float top0 = __shfl_sync(kFull, s, 0);
+  const unsigned below = (1u << lane) - 1u;
+  int total = 0;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) cnt += v[j] >= tau;
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += t;
+  for (int j = 0; j < NJ; ++j) {
+    const bool p = v[j] >= tau;
+    const unsigned bal = __ballot_sync(kFull, p);
+    const int at = total + __popc(bal & below);
+    if (p && at < kTopkCap) cand[at] = Cand{v[j], j * 32 + lane};
+    total += __popc(bal);
   }
-  const int total = __shfl_sync(kFull, incl, 31);
-  if (total <= kTopkCap) {
-    int at = incl - cnt;
+  __syncwarp();
+  if (total <= 32) {
+    const Cand c = lane < total ? cand[lane] : Cand{-INFINITY, 0x7fffffff};
+    int r = 0;
+#pragma unroll 4
+    for (int q = 0; q < total; ++q) {
+      const float ov = __shfl_sync(kFull, c.v, q);
+      const int oi = __shfl_sync(kFull, c.i, q);
+      r += cand_first(ov, oi, c.v, c.i);
+    }
+    const bool top = lane < total && r < K;
+    const float ev = top ? expf(c.v - top0) : 0.f;
+    float den = ev;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j)
-      if (v[j] >= tau) cand[at++] = Cand{v[j], j * 32 + lane};
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+    if (top) {
+      idx[r] = c.i;
+      w[r] = ev / den;
+    }
     __syncwarp();
+    return;
+  }
+  if (total <= kTopkCap) {
     for (int i = lane; i < total; i += 32) {
       const Cand c = cand[i];
       int r = 0;
@@ -198,8 +220,8 @@ __device__ void warp_topk_reg(const float* row, int K, Cand* cand, int* idx, flo
   }
   __syncwarp();
   const float vk = lane < K ? logit_at(row, idx[lane]) : 0.f;
-  const float top0 = __shfl_sync(kFull, vk, 0);
-  const float ev = lane < K ? expf(vk - top0) : 0.f;
+  const float t0 = __shfl_sync(kFull, vk, 0);
+  const float ev = lane < K ? expf(vk - t0) : 0.f;
   float den = ev;
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
   if (lane < K) w[lane] = ev / den;

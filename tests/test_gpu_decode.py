@@ -130,9 +130,12 @@ def test_token_permutation_invariance_bit_exact(small):
     assert np.array_equal(y, y2)                       # run-to-run deterministic
 
 
-def test_every_token_on_the_same_experts(dev):
-    """A router bias that dominates the logits sends every token to experts 0..k-1."""
-    spec = small_spec(seed=3)
+@pytest.mark.parametrize("shape", ["small", "145b"])
+def test_every_token_on_the_same_experts(dev, shape):
+    """A router bias that dominates the logits sends every token to experts 0..k-1: at
+    T = 16 every routed group has 16 tokens (two token tiles in the MMAs) and, at
+    Edge0-145B shapes, every down group spans two units of the ring."""
+    spec = small_spec(seed=3) if shape == "small" else synth.LayerSpec(seed=3, layer=0, latent=1792)
     inp = synth.make_layer(spec)
     inp.bias = np.zeros(spec.n_experts, np.float32)
     inp.bias[:spec.top_k] = 100.0 + 20.0 * np.arange(spec.top_k, 0, -1, dtype=np.float32)
@@ -231,10 +234,11 @@ def test_layer_145b_t1(dev):
     d.close()
 
 
-@pytest.mark.parametrize("T", [11, 16])
+@pytest.mark.parametrize("T", [4, 8, 11, 16])
 def test_layer_145b_large_buckets(dev, T):
-    """The T = 16 bucket at Edge0-145B shapes: P2 runs in several rounds, with the
-    shared expert's slots split over rounds where its h rows do not fit at once."""
+    """Verify-window buckets at Edge0-145B shapes: several waves of gate/up units
+    through the ring, down units packing several experts, and at T = 16 the shared
+    expert's slots split over two down units where its h rows do not fit one slot."""
     spec = synth.LayerSpec(seed=17, layer=0, latent=1792)
     inp = synth.make_layer(spec)
     d = dev.DeviceLayer(inp, max_tokens=16)

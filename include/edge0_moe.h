@@ -144,7 +144,8 @@ typedef struct {
  * borrowed pointers (which must stay valid for the handle's lifetime) and
  * allocates the workspace for max_tokens (the handle owns only that).
  * Supported shapes: hidden % 64 == 0, latent % 256 == 0, ffn % 128 == 0,
- * 1 <= top_k <= 16, top_k <= n_experts <= 1024, n_experts % 32 == 0.  Launches no kernel.
+ * ffn <= 1024, 1 <= top_k <= 16, top_k <= n_experts <= 1024, n_experts % 32 == 0, and
+ * a decode shared-memory plan that fits the device (else UNSUPPORTED).  Launches no kernel.
  * Returns INVALID_ARG, UNSUPPORTED, CUDA or OOM on failure (*handle_out = NULL).
  */
 edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);

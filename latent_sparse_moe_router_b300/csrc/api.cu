@@ -132,6 +132,7 @@ bool decode_fits(const Handle* hd) {
   const int H = hd->d.hidden, L = hd->d.latent, E = hd->d.n_experts, F = hd->d.ffn, G = hd->num_sms;
   const int ne = (E + G - 1) / G, nr = 2 * ((L / 2 + G - 1) / G), nsr = (F + G - 1) / G, nur = (H + G - 1) / G;
   if ((ne + 7) / 8 + (nr + 15) / 16 > kP0Tiles || ne + nr > 32 || nsr > 32 || (nur + 15) / 16 > kDecWarps) return false;
+  if (F / 8 > 32 * kConvPieces) return false;                           // h rows held in registers
   for (int TB = 1; TB <= kDecodeMaxT; TB *= 2) {
     DecodeArgs a;
     decode_plan(hd, TB, a);

@@ -1201,28 +1201,45 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const __grid
           float inv_row = 1.f;                          // lane r < ns: 2^e_r of row r
           for (int r = 0; r < ns; ++r) {
             uint4* rp = reinterpret_cast<uint4*>(hbase + size_t(qs - qa + r) * hrow);
+            // the half's 16-byte pieces of the row, up to kConvPieces per lane in registers
+            uint4 v[kConvPieces];
             float m = 0.f;
-            for (int ix = x0 + lane; ix < x1; ix += 32) {
-              const uint4 v = rp[ix];
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w4[e])), fabsf(bf16_hi(w4[e]))));
+            for (int i = 0; i < kConvPieces; ++i) {
+              const int ix = x0 + lane + 32 * i;
+              v[i] = ix < x1 ? rp[ix] : make_uint4(0u, 0u, 0u, 0u);
+              const float m01 = fmaxf(fmaxf(fabsf(bf16_lo(v[i].x)), fabsf(bf16_hi(v[i].x))),
+                                      fmaxf(fabsf(bf16_lo(v[i].y)), fabsf(bf16_hi(v[i].y))));
+              const float m23 = fmaxf(fmaxf(fabsf(bf16_lo(v[i].z)), fabsf(bf16_hi(v[i].z))),
+                                      fmaxf(fabsf(bf16_lo(v[i].w)), fabsf(bf16_hi(v[i].w))));
+              m = fmaxf(m, fmaxf(m01, m23));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-            float sc, inv;
-            pow2_scale(m, &sc, &inv);
+            // sc = 2^-e with m * sc in [0.5, 1), from m's exponent field; sc = 1 for a zero
+            // or subnormal max (the row then rounds to f16 zeros)
+            const int ex = int((__float_as_uint(m) >> 23) & 0xFFu);
+            float sc = 1.f, inv = 1.f;
+            if (ex > 0 && ex < 253) {
+              sc = __uint_as_float(uint32_t(253 - ex) << 23);
+              inv = __uint_as_float(uint32_t(ex + 1) << 23);
+            } else if (ex >= 253) {
+              pow2_scale(m, &sc, &inv);
+            }
             if (lane == r) inv_row = inv;
-            for (int ix = x0 + lane; ix < x1; ix += 32) {
-              const uint4 v = rp[ix];
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-              uint32_t o4[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __half2 hv = __floats2half2_rn(bf16_lo(w4[e]) * sc, bf16_hi(w4[e]) * sc);
-                o4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            for (int i = 0; i < kConvPieces; ++i) {
+              const int ix = x0 + lane + 32 * i;
+              if (ix < x1) {
+                const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __half2 hv = __floats2half2_rn(bf16_lo(w4[e]) * sc, bf16_hi(w4[e]) * sc);
+                  o4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                rp[ix] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
               }
-              rp[ix] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
             }
           }
           __syncwarp();

@@ -45,6 +45,7 @@ constexpr int kMbScale = 18;     // fp32 scales of the selected records (P1 -> P
 constexpr int kScaleWarp = 2;    // the warp that copies them (one arrival per lane)
 constexpr int kPartCap = 24;     // P1 partial-sum entries (ring slots x parts of a unit)
 constexpr int kPadElems = 32;    // row padding (16-bit elements) of x, zh and c in shared memory
+constexpr int kConvPieces = 4;   // 16-byte pieces of an h row per lane in the down phase: F <= 1024
 
 // Row pitches (bytes) of rows staged in shared memory: the padding puts rows g and
 // g + 1 of an MMA fragment load in different bank groups.

@@ -15,8 +15,9 @@ What one layer computes for a token, as the pages describe it:
     Coding Agent...", table "Released model variants").
 
 Readings where the pages are silent (each listed in the design notes):
-  * one D and one U per layer (the model card's reading; the "eight groups"
-    of the hardware-requirements page are not modelled);
+  * one D and one U per layer (the model card's reading) in ``layer_forward``;
+    the "eight groups" of the hardware-requirements page are ``GroupedLayer``
+    and ``grouped_layer_forward`` (their readings are in that docstring);
   * the router scores the latent z: logits l = R z + b, R [E, l];
   * top-k by (logit descending, expert index ascending); weights are the
     softmax over all E renormalised over the k kept, which equals
@@ -222,3 +223,94 @@ def stack_forward(layers: list, x_bits: np.ndarray, eps: float = 1e-6):
         trace.append((xb, y))
         xb = residual_rmsnorm(xb, f64_to_bf16(y), eps)
     return xb, trace
+
+
+# ---------------------------------------------------------------- grouped latent projections
+class GroupedLayer(Layer):
+    """A layer whose down and up projections come in G groups.
+
+    "Edge0-145B hardware requirements", section "Edge0-145B latent MoE
+    architecture: how 145B fits one GPU": each layer has eight groups of D and U,
+    every expert carries a label naming the group it uses, and each group of 64
+    experts shares its two matrices; "Edge0-145B · Q3_K" model card, section
+    "Architecture" (diagram caption): D maps the token to the latent per routing
+    group.
+
+    D_bits [G*l, H]: rows g*l .. g*l + l - 1 are D_g.  U_bits [H, G*l]: columns
+    g*l .. g*l + l - 1 are U_g.  labels [E]: the group of each routed expert;
+    shared_group: the group of the shared expert.
+    """
+
+    def __init__(self, D_bits, U_bits, R_bits, bias, expert_source, shared_source,
+                 latent: int, ffn: int, top_k: int, labels, shared_group: int):
+        super().__init__(D_bits, U_bits, R_bits, bias, expert_source, shared_source, latent, ffn, top_k)
+        self.groups = self.D.shape[0] // latent
+        assert self.D.shape[0] == self.groups * latent and self.U.shape[1] == self.groups * latent
+        self.labels = np.asarray(labels, dtype=np.int64)
+        assert self.labels.shape == (self.n_experts,)
+        assert self.labels.min() >= 0 and self.labels.max() < self.groups
+        self.shared_group = int(shared_group)
+        assert 0 <= self.shared_group < self.groups
+
+    def D_group(self, g: int) -> np.ndarray:
+        return self.D[g * self.latent:(g + 1) * self.latent]
+
+    def U_group(self, g: int) -> np.ndarray:
+        return self.U[:, g * self.latent:(g + 1) * self.latent]
+
+
+def grouped_layer_forward(layer: GroupedLayer, x_bits: np.ndarray, idx_override: np.ndarray | None = None,
+                          want: tuple = ()):
+    """One layer with grouped latent projections on tokens x (bf16 bits [T, H]).
+
+    Readings where the pages leave the step open:
+      * z_g = D_g x for every group g (one latent per routing group);
+      * expert e's router row scores its own group's latent: l_e = R_e z_{g(e)} + b_e;
+      * expert e runs on z_{g(e)}, the shared expert on z of its group;
+      * each group combines its own experts: c_g = [g = g_shared] o_shared
+        + sum over kept k with g(e_k) = g of w_k o_k (zero for a group nobody used);
+      * y = sum_g U_g c_g.
+    With one group this is ``layer_forward``.  Returns y and whatever of z, c
+    (both [T, G*l], group-major columns), logits, idx, w, o_shared is in ``want``.
+    """
+    x = bf16_to_f64(x_bits)
+    G, l = layer.groups, layer.latent
+    T = x.shape[0]
+    z = [d_projection(x, layer.D_group(g)) for g in range(G)]
+    logits = np.empty((T, layer.n_experts), dtype=np.float64)
+    for g in range(G):
+        rows = np.nonzero(layer.labels == g)[0]
+        logits[:, rows] = router_logits(z[g], layer.R[rows], None)
+    if layer.bias is not None:
+        logits = logits + np.asarray(layer.bias, dtype=np.float32).astype(np.float64)[None, :]
+    idx = top_k(logits, layer.k) if idx_override is None else np.asarray(idx_override, np.int32)
+    w = routing_weights(logits, idx)
+    c = [np.zeros((T, l), dtype=np.float64) for _ in range(G)]
+    Wg, Wu, Wd = layer.matrices(-1)
+    o_shared = swiglu_expert(z[layer.shared_group], Wg, Wu, Wd)
+    c[layer.shared_group] += o_shared
+    for e in np.unique(idx):
+        g = int(layer.labels[e])
+        t_sel, j_sel = np.nonzero(idx == e)
+        Wg, Wu, Wd = layer.matrices(int(e))
+        c[g][t_sel] += w[t_sel, j_sel][:, None] * swiglu_expert(z[g][t_sel], Wg, Wu, Wd)
+    y = np.zeros((T, layer.U.shape[0]), dtype=np.float64)
+    for g in range(G):
+        y += u_projection(c[g], layer.U_group(g))
+    out = {"y": y}
+    loc = dict(z=np.concatenate(z, axis=1), logits=logits, idx=idx, w=w, c=np.concatenate(c, axis=1),
+               o_shared=o_shared)
+    for name in want:
+        if name in loc:
+            out[name] = loc[name]
+    if any(n in want for n in ("counts", "offsets", "perm", "pos")):
+        counts, offsets, perm, pos = permutation(idx, layer.n_experts)
+        out.update(counts=counts, offsets=offsets, perm=perm, pos=pos)
+    return out
+
+
+def forward(layer: Layer, x_bits: np.ndarray, idx_override: np.ndarray | None = None, want: tuple = ()):
+    """``grouped_layer_forward`` for a GroupedLayer, else ``layer_forward``."""
+    if isinstance(layer, GroupedLayer):
+        return grouped_layer_forward(layer, x_bits, idx_override, want)
+    return layer_forward(layer, x_bits, idx_override, want)

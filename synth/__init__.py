@@ -23,6 +23,11 @@ Distributions (the workload recipe):
     the 47 GB stack on the device while this module regenerates any single
     expert bit-identically on the host.
   * Zipf(s) router bias over a seeded expert order: b_e = -s * ln(rank_e).
+  * Grouped latent projections (G groups): D [G*l, H] and U [H, G*l] drawn like the
+    single D and U (each group's block N(0, 1/fan_in) of that block); group labels
+    from a seeded permutation of the experts, E/G experts per group, so that a
+    group's experts are not contiguous indices; the shared expert in group
+    ``shared_group``.  G = 1 gives the same bytes as the ungrouped layer.
 
 Per-expert logical arrays (the order the generator emits bytes in):
   codes  uint8 [3*F*L/2]  = gate [F][L/2] | up [F][L/2] | down [L][F/2]
@@ -154,7 +159,7 @@ def _normal_bf16(seed, layer, tag, shape, std):
     return f32_to_bf16_bits(a)
 
 
-TAG_X, TAG_D, TAG_U, TAG_R, TAG_ZIPF = 1, 2, 3, 4, 5
+TAG_X, TAG_D, TAG_U, TAG_R, TAG_ZIPF, TAG_GROUP = 1, 2, 3, 4, 5, 6
 
 
 def tokens_bf16(seed: int, T: int, hidden: int = HIDDEN, tag_layer: int = 0):
@@ -170,6 +175,15 @@ def zipf_bias(seed: int, layer: int, n_experts: int = N_EXPERTS, s: float = 1.1)
     return (-s * np.log(rank)).astype(np.float32)
 
 
+def group_labels(seed: int, layer: int, n_experts: int, groups: int) -> np.ndarray:
+    """Group of each expert: a seeded permutation split into G equal parts."""
+    labels = np.zeros(n_experts, dtype=np.int32)
+    if groups > 1:
+        order = np.random.default_rng([seed, layer, TAG_GROUP]).permutation(n_experts)
+        labels[order] = (np.arange(n_experts) * groups // n_experts).astype(np.int32)
+    return labels
+
+
 @dataclass
 class LayerSpec:
     seed: int
@@ -180,6 +194,8 @@ class LayerSpec:
     top_k: int = TOP_K
     ffn: int = FFN
     zipf: float = 0.0          # 0 = uniform routing (no bias)
+    groups: int = 1            # latent groups (D/U pairs)
+    shared_group: int = 0      # group of the shared expert
 
 
 @dataclass
@@ -190,6 +206,7 @@ class LayerInputs:
     U: np.ndarray              # u16 [H, L]
     R: np.ndarray              # u16 [E, L]
     bias: np.ndarray | None    # f32 [E] or None
+    labels: np.ndarray = None  # i32 [E] group of each expert (all 0 for one group)
     _cache: dict = field(default_factory=dict, repr=False)
 
     def expert(self, e: int):
@@ -204,12 +221,13 @@ class LayerInputs:
 
 
 def make_layer(spec: LayerSpec) -> LayerInputs:
-    L, H, E = spec.latent, spec.hidden, spec.n_experts
-    D = _normal_bf16(spec.seed, spec.layer, TAG_D, (L, H), 1.0 / math.sqrt(H))
-    U = _normal_bf16(spec.seed, spec.layer, TAG_U, (H, L), 1.0 / math.sqrt(L))
+    L, H, E, G = spec.latent, spec.hidden, spec.n_experts, spec.groups
+    assert G >= 1 and E % G == 0 and 0 <= spec.shared_group < G
+    D = _normal_bf16(spec.seed, spec.layer, TAG_D, (G * L, H), 1.0 / math.sqrt(H))
+    U = _normal_bf16(spec.seed, spec.layer, TAG_U, (H, G * L), 1.0 / math.sqrt(L))
     R = _normal_bf16(spec.seed, spec.layer, TAG_R, (E, L), 1.0 / math.sqrt(L))
     bias = zipf_bias(spec.seed, spec.layer, E, spec.zipf) if spec.zipf > 0 else None
-    return LayerInputs(spec, D, U, R, bias)
+    return LayerInputs(spec, D, U, R, bias, group_labels(spec.seed, spec.layer, E, G))
 
 
 # The five seeded workloads (shapes and seeds of the stated configurations).

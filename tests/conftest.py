@@ -18,14 +18,19 @@ def oracle_layer(inputs):
     """Oracle view of a synth.LayerInputs (exact decode, experts on demand)."""
     from oracle import moe
     s = inputs.spec
+    if s.groups > 1:
+        return moe.GroupedLayer(inputs.D, inputs.U, inputs.R, inputs.bias, inputs.expert, inputs.shared,
+                                s.latent, s.ffn, s.top_k, inputs.labels, s.shared_group)
     return moe.Layer(inputs.D, inputs.U, inputs.R, inputs.bias,
                      inputs.expert, inputs.shared, s.latent, s.ffn, s.top_k)
 
 
-def tiny_spec(seed=0, layer=0, latent=64, hidden=128, n_experts=16, top_k=3, ffn=32, zipf=0.0):
+def tiny_spec(seed=0, layer=0, latent=64, hidden=128, n_experts=16, top_k=3, ffn=32, zipf=0.0, groups=1,
+              shared_group=0):
     import synth
     return synth.LayerSpec(seed=seed, layer=layer, latent=latent, hidden=hidden,
-                           n_experts=n_experts, top_k=top_k, ffn=ffn, zipf=zipf)
+                           n_experts=n_experts, top_k=top_k, ffn=ffn, zipf=zipf, groups=groups,
+                           shared_group=shared_group)
 
 
 @pytest.fixture

@@ -19,6 +19,16 @@
  * The softmax/top-k rule, tie-break, NVFP4 record layout and this interface
  * are this library's readings; the pages print no formula or layout.
  *
+ * Grouped latent projections (n_groups = G > 1; "Edge0-145B hardware
+ * requirements", same section: eight groups of D and U per layer, each shared
+ * by 64 experts, every expert labelled with its group; model card, section
+ * "Architecture": D maps the token to the latent per routing group):
+ *   z_g = D_g x for every group g;  l_e = R_e . z_(g(e)) + b_e
+ *   expert e runs on z_(g(e)), the shared expert on z of shared_group
+ *   c_g = [g = shared_group] o_shared + sum over kept k with g(e_k) = g of w_k o_(e_k)
+ *   y = sum_g U_g c_g
+ * With G = 1 this is the layer above.
+ *
  * Conventions for every call:
  *   - Pointers named "device" point to CUDA device memory of the current device;
  *     "host" pointers to host memory.  The caller owns every buffer it passes.
@@ -122,7 +132,7 @@ edge0_status edge0_quantize_nvfp4(const float *w, int rows, int K, float g,
                                   uint8_t *codes, uint8_t *scales,
                                   edge0_stream_t stream);
 
-/* One layer's shapes and borrowed device weights. */
+/* One layer's shapes and borrowed device weights.  G = max(1, n_groups). */
 typedef struct {
   int hidden;     /* 2560 */
   int latent;     /* l: 1792 (145B) or 1280 (120B); multiple of 256 */
@@ -130,13 +140,17 @@ typedef struct {
   int top_k;      /* 10 */
   int ffn;        /* SwiGLU width 640; multiple of 128 */
   int max_tokens; /* largest T forward will accept (workspace sizing) */
-  const void *D;            /* device bf16 [latent][hidden] */
-  const void *U;            /* device bf16 [hidden][latent] */
+  const void *D;            /* device bf16 [G*latent][hidden]: rows g*latent.. are D_g */
+  const void *U;            /* device bf16 [hidden][G*latent]: columns g*latent.. are U_g */
   const void *router;       /* device bf16 [n_experts][latent] */
   const float *router_bias; /* device fp32 [n_experts], or NULL for zeros */
   const void *experts;      /* device, n_experts records, 256-byte aligned */
   size_t expert_stride;     /* bytes between records; multiple of 256 */
   const void *shared_expert;/* device, one record, 256-byte aligned */
+  int n_groups;             /* latent groups: 0 or 1 = one D/U pair; at most 16 */
+  const int *expert_group;  /* G > 1: device int32 [n_experts], group of each routed
+                               expert in [0, G); read once by edge0_moe_create */
+  int shared_group;         /* G > 1: group of the shared expert, in [0, G) */
 } edge0_moe_desc;
 
 /*
@@ -145,7 +159,11 @@ typedef struct {
  * allocates the workspace for max_tokens (the handle owns only that).
  * Supported shapes: hidden % 64 == 0, latent % 256 == 0, ffn % 128 == 0,
  * ffn <= 1024, 1 <= top_k <= 16, top_k <= n_experts <= 1024, n_experts % 32 == 0, and
- * a decode shared-memory plan that fits the device (else UNSUPPORTED).  Launches no kernel.
+ * a decode shared-memory plan that fits the device (else UNSUPPORTED).  A grouped
+ * layer (G > 1) also needs G * latent <= 16384, latent <= 2048 and valid labels
+ * (else INVALID_ARG); it allocates workspace for max(max_tokens, 16) tokens.
+ * Runs the router fold and the |z| bound on the device (legacy stream) and
+ * synchronises before returning.
  * Returns INVALID_ARG, UNSUPPORTED, CUDA or OOM on failure (*handle_out = NULL).
  */
 edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);
@@ -154,7 +172,8 @@ edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);
  * y = Layer(x) for T tokens.  x device bf16 [T][hidden]; y device bf16
  * [T][hidden] (round to nearest even); x and y must not overlap.
  * T = 0 is a no-op; T > max_tokens returns INVALID_ARG.  T <= 16 runs the
- * decode path (one persistent kernel); larger T the prefill path.
+ * decode path (one persistent kernel); larger T the prefill path.  A grouped
+ * layer (G > 1) runs the prefill path's kernels at every T.
  * Calls on one handle must be ordered (one stream, or synchronised): they
  * share the handle's workspace.
  */
@@ -178,15 +197,16 @@ edge0_status edge0_moe_debug_routing(void *handle, int *idx, float *w, int *coun
 
 /*
  * Copy an intermediate of the last forward (for stage-by-stage parity):
- *   what = 0: latent z [T][latent]; 1: router logits fp32 [T][n_experts];
- *   2: combined latent c [T][latent].  After a decode forward (T <= 16) z and
+ *   what = 0: latent z [T][G*latent]; 1: router logits fp32 [T][n_experts];
+ *   2: combined latent c [T][G*latent].  After a decode forward (T <= 16) z and
  *   c are fp32.  After a prefill forward (T > 16) they are in the form the
  *   experts and U consume: z as f16 z_t * 2^-e_t, with e_t the binary exponent
  *   of the bound max_r sum_h |D_rh| * max_h |x_t,h| (so every value is below 1
  *   in magnitude), and c as bf16.  After a prefill forward also what = 3: the
  *   SwiGLU activations H bf16 [T*top_k + T][ffn] and 4: the expert outputs O
  *   bf16 [T*top_k + T][latent], rows in grouped position order (the shared
- *   expert's T rows last).  dst device, `bytes` >= size.
+ *   expert's T rows last).  A grouped layer's forwards are prefill forwards at
+ *   every T.  dst device, `bytes` >= size.
  * Returns UNSUPPORTED if no forward has run yet, INVALID_ARG for other `what`.
  */
 edge0_status edge0_moe_debug_tensor(void *handle, int what, void *dst, size_t bytes,
@@ -216,8 +236,8 @@ edge0_status edge0_residual_rmsnorm(const void *x, const void *y, void *out, int
  *   x_0 = x;  x_{i+1} = RMSNorm(x_i + Layer_i(x_i));  y = x_n
  * handles: host array of n_layers handles of identical shapes; T <= 16
  * (decode) runs all layers in one persistent kernel.  x, y device bf16
- * [T][hidden], may be the same buffer.  Larger T chains forward and
- * edge0_residual_rmsnorm per layer.
+ * [T][hidden], may be the same buffer.  Larger T, or any grouped layer, chains
+ * forward and edge0_residual_rmsnorm per layer.
  * The decode kernel reads a small device table of the layers, held by
  * handles[0]: a call with a list of layers different from the previous call's
  * uploads it (stream-ordered).  A call captured into a CUDA graph must use the
@@ -251,10 +271,10 @@ edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, c
  *             EDGE0_OK or the device error bits (a wait that ran out)
  * Scratch lives in one static device array of this library (about 7.8 MB, held
  * by every GPU that loads the library until the process exits).  Limits:
- * T <= 16, hidden <= 3072, latent <= 2048, n_experts <= 512, ffn <= 1024, and
- * the decode kernel's shared-memory plan must fit the device (the check
- * edge0_moe_create makes); other sizes return EDGE0_ERR_UNSUPPORTED without
- * launching anything.
+ * T <= 16, hidden <= 3072, latent <= 2048, n_experts <= 512, ffn <= 1024, one
+ * latent group (n_groups 0 or 1), and the decode kernel's shared-memory plan
+ * must fit the device (the check edge0_moe_create makes); other sizes return
+ * EDGE0_ERR_UNSUPPORTED without launching anything.
  * The first call on a device looks up the array's device address and sets the
  * decode kernel's launch attributes (once per device, with that device
  * current): make that first call before any stream capture.  All calls share
@@ -328,8 +348,9 @@ edge0_status edge0_moe_decode_phase_times(void *handle, float *us, int max, int 
  *   with the mapped flag), 256-byte aligned; caller-owned, valid until detach.
  *   Allocates n_slots device slots (all empty at first) and a staging area of
  *   16 * top_k records.  From then on the handle ignores desc.experts.  Requires a
- *   handle created with max_tokens <= 16 (prefill forwards read every record from
- *   device memory: UNSUPPORTED); a second attach is UNSUPPORTED.  Synchronises.
+ *   handle created with max_tokens <= 16 and one latent group (prefill forwards,
+ *   which grouped layers run at every T, read every record from device memory:
+ *   UNSUPPORTED); a second attach is UNSUPPORTED.  Synchronises.
  * edge0_moe_tier_place: puts expert slot_expert[k] (host int [n_slots], -1 =
  *   empty, no expert twice) into slot k, copying the records on `stream` and
  *   updating the table; synchronises `stream`.

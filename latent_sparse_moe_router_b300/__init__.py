@@ -54,6 +54,7 @@ class edge0_moe_desc(ctypes.Structure):
         ("D", ctypes.c_void_p), ("U", ctypes.c_void_p), ("router", ctypes.c_void_p),
         ("router_bias", ctypes.c_void_p), ("experts", ctypes.c_void_p),
         ("expert_stride", ctypes.c_size_t), ("shared_expert", ctypes.c_void_p),
+        ("n_groups", ctypes.c_int), ("expert_group", ctypes.c_void_p), ("shared_group", ctypes.c_int),
     ]
 
 
@@ -169,10 +170,11 @@ def edge0_quantize_nvfp4(w, rows, K, g, codes, scales, stream=None):
 
 # ------------------------------------------------------------------ layer
 def edge0_moe_create(hidden, latent, n_experts, top_k, ffn, max_tokens, D, U, router, router_bias,
-                     experts, expert_stride, shared_expert) -> int:
+                     experts, expert_stride, shared_expert, n_groups=1, expert_group=None,
+                     shared_group=0) -> int:
     d = edge0_moe_desc(hidden, latent, n_experts, top_k, ffn, max_tokens, _ptr(D), _ptr(U),
                        _ptr(router), _ptr(router_bias), _ptr(experts), expert_stride,
-                       _ptr(shared_expert))
+                       _ptr(shared_expert), n_groups, _ptr(expert_group), shared_group)
     h = ctypes.c_void_p()
     _check(lib().edge0_moe_create(ctypes.byref(d), ctypes.byref(h)), "edge0_moe_create")
     return h.value
@@ -333,12 +335,15 @@ class MoELayer:
     """A layer handle plus references to the device tensors it borrows."""
 
     def __init__(self, *, hidden, latent, n_experts, top_k, ffn, max_tokens, D, U, router,
-                 router_bias, experts, expert_stride, shared_expert):
+                 router_bias, experts, expert_stride, shared_expert, n_groups=1, expert_group=None,
+                 shared_group=0):
         self._keep = (D, U, router, router_bias, experts, shared_expert)
         self.hidden, self.latent, self.n_experts, self.top_k, self.ffn = hidden, latent, n_experts, top_k, ffn
         self.max_tokens = max_tokens
+        self.n_groups = n_groups
         self.handle = edge0_moe_create(hidden, latent, n_experts, top_k, ffn, max_tokens, D, U, router,
-                                       router_bias, experts, expert_stride, shared_expert)
+                                       router_bias, experts, expert_stride, shared_expert, n_groups,
+                                       expert_group, shared_group)
 
     def forward(self, x, y, T=None, stream=None):
         edge0_moe_forward(self.handle, x, y, x.shape[0] if T is None else T, stream)

@@ -25,6 +25,7 @@ using namespace edge0;
 namespace {
 
 constexpr int kStackMax = 64;
+constexpr int kMaxGroups = 16;     // latent groups (D/U pairs) per layer
 
 struct Handle {
   edge0_moe_desc d;
@@ -40,7 +41,9 @@ struct Handle {
   int* idx = nullptr; float* w = nullptr; int* counts = nullptr; int* offsets = nullptr;
   int* perm = nullptr; int* pos = nullptr;
   GridBarrier* bar = nullptr; int* err = nullptr;
-  float* rd = nullptr;        // R D, fp32 [n_experts][hidden]
+  float* rd = nullptr;        // R D, fp32 [n_experts][hidden] (grouped: row e = R_e D_(g(e)))
+  int groups = 1;             // latent groups G (d.n_groups normalised to >= 1)
+  int* labels = nullptr;      // G > 1: device copy of the experts' group labels (d.expert_group points here)
   float dnorm = 0.f;          // max_r sum_h |D[r][h]|
   __half* zh = nullptr;       // f16 copy of z for the decode experts
   LayerW* d_layer = nullptr;  // this layer (1 entry)
@@ -208,9 +211,11 @@ __global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __
 
 // RD[e][h] = sum_l R[e][l] * D[l][h] in fp32 (the router folded with the
 // down-projection, so decode computes the logits from x directly).  32x32 output
-// tiles, K staged through shared memory in fixed order.
+// tiles, K staged through shared memory in fixed order.  With grouped projections
+// (labels non-null) D is D_g and only the rows of the experts labelled g are written.
 __global__ void fold_router_kernel(const __nv_bfloat16* __restrict__ R, const __nv_bfloat16* __restrict__ D,
-                                   float* __restrict__ RD, int E, int L, int H) {
+                                   float* __restrict__ RD, int E, int L, int H, const int* __restrict__ labels,
+                                   int g) {
   __shared__ float rs[32][33];
   __shared__ float ds[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
@@ -232,7 +237,7 @@ __global__ void fold_router_kernel(const __nv_bfloat16* __restrict__ R, const __
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = e0 + ty + 8 * j;
-    if (e < E && h0 + tx < H) RD[size_t(e) * H + h0 + tx] = acc[j];
+    if (e < E && h0 + tx < H && (!labels || labels[e] == g)) RD[size_t(e) * H + h0 + tx] = acc[j];
   }
 }
 
@@ -432,9 +437,30 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
     return EDGE0_ERR_INVALID_ARG;
   if (d.expert_stride < edge0_expert_record_bytes(d.latent, d.ffn) || d.expert_stride % 256)
     return EDGE0_ERR_INVALID_ARG;
+  // grouped latent projections: G D/U pairs, a group label per routed expert
+  const int G = d.n_groups > 1 ? d.n_groups : 1;
+  std::vector<int> labels;
+  if (d.n_groups < 0 || d.n_groups > kMaxGroups) return EDGE0_ERR_INVALID_ARG;
+  if (G > 1) {
+    if (size_t(G) * d.latent > 16384 || d.latent > 2048 || !d.expert_group || !aligned(d.expert_group, 4) ||
+        d.shared_group < 0 || d.shared_group >= G)
+      return EDGE0_ERR_INVALID_ARG;
+    labels.resize(d.n_experts);
+    if (cudaMemcpy(labels.data(), d.expert_group, sizeof(int) * d.n_experts, cudaMemcpyDeviceToHost) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return EDGE0_ERR_INVALID_ARG;
+    }
+    for (int v : labels)
+      if (v < 0 || v >= G) return EDGE0_ERR_INVALID_ARG;
+  }
 
   Handle* hd = new Handle();
   hd->d = d;
+  hd->d.n_groups = G;
+  hd->d.shared_group = G > 1 ? d.shared_group : 0;
+  hd->d.expert_group = nullptr;
+  hd->groups = G;
   cudaError_t ce = cudaGetDevice(&hd->device);
   cudaDeviceProp prop;
   if (ce == cudaSuccess) ce = cudaGetDeviceProperties(&prop, hd->device);
@@ -442,12 +468,14 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   if (prop.major < 10 || !prop.cooperativeLaunch) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
   hd->num_sms = prop.multiProcessorCount;
   hd->smem_total = (int)prop.sharedMemPerBlockOptin - 1024;
-  if (!decode_fits(hd)) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
-  if ((ce = decode_prepare(hd->smem_total)) != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
-  int occ = 0;
-  if ((ce = decode_occupancy(hd->smem_total, &occ)) != cudaSuccess || occ < 1) {
-    delete hd;
-    return ce != cudaSuccess ? EDGE0_ERR_CUDA : EDGE0_ERR_UNSUPPORTED;
+  if (G == 1) {                     // the decode kernel serves one latent group
+    if (!decode_fits(hd)) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
+    if ((ce = decode_prepare(hd->smem_total)) != cudaSuccess) { delete hd; return EDGE0_ERR_CUDA; }
+    int occ = 0;
+    if ((ce = decode_occupancy(hd->smem_total, &occ)) != cudaSuccess || occ < 1) {
+      delete hd;
+      return ce != cudaSuccess ? EDGE0_ERR_CUDA : EDGE0_ERR_UNSUPPORTED;
+    }
   }
 
   // workspace
@@ -468,7 +496,12 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   const size_t o_bar = take(sizeof(GridBarrier)), o_err = take(sizeof(int));
   const size_t o_lw = take(sizeof(LayerW)), o_st = take(sizeof(LayerW) * kStackMax);
   const size_t o_rd = take(size_t(E) * H * 4);
-  const size_t o_pf = take(prefill_workspace_bytes(d, d.max_tokens));
+  const size_t o_lab = take(size_t(E) * 4);
+  // grouped layers run the prefill kernels at every T (at least the decode sizes)
+  const int pf_tokens = G > 1 ? std::max(d.max_tokens, TD) : d.max_tokens;
+  const size_t pf_bytes = prefill_workspace_bytes(hd->d, pf_tokens);
+  if (G > 1 && pf_bytes == 0) { delete hd; return EDGE0_ERR_UNSUPPORTED; }
+  const size_t o_pf = take(pf_bytes);
   hd->ws_bytes = off;
   if (cudaMalloc(&hd->ws, hd->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -486,26 +519,33 @@ edge0_status edge0_moe_create(const edge0_moe_desc* desc, void** handle_out) {
   hd->bar = (GridBarrier*)(b + o_bar); hd->err = (int*)(b + o_err);
   hd->d_layer = (LayerW*)(b + o_lw); hd->d_stack = (LayerW*)(b + o_st);
   hd->rd = (float*)(b + o_rd);
-  prefill_workspace_carve(d, d.max_tokens, b + o_pf, &hd->pf);
+  if (G > 1) {
+    hd->labels = (int*)(b + o_lab);
+    hd->d.expert_group = hd->labels;
+  }
+  prefill_workspace_carve(hd->d, pf_tokens, b + o_pf, &hd->pf);
   hd->pf.idx = hd->idx; hd->pf.w = hd->w; hd->pf.counts = hd->counts; hd->pf.offsets = hd->offsets;
   hd->pf.perm = hd->perm; hd->pf.pos = hd->pos;
   hd->pf.err = hd->err;
   hd->pf.rd = hd->rd;
   ce = cudaMemset(hd->ws, 0, o_lw);
+  if (ce == cudaSuccess && G > 1)
+    ce = cudaMemcpy(hd->labels, labels.data(), sizeof(int) * E, cudaMemcpyHostToDevice);
   if (ce == cudaSuccess) {
-    row_l1_max_kernel<<<(L + 7) / 8, 256>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, d_dnorm);
+    row_l1_max_kernel<<<(G * L + 7) / 8, 256>>>(static_cast<const __nv_bfloat16*>(d.D), G * L, H, d_dnorm);
     ce = cudaGetLastError();
   }
   if (ce == cudaSuccess) ce = cudaMemcpy(&hd->dnorm, d_dnorm, sizeof(float), cudaMemcpyDeviceToHost);
   hd->pf.dnorm = hd->dnorm;
   const LayerW lw = layer_of(hd);
-  if (ce == cudaSuccess) {
+  for (int g = 0; g < G && ce == cudaSuccess; ++g) {   // grouped: row e folds with D_(g(e))
     fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256>>>(
-        static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), hd->rd, E, L, H);
+        static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D) + size_t(g) * L * H,
+        hd->rd, E, L, H, hd->labels, g);
     ce = cudaGetLastError();
   }
   if (ce == cudaSuccess) ce = cudaMemcpy(hd->d_layer, &lw, sizeof(lw), cudaMemcpyHostToDevice);
-  if (ce == cudaSuccess) ce = prefill_init(d, &hd->pf, hd->num_sms);
+  if (ce == cudaSuccess) ce = prefill_init(hd->d, &hd->pf, hd->num_sms);
   // the fold and the initialisation above ran on the legacy stream: finish them
   // before the handle is used from any stream
   if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
@@ -529,7 +569,7 @@ edge0_status edge0_moe_forward(void* handle, const void* x, void* y, int T, edge
   const char* xc = static_cast<const char*>(x);
   const char* yc = static_cast<const char*>(y);
   if (xc < yc + xy && yc < xc + xy) return EDGE0_ERR_INVALID_ARG;
-  if (T <= kDecodeMaxT) {
+  if (T <= kDecodeMaxT && hd->groups == 1) {
     DecodeArgs a;
     fill_decode_args(hd, a, x, y, T);
     if (attach_stamps(hd, a, 1, (cudaStream_t)stream) != cudaSuccess) return EDGE0_ERR_CUDA;
@@ -539,7 +579,7 @@ edge0_status edge0_moe_forward(void* handle, const void* x, void* y, int T, edge
     hd->last_path = 1;
     return EDGE0_OK;
   }
-  if (T > hd->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
+  if (T > hd->pf.max_tokens) return EDGE0_ERR_INVALID_ARG;
   if (hd->tiered) return EDGE0_ERR_UNSUPPORTED;   // prefill reads every record from device memory
   const edge0_status st = prefill_forward(hd->d, &hd->pf, hd->num_sms,
                                           static_cast<const __nv_bfloat16*>(x),
@@ -618,15 +658,15 @@ static edge0_status stack_impl(void* const* handles, int n_layers, const void* x
     const Handle* hi = static_cast<const Handle*>(handles[i]);
     if (!hi || hi->d.hidden != h0->d.hidden || hi->d.latent != h0->d.latent ||
         hi->d.n_experts != h0->d.n_experts || hi->d.top_k != h0->d.top_k || hi->d.ffn != h0->d.ffn ||
-        hi->device != h0->device)
+        hi->groups != h0->groups || hi->device != h0->device)
       return EDGE0_ERR_INVALID_ARG;
   }
-  if (T > kDecodeMaxT || n_layers > kStackMax) {
+  if (T > kDecodeMaxT || n_layers > kStackMax || h0->groups > 1) {
     if (trace_x || trace_y || trace_idx) return EDGE0_ERR_UNSUPPORTED;
     for (int i = 0; i < n_layers; ++i)
       if (static_cast<const Handle*>(handles[i])->tiered) return EDGE0_ERR_UNSUPPORTED;
     // chain: layer forward into the prefill scratch of handle 0, then the residual norm
-    if (T > h0->d.max_tokens) return EDGE0_ERR_INVALID_ARG;
+    if (T > h0->pf.max_tokens) return EDGE0_ERR_INVALID_ARG;
     __nv_bfloat16* tmp = prefill_stack_scratch(&h0->pf);
     if (!tmp) return EDGE0_ERR_UNSUPPORTED;
     const void* cur = x;
@@ -819,7 +859,7 @@ edge0_status edge0_moe_tier_attach(void* handle, const void* host_records, int n
   Handle* hd = static_cast<Handle*>(handle);
   if (!hd || !host_records || n_slots < 0 || n_slots > hd->d.n_experts) return EDGE0_ERR_INVALID_ARG;
   if (hd->tiered) return EDGE0_ERR_UNSUPPORTED;
-  if (hd->d.max_tokens > kDecodeMaxT) return EDGE0_ERR_UNSUPPORTED;   // tiering serves decode forwards
+  if (hd->d.max_tokens > kDecodeMaxT || hd->groups > 1) return EDGE0_ERR_UNSUPPORTED;   // decode forwards only
   void* dev = nullptr;
   if (cudaHostGetDevicePointer(&dev, const_cast<void*>(host_records), 0) != cudaSuccess || !dev) {
     cudaGetLastError();
@@ -1048,8 +1088,9 @@ extern "C" edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc* desc, co
       (d.router_bias && !aligned(d.router_bias, 4)) ||
       d.expert_stride < edge0_expert_record_bytes(d.latent, d.ffn) || d.expert_stride % 256)
     return EDGE0_ERR_INVALID_ARG;
-  // sizes beyond what the static scratch holds
-  if (T > kNaMaxT || d.hidden > kNaMaxH || d.latent > kNaMaxL || d.n_experts > kNaMaxE || d.ffn > kNaMaxF)
+  // sizes beyond what the static scratch holds; grouped projections run on handles only
+  if (T > kNaMaxT || d.hidden > kNaMaxH || d.latent > kNaMaxL || d.n_experts > kNaMaxE || d.ffn > kNaMaxF ||
+      d.n_groups > 1)
     return EDGE0_ERR_UNSUPPORTED;
   if (T == 0) return EDGE0_OK;
   if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return EDGE0_ERR_INVALID_ARG;
@@ -1099,7 +1140,8 @@ extern "C" edge0_status edge0_moe_forward_noalloc(const edge0_moe_desc* desc, co
   // kernel scales z per token by a power of two from that bound, as on a handle)
   const int H = d.hidden, L = d.latent, E = d.n_experts;
   fold_router_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256, 0, cs>>>(
-      static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), view.rd, E, L, H);
+      static_cast<const __nv_bfloat16*>(d.router), static_cast<const __nv_bfloat16*>(d.D), view.rd, E, L, H,
+      nullptr, 0);
   row_l1_max_kernel<<<(L + 7) / 8, 256, 0, cs>>>(static_cast<const __nv_bfloat16*>(d.D), L, H, dnorm_dev);
   if (cudaGetLastError() != cudaSuccess) return EDGE0_ERR_CUDA;
   DecodeArgs a;

@@ -19,6 +19,11 @@
 //   7. grouped NVFP4 GEMM down -> O bf16;
 //   8. combine c[t] = O[shared t] + sum_k w[t,k] O[pos[t,k]] in fixed k order;
 //   9. tcgen05 GEMM  c x U^T -> y bf16 (round to nearest even).
+// Grouped latent projections (G D/U pairs, a group label per expert): step 1's D is
+// the G stacked D_g (z is [T][G l]), the router fold uses each expert's own D_g,
+// step 5 gathers the latent of each expert's group, the shared expert reads its
+// group's latent, step 8 adds each expert into its group's block of c [T][G l], and
+// step 9 contracts over all G l columns (U [H][G l]): y = sum_g U_g c_g.
 #include <algorithm>
 
 #include "gemm_pair.cuh"
@@ -35,8 +40,11 @@ constexpr int kPfBox = 128, kPfStages = 6;   // CTA-pair GEMM: 128-row B halves,
 
 size_t pf_align(size_t v) { return (v + 1023) & ~size_t(1023); }
 
+int pf_groups(const edge0_moe_desc& d) { return d.n_groups > 1 ? d.n_groups : 1; }
+
 bool prefill_shapes_ok(const edge0_moe_desc& d) {
-  return d.latent <= 2048 && d.ffn <= 2048 && d.n_experts <= 1024 && d.hidden % 64 == 0;
+  return d.latent <= 2048 && d.ffn <= 2048 && d.n_experts <= 1024 && d.hidden % 64 == 0 &&
+         size_t(pf_groups(d)) * d.latent <= 16384;
 }
 
 // ------------------------------------------------------------------ kernels
@@ -375,16 +383,22 @@ __global__ void __launch_bounds__(256) token_scale_kernel(const __nv_bfloat16* _
   }
 }
 
-// zg[p] = zh[perm[p] / K] and its scale: one warp per row, 16-byte copies.
+// zg[p] = the latent of token perm[p] / K (with grouped projections: of the group
+// labels[e] of its expert e = idx[perm[p]], columns labels[e] L .. of a row of ld
+// elements; labels = null: one group, ld = L) and its scale: one warp per row,
+// 16-byte copies.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restrict__ zh,
                                                           const float* __restrict__ zinv,
                                                           const int* __restrict__ perm, int TK, int K, int L,
+                                                          const int* __restrict__ idx,
+                                                          const int* __restrict__ labels, int ld,
                                                           __half* __restrict__ zg, float* __restrict__ pos_inv) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n16 = L / 8;
   for (int p = blockIdx.x * 8 + warp; p < TK; p += gridDim.x * 8) {
-    const int t = perm[p] / K;
-    const uint4* src = reinterpret_cast<const uint4*>(zh + size_t(t) * L);
+    const int s = perm[p], t = s / K;
+    const size_t col = labels ? size_t(labels[idx[s]]) * L : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(zh + size_t(t) * ld + col);
     uint4* dst = reinterpret_cast<uint4*>(zg + size_t(p) * L);
     for (int i = lane; i < n16; i += 32) dst[i] = src[i];
     if (lane == 0) pos_inv[p] = zinv[t];
@@ -425,6 +439,50 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ ob, const int* 
   *reinterpret_cast<uint4*>(cb + size_t(t) * L + j) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Grouped projections: c[t][g L + j] = [g = gs] O[TK + t][j] + sum over k with
+// labels[idx[t,k]] = g of w[t,k] O[pos[t,k]][j]  (fp32, k in rank order) -> bf16;
+// a group nobody used gets zeros.  Block = one token, thread = 8 columns of the
+// G L wide row at a time.
+__global__ void __launch_bounds__(256) combine_grouped_kernel(const __nv_bfloat16* __restrict__ ob,
+                                                              const int* __restrict__ pos,
+                                                              const float* __restrict__ w,
+                                                              const int* __restrict__ idx,
+                                                              const int* __restrict__ labels, int gs, int T,
+                                                              int K, int L, int G,
+                                                              __nv_bfloat16* __restrict__ cb) {
+  const int t = blockIdx.x, GL = G * L;
+  const size_t TK = size_t(T) * K;
+  for (int col = threadIdx.x * 8; col < GL; col += blockDim.x * 8) {
+    const int g = col / L, j = col - g * L;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (g == gs) {
+      const uint4 u = *reinterpret_cast<const uint4*>(ob + (TK + t) * L + j);
+      const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { acc[2 * i] = bf16_lo(uu[i]); acc[2 * i + 1] = bf16_hi(uu[i]); }
+    }
+    for (int k = 0; k < K; ++k) {
+      if (labels[idx[size_t(t) * K + k]] != g) continue;
+      const int p = pos[size_t(t) * K + k];
+      const float wk = w[size_t(t) * K + k];
+      const uint4 u = *reinterpret_cast<const uint4*>(ob + size_t(p) * L + j);
+      const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wk, bf16_lo(uu[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wk, bf16_hi(uu[i]), acc[2 * i + 1]);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(cb + size_t(t) * GL + col) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int num_sms, cudaStream_t s) {
   static int max_pairs = 0;
   cudaLaunchConfig_t cfg = {};
@@ -458,12 +516,14 @@ cudaError_t launch_grouped(const GgMaps& maps, const GgParams& p, int num_sms, c
 
 // ------------------------------------------------------------------ workspace
 size_t prefill_workspace_bytes(const edge0_moe_desc& d, int max_tokens) {
-  if (max_tokens <= 16 || !prefill_shapes_ok(d)) return 0;
+  // one group: T <= 16 runs the decode kernel; grouped layers run these kernels at every T
+  if ((max_tokens <= 16 && pf_groups(d) == 1) || max_tokens < 1 || !prefill_shapes_ok(d)) return 0;
   const size_t T = max_tokens, H = d.hidden, L = d.latent, E = d.n_experts, K = d.top_k, F = d.ffn;
+  const size_t GL = size_t(pf_groups(d)) * L;
   const size_t nch = (T + kChunk - 1) / kChunk;
   size_t n = 0;
   n += pf_align(2 * E * H * 2);               // rdcat
-  n += pf_align(T * L * 2);                   // zh
+  n += pf_align(T * GL * 2);                  // zh
   n += pf_align(T * 4) * 2;                   // zsc, zinv
   n += pf_align((T * K + T) * 4);             // pos_inv
   n += pf_align(T * E * 4);                   // logits
@@ -472,7 +532,7 @@ size_t prefill_workspace_bytes(const edge0_moe_desc& d, int max_tokens) {
   n += pf_align(T * K * L * 2);               // zg
   n += pf_align((T * K + T) * F * 2);         // hb
   n += pf_align((T * K + T) * L * 2);         // ob
-  n += pf_align(T * L * 2);                   // cb
+  n += pf_align(T * GL * 2);                  // cb
   n += pf_align(T * H * 2);                   // scratch
   n += pf_align(4);                           // abort
   return n;
@@ -482,11 +542,12 @@ void prefill_workspace_carve(const edge0_moe_desc& d, int max_tokens, char* base
   pf->max_tokens = max_tokens;
   if (prefill_workspace_bytes(d, max_tokens) == 0) return;
   const size_t T = max_tokens, H = d.hidden, L = d.latent, E = d.n_experts, K = d.top_k, F = d.ffn;
+  const size_t GL = size_t(pf_groups(d)) * L;
   const size_t nch = (T + kChunk - 1) / kChunk;
   size_t o = 0;
   auto take = [&](size_t bytes) { char* p = base + o; o += pf_align(bytes); return p; };
   pf->rdcat = reinterpret_cast<__nv_bfloat16*>(take(2 * E * H * 2));
-  pf->zh = reinterpret_cast<__half*>(take(T * L * 2));
+  pf->zh = reinterpret_cast<__half*>(take(T * GL * 2));
   pf->zsc = reinterpret_cast<float*>(take(T * 4));
   pf->zinv = reinterpret_cast<float*>(take(T * 4));
   pf->pos_inv = reinterpret_cast<float*>(take((T * K + T) * 4));
@@ -496,7 +557,7 @@ void prefill_workspace_carve(const edge0_moe_desc& d, int max_tokens, char* base
   pf->zg = reinterpret_cast<__half*>(take(T * K * L * 2));
   pf->hb = reinterpret_cast<__nv_bfloat16*>(take((T * K + T) * F * 2));
   pf->ob = reinterpret_cast<__nv_bfloat16*>(take((T * K + T) * L * 2));
-  pf->cb = reinterpret_cast<__nv_bfloat16*>(take(T * L * 2));
+  pf->cb = reinterpret_cast<__nv_bfloat16*>(take(T * GL * 2));
   pf->scratch = reinterpret_cast<__nv_bfloat16*>(take(T * H * 2));
   pf->abort = reinterpret_cast<int*>(take(4));
 }
@@ -504,6 +565,7 @@ void prefill_workspace_carve(const edge0_moe_desc& d, int max_tokens, char* base
 cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_sms) {
   if (!pf->rdcat) return cudaSuccess;
   const int H = d.hidden, L = d.latent, E = d.n_experts, K = d.top_k, F = d.ffn;
+  const int G = pf_groups(d), GL = G * L, gs = G > 1 ? d.shared_group : 0;
   const size_t T = pf->max_tokens, TK = T * K;
   split_rd_kernel<<<num_sms * 4, 256>>>(pf->rd, pf->rdcat, E, H);
   cudaError_t e = cudaGetLastError();
@@ -515,10 +577,10 @@ cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_
   const uint64_t gu_row = 9ull * L / 8, d_pair = 9ull * F / 8, d_block = uint64_t(F) * gu_row;
   bool ok = true;
   // dense GEMM operands
-  ok &= make_tmap_2d(&pf->m_D, d.D, BF, 2, L, H, uint64_t(H) * 2, 64, kPfBox, SW);
+  ok &= make_tmap_2d(&pf->m_D, d.D, BF, 2, GL, H, uint64_t(H) * 2, 64, kPfBox, SW);
   ok &= make_tmap_2d(&pf->m_rdcat, pf->rdcat, BF, 2, 2ull * E, H, uint64_t(H) * 2, 64, kPfBox, SW);
-  ok &= make_tmap_2d(&pf->m_U, d.U, BF, 2, H, L, uint64_t(L) * 2, 64, kPfBox, SW);
-  ok &= make_tmap_2d(&pf->m_cb, pf->cb, BF, 2, T, L, uint64_t(L) * 2, 64, 128, SW);
+  ok &= make_tmap_2d(&pf->m_U, d.U, BF, 2, H, GL, uint64_t(GL) * 2, 64, kPfBox, SW);
+  ok &= make_tmap_2d(&pf->m_cb, pf->cb, BF, 2, T, GL, uint64_t(GL) * 2, 64, 128, SW);
   // gate/up: records' GU blocks [E][F rows][9L/8 bytes]
   ok &= make_tmap_3d(&pf->maps1.a_codes, ex, U8, gu_row, F, E, gu_row, d.expert_stride, 32, 64, 1, NS);
   ok &= make_tmap_3d(&pf->maps1.a_scales, ex, U8, gu_row, F, E, gu_row, d.expert_stride, L / 16, 64, 1, NS);
@@ -526,7 +588,8 @@ cudaError_t prefill_init(const edge0_moe_desc& d, PrefillWorkspace* pf, int num_
   ok &= make_tmap_2d(&pf->maps1.s_scales, sh, U8, 1, F, gu_row, gu_row, L / 16, 64, NS);
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   ok &= make_tmap_2d(&pf->maps1.b_routed, pf->zg, F16, 2, TK, L, uint64_t(L) * 2, 64, kGgBBox, SW);
-  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zh, F16, 2, T, L, uint64_t(L) * 2, 64, kGgBBox, SW);
+  ok &= make_tmap_2d(&pf->maps1.b_shared, pf->zh + size_t(gs) * L, F16, 2, T, L, uint64_t(GL) * 2, 64, kGgBBox,
+                     SW);
   // down: records' D blocks [E][L/2 row pairs][9F/8 bytes]
   ok &= make_tmap_3d(&pf->maps2.a_codes, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, 32, 64, 1, NS);
   ok &= make_tmap_3d(&pf->maps2.a_scales, ex + d_block, U8, d_pair, L / 2, E, d_pair, d.expert_stride, F / 8, 64, 1,
@@ -543,6 +606,7 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   if (!pf->rdcat) return EDGE0_ERR_UNSUPPORTED;
   if (T > pf->max_tokens) return EDGE0_ERR_INVALID_ARG;
   const int H = d.hidden, L = d.latent, E = d.n_experts, K = d.top_k, F = d.ffn;
+  const int G = pf_groups(d), GL = G * L;
   const int TK = T * K, nch = (T + kChunk - 1) / kChunk;
   CUtensorMap mx;
   if (!make_tmap_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, uint64_t(H) * 2, 64, 128,
@@ -562,8 +626,8 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   }
   // 1. x -> z (f16, scaled), logits
   if (e == cudaSuccess)
-    e = launch_gemm_pair<kPfStages>(mx, pf->m_D, pf->m_rdcat, T, L + 2 * E, H, L, pf->err, pf->abort,
-                                         EpiXZ{pf->zh, pf->zsc, pf->logits, d.router_bias, L, E}, s);
+    e = launch_gemm_pair<kPfStages>(mx, pf->m_D, pf->m_rdcat, T, GL + 2 * E, H, GL, pf->err, pf->abort,
+                                         EpiXZ{pf->zh, pf->zsc, pf->logits, d.router_bias, GL, E}, s);
   mark();
   // 2-4. routing and permutation
   if (e == cudaSuccess) {
@@ -589,7 +653,8 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   // 5. grouped z rows
   if (e == cudaSuccess) {
     const int blocks = std::min((TK + 7) / 8, num_sms * 16);
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(pf->zh, pf->zinv, pf->perm, TK, K, L, pf->zg, pf->pos_inv);
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(pf->zh, pf->zinv, pf->perm, TK, K, L, pf->idx,
+                                              G > 1 ? d.expert_group : nullptr, GL, pf->zg, pf->pos_inv);
     e = cudaGetLastError();
   }
   mark();
@@ -614,13 +679,17 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   mark();
   // 8. combine
   if (e == cudaSuccess) {
-    combine_kernel<<<T, (L / 8 + 31) / 32 * 32, 0, s>>>(pf->ob, pf->pos, pf->w, T, K, L, pf->cb);
+    if (G == 1)
+      combine_kernel<<<T, (L / 8 + 31) / 32 * 32, 0, s>>>(pf->ob, pf->pos, pf->w, T, K, L, pf->cb);
+    else
+      combine_grouped_kernel<<<T, 256, 0, s>>>(pf->ob, pf->pos, pf->w, pf->idx, d.expert_group, d.shared_group, T,
+                                               K, L, G, pf->cb);
     e = cudaGetLastError();
   }
   mark();
   // 9. y = c U^T
   if (e == cudaSuccess)
-    e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, L, 1 << 30, pf->err, pf->abort,
+    e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
                                          EpiStoreBF16{y, H, H}, s);
   mark();
   if (pf->profile && e == cudaSuccess) pf->timed = (stage == 11);
@@ -630,9 +699,10 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
 const void* prefill_debug_tensor(const PrefillWorkspace* pf, int what, const edge0_moe_desc& d, int T,
                                  size_t* bytes) {
   if (!pf->rdcat) return nullptr;
-  if (what == 0) { *bytes = size_t(T) * d.latent * 2; return pf->zh; }
+  const size_t GL = size_t(pf_groups(d)) * d.latent;
+  if (what == 0) { *bytes = size_t(T) * GL * 2; return pf->zh; }
   if (what == 1) { *bytes = size_t(T) * d.n_experts * 4; return pf->logits; }
-  if (what == 2) { *bytes = size_t(T) * d.latent * 2; return pf->cb; }
+  if (what == 2) { *bytes = size_t(T) * GL * 2; return pf->cb; }
   const size_t rows = size_t(T) * d.top_k + T;
   if (what == 3) { *bytes = rows * d.ffn * 2; return pf->hb; }
   if (what == 4) { *bytes = rows * d.latent * 2; return pf->ob; }

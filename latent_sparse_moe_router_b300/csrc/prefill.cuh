@@ -18,7 +18,7 @@ struct PrefillWorkspace {
   float dnorm = 0.f;                // max_r sum_h |D[r][h]|
   // prefill buffers (carved from the handle's workspace)
   __nv_bfloat16* rdcat = nullptr;   // [2E][hidden]: rows 2e, 2e+1 = bf16 high / low parts of R D row e
-  __half* zh = nullptr;             // [T][latent]  z * 2^-e_t in f16 (e_t: exponent of the bound
+  __half* zh = nullptr;             // [T][G latent]  z * 2^-e_t in f16 (e_t: exponent of the bound
                                     //               dnorm * max|x_t| of |z_t|, so |z * 2^-e_t| < 1)
   float* zsc = nullptr;             // [T] 2^-e_t
   float* zinv = nullptr;            // [T] 2^e_t
@@ -29,7 +29,7 @@ struct PrefillWorkspace {
   __half* zg = nullptr;             // [T K][latent] zh rows in expert-grouped order
   __nv_bfloat16* hb = nullptr;      // [T K + T][ffn] SwiGLU activations (routed, then shared)
   __nv_bfloat16* ob = nullptr;      // [T K + T][latent] expert outputs (routed, then shared)
-  __nv_bfloat16* cb = nullptr;      // [T][latent] combined latent
+  __nv_bfloat16* cb = nullptr;      // [T][G latent] combined latent (G latent groups)
   __nv_bfloat16* scratch = nullptr; // [T][hidden] layer output for stacked calls
   int* abort = nullptr;             // per-forward abort word of the bounded waits
   // stage timing (profiling): events[0] before the first kernel, events[i + 1]

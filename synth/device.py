@@ -92,10 +92,12 @@ class DeviceLayer:
         self.R = bf16_tensor(inputs.R)
         self.bias = None if inputs.bias is None else torch.from_numpy(inputs.bias).cuda()
         self.records, self.shared, self.stride = pack_layer_records(s, records, shared)
+        self.labels = torch.from_numpy(inputs.labels).cuda() if s.groups > 1 else None
         self.layer = ext.MoELayer(hidden=s.hidden, latent=s.latent, n_experts=s.n_experts, top_k=s.top_k,
                                   ffn=s.ffn, max_tokens=max_tokens, D=self.D, U=self.U, router=self.R,
                                   router_bias=self.bias, experts=self.records,
-                                  expert_stride=self.stride, shared_expert=self.shared)
+                                  expert_stride=self.stride, shared_expert=self.shared,
+                                  n_groups=s.groups, expert_group=self.labels, shared_group=s.shared_group)
 
     @property
     def handle(self):
@@ -123,10 +125,12 @@ class DeviceLayer:
 
     def debug_tensor(self, what: int, T: int):
         """Stage tensor of the last forward as float64 [T, n]: z (0), logits (1), c (2).
-        z and c are fp32 on the decode path (T <= 16); on the prefill path z is f16
-        times a per-token power of two and c is bf16."""
-        n = {0: self.spec.latent, 1: self.spec.n_experts, 2: self.spec.latent}[what]
-        if T > 16 and what in (0, 2):
+        z and c are fp32 on the decode path (T <= 16); on the prefill path (and at
+        every T for grouped layers) z is f16 times a per-token power of two and c is
+        bf16, both G * latent wide."""
+        GL = self.spec.groups * self.spec.latent
+        n = {0: GL, 1: self.spec.n_experts, 2: GL}[what]
+        if (T > 16 or self.spec.groups > 1) and what in (0, 2):
             # prefill: z as f16 scaled by a power of two per token, c as bf16
             out = torch.empty(T * n, dtype=torch.float16 if what == 0 else torch.bfloat16, device="cuda")
             ext.edge0_moe_debug_tensor(self.handle, what, out, out.numel() * 2)

@@ -17,12 +17,12 @@ def check_layer(dev, lay, x_bits: np.ndarray, y_gpu_bits: np.ndarray, routing: d
     checks to a sample of token rows (the permutation is always checked whole)."""
     T, k = routing["idx"].shape
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
-    ref = moe.layer_forward(lay, x_bits[sel], want=("logits", "idx", "w"))
+    ref = moe.forward(lay, x_bits[sel], want=("logits", "idx", "w"))
     gidx = routing["idx"][sel]
     flipped, bad = routing_flips(gidx, ref["logits"], k)
     assert not bad, f"routing differs beyond near-ties at tokens {bad[:8]}"
     if flipped:
-        ref = moe.layer_forward(lay, x_bits[sel], idx_override=gidx, want=("logits", "idx", "w"))
+        ref = moe.forward(lay, x_bits[sel], idx_override=gidx, want=("logits", "idx", "w"))
     w_ref = moe.routing_weights(ref["logits"], gidx)
     assert np.abs(routing["w"][sel] - w_ref).max() < 1e-5
     if check_perm:

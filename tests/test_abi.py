@@ -67,6 +67,18 @@ def test_create_rejects_bad_shapes_before_touching_the_device():
     assert h.value is None
 
 
+def test_create_rejects_bad_groups_before_touching_the_device():
+    import ctypes
+    stride = ext.edge0_expert_record_stride(1792, 640)
+    h = ctypes.c_void_p()
+    for n_groups, labels, shared in ((17, 256, 0), (-1, 256, 0), (2, None, 0), (2, 258, 0), (2, 256, 2),
+                                     (8, 256, -1), (16, 256, 0)):   # 16 x 1792 > 16384 latent columns
+        d = ext.edge0_moe_desc(2560, 1792, 512, 10, 640, 16, 256, 256, 256, None, 256, stride, 256,
+                               n_groups, labels, shared)
+        assert ext.lib().edge0_moe_create(ctypes.byref(d), ctypes.byref(h)) == ext.EDGE0_ERR_INVALID_ARG
+        assert h.value is None
+
+
 def _imports(path):
     tree = ast.parse(open(path).read())
     out = set()

@@ -198,11 +198,15 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def _oracle_layer(seed, layer, latent, zipf):
+def _oracle_layer(seed, layer, latent, zipf, groups=1, shared_group=0):
     import synth
     from oracle import moe
-    spec = synth.LayerSpec(seed=seed, layer=layer, latent=latent, zipf=zipf)
+    spec = synth.LayerSpec(seed=seed, layer=layer, latent=latent, zipf=zipf, groups=groups,
+                           shared_group=shared_group)
     inp = synth.make_layer(spec)
+    if groups > 1:
+        return moe.GroupedLayer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn,
+                                spec.top_k, inp.labels, shared_group), inp
     return moe.Layer(inp.D, inp.U, inp.R, inp.bias, inp.expert, inp.shared, spec.latent, spec.ffn,
                      spec.top_k), inp
 
@@ -217,14 +221,19 @@ def _pool_init():
 
 def oracle_task(task):
     """One parity task (run in a spawned worker): ("layer", seed, layer, latent, zipf,
-    x, y, idx) -> per-layer metrics on the GPU's input and routing; ("chain", seed,
-    n_layers, latent, zipfs, x, idx per layer, y) -> end-to-end error of the oracle
-    stack forced to the GPU's routing."""
+    x, y, idx) -> per-layer metrics on the GPU's input and routing (a grouped layer:
+    ("glayer", seed, layer, latent, zipf, groups, shared_group, x, y, idx)); ("chain",
+    seed, n_layers, latent, zipfs, x, idx per layer, y) -> end-to-end error of the
+    oracle stack forced to the GPU's routing."""
     from oracle import compare, moe
     import numpy as np
-    if task[0] == "layer":
-        _, seed, layer, latent, zipf, x, y, idx = task
-        lay, _ = _oracle_layer(seed, layer, latent, zipf)
+    if task[0] in ("layer", "glayer"):
+        if task[0] == "layer":
+            _, seed, layer, latent, zipf, x, y, idx = task
+            lay, _ = _oracle_layer(seed, layer, latent, zipf)
+        else:
+            _, seed, layer, latent, zipf, groups, sg, x, y, idx = task
+            lay, _ = _oracle_layer(seed, layer, latent, zipf, groups, sg)
         rel, mx, flips, bad = compare.layer_check_metrics(lay, x, y, idx)
         return {"kind": "layer", "rel_l2": rel, "max_abs_over_rms": mx, "flips": flips, "bad": len(bad),
                 "tokens": int(x.shape[0])}
@@ -893,6 +902,77 @@ def run_noalloc(args, rank, world, local, n=40):
     return out
 
 
+GROUPED = dict(latent=1792, groups=8, shared_group=0, seed=6, T=(1, 4096), inputs=16,
+               desc="one Edge0-145B layer with grouped latent projections: 8 D/U pairs, 64 experts per group")
+
+
+def run_grouped(args, rank, world, local, parity_tokens=4):
+    """A grouped layer (8 D/U pairs, each expert labelled with its group) at a decode
+    size and a prefill size.  Both run the prefill kernels.  T=1 is reported against
+    the HBM roofline (every group's D and U, the router operand, the distinct records,
+    x and y), T=4096 against the bf16 tensor roofline (the layer's FLOPs with all G
+    groups in D and U)."""
+    import numpy as np
+    import torch
+    import synth
+    import latent_sparse_moe_router_b300 as ext
+    from synth import device
+    torch.cuda.set_device(local)
+    g = GROUPED
+    L, G = g["latent"], g["groups"]
+    hbm, bf16, bf16_s, peak_kind = measured_peaks()
+    spec = synth.LayerSpec(seed=g["seed"], layer=0, latent=L, groups=G, shared_group=g["shared_group"])
+    d = device.DeviceLayer(synth.make_layer(spec), max_tokens=max(g["T"]))
+    stream = torch.cuda.Stream()
+    out = {"desc": g["desc"], "groups": G, "latent": L, "experts_per_group": E // G, "jobs": []}
+    for T in g["T"]:
+        n_in = g["inputs"] if T <= 16 else 2
+        x_bits = [synth.tokens_bf16(g["seed"] * 1000 + rank * 100 + 10 * T + i, T, HIDDEN) for i in range(n_in)]
+        xs = [device.bf16_tensor(b) for b in x_bits]
+        ys = [torch.empty_like(x) for x in xs]
+
+        def step(i, s):
+            ext.edge0_moe_forward(d.handle, xs[i % n_in], ys[i % n_in], T, s)
+        el_ms, steps_done, _, clocks = timed_region(step, args, stream, world, local)
+        ms = el_ms / steps_done
+        r = {"T": T, "value": round(T * world / (ms / 1e3), 1), "unit": "tok/s", "ms_per_step": round(ms, 6),
+             "clocks": clocks, "gpu_launches": ext.PREFILL_KERNELS_PER_FORWARD * steps_done,
+             "steps": steps_done}
+        if T <= 16:
+            distinct = []
+            for i in range(n_in):
+                ext.edge0_moe_forward(d.handle, xs[i], ys[i], T, stream)
+                stream.synchronize()
+                distinct.append(len(np.unique(d.routing(T)["idx"])))
+            nbytes = (2 * G * L * HIDDEN * 2 + E * HIDDEN * 4 + (np.mean(distinct) + 1) * record_bytes(L)
+                      + 2 * T * HIDDEN * 2)
+            ach = nbytes / (ms / 1e3) / 1e9
+            r["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(ach / hbm, 4), "traffic": None, "kernel": "whole forward",
+                             "bytes_per_forward": int(nbytes),
+                             "bytes": "all G D_g and U_g (bf16), the router operand R D (fp32), the "
+                                      "distinct routed records and the shared one, x and y",
+                             "peak_kind": f"{peak_kind} HBM copy bandwidth"}
+        else:
+            fl = T * (2 * HIDDEN * G * L + 2 * L * E + (K + 1) * 3 * 2 * L * F + 2 * G * L * HIDDEN)
+            tf = fl / (ms / 1e3) / 1e12
+            r["roofline"] = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16, "unit": "TFLOP/s",
+                             "frac": round(tf / bf16, 4), "traffic": None, "kernel": "whole forward",
+                             "flops_per_forward": fl, "frac_of_sustained": round(tf / bf16_s, 4),
+                             "peak_kind": f"{peak_kind} cuBLAS bf16 dense burst"}
+        # parity sample: seeded tokens of the timed input, oracle on the GPU's routing
+        ext.edge0_moe_forward(d.handle, xs[0], ys[0], T, stream)
+        stream.synchronize()
+        sel = np.sort(np.random.default_rng(78).choice(T, min(T, parity_tokens), replace=False))
+        idx = d.routing(T)["idx"][sel]
+        out["jobs"].append(("glayer", g["seed"], 0, L, 0.0, G, g["shared_group"], x_bits[0][sel],
+                            device.bf16_bits(ys[0])[sel], idx))
+        out[f"t{T}"] = r
+    assert ext.edge0_moe_get_error(d.handle) == ext.EDGE0_OK
+    d.close()
+    return out
+
+
 def config_of(name, wl, world):
     if wl["kind"] == "prefill":
         l2 = (f"inputs larger than L2: x {wl['T'] * HIDDEN * 2 / 1e6:.0f} MB per layer input, "
@@ -990,6 +1070,11 @@ def main():
             extra["tiered_decode"] = run_tiered(args, rank, world, local)
         if not args.only or "noalloc" in args.only.split(","):
             extra["noalloc_decode"] = run_noalloc(args, rank, world, local)
+        if not args.only or "grouped" in args.only.split(","):
+            torch.cuda.empty_cache()
+            gr = run_grouped(args, rank, world, local)
+            jobs["grouped_145b_g8"] = gr.pop("jobs")
+            extra["grouped_145b_g8"] = gr
     if rank != 0:
         return
     if pool is not None:

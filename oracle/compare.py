@@ -73,10 +73,10 @@ def error_metrics(y_gpu_bits: np.ndarray, y_ref: np.ndarray):
 def layer_check_metrics(lay, x_bits: np.ndarray, y_gpu_bits: np.ndarray, gidx: np.ndarray):
     """One layer on the other implementation's input and routing:
     (rel L2, max abs / rms, flipped token count, bad token list)."""
-    ref = moe.layer_forward(lay, x_bits, want=("logits",))
+    ref = moe.forward(lay, x_bits, want=("logits",))
     flipped, bad = routing_flips(gidx, ref["logits"], lay.k)
     if flipped:
-        ref = moe.layer_forward(lay, x_bits, idx_override=gidx)
+        ref = moe.forward(lay, x_bits, idx_override=gidx)
     rel, mx = error_metrics(y_gpu_bits, ref["y"])
     return rel, mx, len(flipped), bad
 
@@ -90,7 +90,7 @@ def stack_chain(lays, x_bits: np.ndarray, idx_per_layer, eps: float = 1e-6):
     n_flip, bad_all = 0, []
     for l, lay in enumerate(lays):
         idx = np.asarray(idx_per_layer[l], dtype=np.int32)
-        out = moe.layer_forward(lay, xb, idx_override=idx, want=("logits",))
+        out = moe.forward(lay, xb, idx_override=idx, want=("logits",))
         flipped, bad = routing_flips(idx, out["logits"], lay.k)
         n_flip += len(flipped)
         bad_all += [(l, t) for t in bad]

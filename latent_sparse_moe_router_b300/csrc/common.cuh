@@ -218,11 +218,13 @@ __device__ __forceinline__ bool grid_sync(GridBarrier* bar, int* err) {
   if (threadIdx.x == 0) {
     int ok = 1;
     unsigned long long tk;
-    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(tk) : "l"(&bar->ticket) : "memory");
+    // acquire-release: the CTA that arrives last sees every other arrival in the
+    // value it gets back and needs no further load; the others poll with acquire
+    // loads, the one that sees the round complete ordering this CTA after every
+    // other CTA's release (its arrival); the __syncthreads below passes that on
+    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(tk) : "l"(&bar->ticket) : "memory");
     const unsigned long long target = (tk / gridDim.x + 1) * gridDim.x;
-    // acquire loads: the load that sees the round complete orders this CTA after
-    // every other CTA's release (its arrival); the __syncthreads below passes that on
-    if (ld_acquire_u64(&bar->ticket) < target) {
+    if (tk + 1 != target && ld_acquire_u64(&bar->ticket) < target) {
       const unsigned long long t0 = globaltimer_ns();
       unsigned int spins = 0;
       while (ld_acquire_u64(&bar->ticket) < target) {

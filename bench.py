@@ -936,7 +936,8 @@ def run_grouped(args, rank, world, local, parity_tokens=4):
         el_ms, steps_done, _, clocks = timed_region(step, args, stream, world, local)
         ms = el_ms / steps_done
         r = {"T": T, "value": round(T * world / (ms / 1e3), 1), "unit": "tok/s", "ms_per_step": round(ms, 6),
-             "clocks": clocks, "gpu_launches": ext.PREFILL_KERNELS_PER_FORWARD * steps_done,
+             "clocks": clocks,
+             "gpu_launches": (ext.PREFILL_KERNELS_PER_FORWARD + (T <= ext.U_SPLIT_MAX_TOKENS)) * steps_done,
              "steps": steps_done}
         if T <= 16:
             distinct = []

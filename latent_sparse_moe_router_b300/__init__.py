@@ -37,6 +37,7 @@ EDGE0_PREFILL_STAGES = 10
 # kernels one prefill forward launches (token scale, x -> [z | logits], top-k +
 # histogram, scan, offsets, scatter, row gather, gate/up, down, combine, U)
 PREFILL_KERNELS_PER_FORWARD = 11
+U_SPLIT_MAX_TOKENS = 768          # prefill forwards up to this T split the U GEMM along K (one more kernel)
 PREFILL_STAGE_NAMES = ("xz_gemm", "topk_hist", "scan_chunks", "offsets", "scatter", "gather_rows",
                        "gate_up_grouped", "down_grouped", "combine", "u_gemm")
 

@@ -6,8 +6,11 @@
 // stages rows m0 + 128 r .. + 127 of A and rows n0 + 128 r .. + 127 of B (128 x 64,
 // 128-byte swizzle) per 64-wide k-step, so each SM moves half the B tile a
 // single-CTA 128 x 256 tile would need through its shared memory and from L2.
-// Persistent: the pairs walk the tiles (i -> m = i / n_tiles, n = i % n_tiles) with
-// a stride of the number of pairs.  Warp roles in both CTAs:
+// Persistent: the pairs walk the tiles (i -> split = i % k_splits, and with
+// j = i / k_splits, m = j / n_tiles, n = j % n_tiles) with a stride of the number of
+// pairs; a tile of split s covers k-steps [s nk / k_splits, (s + 1) nk / k_splits) and
+// hands its rows to the epilogue as row + s M (k_splits = 1: the whole K, row).
+// Warp roles in both CTAs:
 //   warp 0 (one lane): TMA producer; both CTAs' copies complete on rank 0's `full`
 //     barrier (two arrivals with their byte counts);
 //   warp 1 (one lane, rank 0 only): tcgen05.mma.cta_group::2 (M=256, N=256, K=16,
@@ -46,14 +49,15 @@ struct GemmPairSmem {
 };
 
 // Epilogue interface: operator()(int row, int col0, const float* v32) for the 32
-// consecutive columns col0 .. col0+31 of one row; rows >= M are not passed.
+// consecutive columns col0 .. col0+31 of one row (plus s M for split s of a K-split
+// launch); rows >= M are not passed.
 // Output columns [0, n_split) multiply B's rows, columns from n_split on multiply
 // B2's rows (n_split a multiple of 256; pass B2 = B for one matrix).
 template <int STAGES, class Epi>
 __global__ void __launch_bounds__(kGemmPairThreads, 1)
 gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmB2, int M, int N, int K, int n_split, int* err,
-                         int* abort, Epi epi) {
+                         const __grid_constant__ CUtensorMap tmB2, int M, int N, int K, int n_split,
+                         int k_splits, int* err, int* abort, Epi epi) {
   using S = GemmPairSmem<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -68,7 +72,7 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const uint32_t rank = cluster_ctarank();
   const int nk = K / 64;
   const int n_tiles = (N + 255) / 256;
-  const int total = ((M + 255) / 256) * n_tiles;
+  const int total = ((M + 255) / 256) * n_tiles * k_splits;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (pair >= total) return;   // both CTAs of the pair leave together
 
@@ -96,9 +100,11 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
       int it = 0;
       for (int tile = pair; ok && tile < total; tile += npairs) {
-        const int m0 = (tile / n_tiles) * 256, n0 = (tile % n_tiles) * 256;
+        const int ks = tile % k_splits, mn = tile / k_splits;
+        const int m0 = (mn / n_tiles) * 256, n0 = (mn % n_tiles) * 256;
         const int ya = m0 + 128 * int(rank), yb = n0 + 128 * int(rank);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int kb1 = (ks + 1) * nk / k_splits;
+        for (int kb = ks * nk / k_splits; kb < kb1; ++kb, ++it) {
           const int s = it % STAGES;
           if (!mbar_wait_abort(&empty[s], ((it / STAGES) & 1) ^ 1, err, abort)) { ok = false; break; }
           uint8_t* sa = smem + s * S::kStage;
@@ -120,7 +126,8 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         if (!mbar_wait_cl_abort(&acc_empty[ab], ((ti >> 1) & 1) ^ 1, err, abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int ks = tile % k_splits, kb0 = ks * nk / k_splits, kb1 = (ks + 1) * nk / k_splits;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % STAGES;
           // the stage's bytes were written by bulk copies: the barrier's completion orders
           // them before the MMA, no cluster-scope acquire is needed
@@ -130,7 +137,7 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           const uint32_t sb = sa + S::kA;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_pair_f16(acc, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), idesc, (kb | k) != 0);
+            mma_pair_f16(acc, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), idesc, kb != kb0 || k != 0);
           mma_pair_commit_both(&empty[s]);
         }
         if (!ok) break;
@@ -149,7 +156,8 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     int ti = 0;
     for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
-      const int m0 = (tile / n_tiles) * 256, n0 = (tile % n_tiles) * 256;
+      const int ks = tile % k_splits, mn = tile / k_splits;
+      const int m0 = (mn / n_tiles) * 256, n0 = (mn % n_tiles) * 256;
       const int ab = ti & 1;
       ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, err, abort);
       if (!gemm_named_and(1, 128, ok)) { ok = false; break; }
@@ -160,7 +168,7 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t r[32];
         tmem_ld32(tmem + (uint32_t(q * 32) << 16) + ab * 256 + c * 32, r);
         tmem_ld_wait();
-        if (row < M) epi(row, n0 + c * 32, reinterpret_cast<const float*>(r));
+        if (row < M) epi(row + ks * M, n0 + c * 32, reinterpret_cast<const float*>(r));
       }
       tc_fence_before();
       __syncwarp();
@@ -184,10 +192,12 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 }
 
 // Launch of one GEMM on CTA pairs: min(tiles, resident pairs) clusters of two.
-// A's, B's and B2's maps have 64 x 128 boxes (128-byte swizzle).  K a multiple of 64.
+// A's, B's and B2's maps have 64 x 128 boxes (128-byte swizzle).  K a multiple of 64,
+// 1 <= k_splits <= K / 64.
 template <int STAGES, class Epi>
 cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N,
-                             int K, int n_split, int* err, int* abort, const Epi& epi, cudaStream_t s) {
+                             int K, int n_split, int* err, int* abort, const Epi& epi, cudaStream_t s,
+                             int k_splits = 1) {
   using Sm = GemmPairSmem<STAGES>;
   auto kern = gemm_pair_bf16_tn_kernel<STAGES, Epi>;
   static int max_pairs = 0;
@@ -214,11 +224,12 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     max_pairs = clusters;
   }
-  const long tiles = long((M + 255) / 256) * ((N + 255) / 256);
+  if (k_splits < 1 || k_splits > K / 64) return cudaErrorInvalidValue;
+  const long tiles = long((M + 255) / 256) * ((N + 255) / 256) * k_splits;
   const int pairs = int(tiles < max_pairs ? tiles : max_pairs);
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, M, N, K, n_split, err, abort, epi);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, M, N, K, n_split, k_splits, err, abort, epi);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -37,6 +37,9 @@ namespace {
 
 constexpr int kChunk = 64;          // tokens per routing chunk
 constexpr int kPfBox = 128, kPfStages = 6;   // CTA-pair GEMM: 128-row B halves, 6 stages
+// U GEMM split along K when its output tiles would leave most SM pairs idle (few tokens):
+// at most kUSplits partial sums, for up to kUSplitTokens tokens
+constexpr int kUSplits = 8, kUSplitTokens = 768;
 
 size_t pf_align(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -99,6 +102,31 @@ struct EpiXZ {
     }
   }
 };
+
+// fp32 partial sums of a K-split GEMM: row r + s M of split s lands in part[s][r][..].
+struct EpiStoreF32 {
+  float* part;
+  int ldc;
+  __device__ __forceinline__ void operator()(int row, int col0, const float* v) const {
+    float4* dst = reinterpret_cast<float4*>(part + size_t(row) * ldc + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+};
+
+// y = bf16(sum over s = 0 .. S-1 of part[s]) element by element, in s order.
+__global__ void splitk_reduce_bf16_kernel(const float* __restrict__ part, int S, int MN, __nv_bfloat16* __restrict__ y) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < MN / 4; i += gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4*>(part)[i];
+    for (int sp = 1; sp < S; ++sp) {
+      const float4 b = reinterpret_cast<const float4*>(part + size_t(sp) * MN)[i];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    reinterpret_cast<uint2*>(y)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                                *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
 
 struct EpiStoreBF16 {
   __nv_bfloat16* C;
@@ -534,6 +562,7 @@ size_t prefill_workspace_bytes(const edge0_moe_desc& d, int max_tokens) {
   n += pf_align((T * K + T) * L * 2);         // ob
   n += pf_align(T * GL * 2);                  // cb
   n += pf_align(T * H * 2);                   // scratch
+  n += pf_align(size_t(kUSplits) * std::min<size_t>(T, kUSplitTokens) * H * 4);   // U partial sums
   n += pf_align(4);                           // abort
   return n;
 }
@@ -559,6 +588,7 @@ void prefill_workspace_carve(const edge0_moe_desc& d, int max_tokens, char* base
   pf->ob = reinterpret_cast<__nv_bfloat16*>(take((T * K + T) * L * 2));
   pf->cb = reinterpret_cast<__nv_bfloat16*>(take(T * GL * 2));
   pf->scratch = reinterpret_cast<__nv_bfloat16*>(take(T * H * 2));
+  pf->upart = reinterpret_cast<float*>(take(size_t(kUSplits) * std::min<size_t>(T, kUSplitTokens) * H * 4));
   pf->abort = reinterpret_cast<int*>(take(4));
 }
 
@@ -687,10 +717,24 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
     e = cudaGetLastError();
   }
   mark();
-  // 9. y = c U^T
-  if (e == cudaSuccess)
-    e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
-                                         EpiStoreBF16{y, H, H}, s);
+  // 9. y = c U^T; with few output tiles, split along K (partial sums, then their sum
+  // in split order) so that the SM pairs stream U together
+  if (e == cudaSuccess) {
+    const int pairs = num_sms / 2, tiles = ((T + 255) / 256) * ((H + 255) / 256);
+    const int ksp = T <= kUSplitTokens && 2 * tiles <= pairs ? std::min({kUSplits, pairs / tiles, GL / 128}) : 1;
+    if (ksp > 1) {
+      e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
+                                      EpiStoreF32{pf->upart, H}, s, ksp);
+      if (e == cudaSuccess) {
+        splitk_reduce_bf16_kernel<<<std::min((T * H / 4 + 255) / 256, num_sms * 4), 256, 0, s>>>(pf->upart, ksp,
+                                                                                                 T * H, y);
+        e = cudaGetLastError();
+      }
+    } else {
+      e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
+                                      EpiStoreBF16{y, H, H}, s);
+    }
+  }
   mark();
   if (pf->profile && e == cudaSuccess) pf->timed = (stage == 11);
   return e == cudaSuccess ? EDGE0_OK : EDGE0_ERR_CUDA;

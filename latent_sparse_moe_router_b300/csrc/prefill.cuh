@@ -31,6 +31,7 @@ struct PrefillWorkspace {
   __nv_bfloat16* ob = nullptr;      // [T K + T][latent] expert outputs (routed, then shared)
   __nv_bfloat16* cb = nullptr;      // [T][G latent] combined latent (G latent groups)
   __nv_bfloat16* scratch = nullptr; // [T][hidden] layer output for stacked calls
+  float* upart = nullptr;           // [splits][min(T, 768)][hidden] fp32 partial sums of a K-split U GEMM
   int* abort = nullptr;             // per-forward abort word of the bounded waits
   // stage timing (profiling): events[0] before the first kernel, events[i + 1]
   // after stage i

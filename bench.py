@@ -47,6 +47,10 @@ WORKLOADS = {
     "prefill4x145b_t16384": dict(kind="prefill", latent=1792, T=16384, seed=4, layers=4,
                                  zipf=(0.0, 1.1, 0.0, 1.1), instances=1,
                                  desc="4 Edge0-145B layers, prefill T=16384, uniform/Zipf(1.1) alternating"),
+    # the grouped layer of the default line's grouped object at its prefill size (profiling size)
+    "grouped145b_g8_t4096": dict(kind="prefill", latent=1792, T=4096, seed=6, layers=1, zipf=(0.0,), instances=1,
+                                 groups=8, shared_group=0,
+                                 desc="one Edge0-145B layer with 8 D/U pairs (64 experts per group), prefill T=4096"),
 }
 DEFAULT_WORKLOAD = "prefill4x145b_t16384"
 # reported with the default workload, each as an object of the same line
@@ -64,19 +68,20 @@ TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1524064000,
            ("layer145b_t1", "moe_decode_kernel"): 45104128}
 
 
-def flops_per_token_layer(latent):
-    """Algorithmic FLOPs of one token through one layer: D, router, k routed and
-    the shared SwiGLU expert, U (2 per multiply-add)."""
-    return 2 * HIDDEN * latent + 2 * latent * E + (K + 1) * 3 * 2 * latent * F + 2 * latent * HIDDEN
+def flops_per_token_layer(latent, groups=1):
+    """Algorithmic FLOPs of one token through one layer: D (every group), router, k
+    routed and the shared SwiGLU expert, U (every group) (2 per multiply-add)."""
+    return (2 * HIDDEN * groups * latent + 2 * latent * E + (K + 1) * 3 * 2 * latent * F
+            + 2 * groups * latent * HIDDEN)
 
 
-def stage_flops(latent, T):
+def stage_flops(latent, T, groups=1):
     """Algorithmic FLOPs per launch of the prefill stages that are contractions."""
     TK = T * K
-    return {"xz_gemm": 2 * T * HIDDEN * latent + 2 * T * latent * E,
+    return {"xz_gemm": 2 * T * HIDDEN * groups * latent + 2 * T * latent * E,
             "gate_up_grouped": 2 * (TK + T) * latent * 2 * F,
             "down_grouped": 2 * (TK + T) * F * latent,
-            "u_gemm": 2 * T * latent * HIDDEN}
+            "u_gemm": 2 * T * groups * latent * HIDDEN}
 
 
 def record_bytes(latent):
@@ -625,12 +630,14 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
 
     torch.cuda.set_device(local)
     T, L, n_layers = wl["T"], wl["latent"], wl["layers"]
+    G, sg = wl.get("groups", 1), wl.get("shared_group", 0)
     hbm, bf16, bf16_s, peak_kind = measured_peaks()
     stream = torch.cuda.Stream()
     n_inst = n_layers if n_layers > 1 else wl["instances"]
     insts = []
     for l in range(n_inst):
-        spec = synth.LayerSpec(seed=wl["seed"], layer=l, latent=L, zipf=wl["zipf"][l % len(wl["zipf"])])
+        spec = synth.LayerSpec(seed=wl["seed"], layer=l, latent=L, zipf=wl["zipf"][l % len(wl["zipf"])], groups=G,
+                               shared_group=sg)
         insts.append(device.DeviceLayer(synth.make_layer(spec), max_tokens=T))
     torch.cuda.synchronize()
     handles = [d.handle for d in insts]
@@ -638,7 +645,7 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
     x_bits = [synth.tokens_bf16(wl["seed"] * 1000 + rank * 100 + i, T, HIDDEN) for i in range(n_x)]
     xs = [device.bf16_tensor(b) for b in x_bits]
     ys = [torch.empty_like(x) for x in xs]
-    per_fwd = ext.PREFILL_KERNELS_PER_FORWARD
+    per_fwd = ext.PREFILL_KERNELS_PER_FORWARD + (T <= ext.U_SPLIT_MAX_TOKENS)
     if n_layers > 1:
         def step(i, s):
             ext.edge0_moe_stack_forward(handles, xs[0], ys[0], T, 1e-6, s)
@@ -653,7 +660,7 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
     el_ms, steps_done, reps, clocks = timed_region(step, args, stream, world, local)
     ms_per_step = el_ms / steps_done
     value = T * world / (ms_per_step / 1e3)          # tokens through the whole step per second
-    step_flops = T * n_layers * flops_per_token_layer(L)
+    step_flops = T * n_layers * flops_per_token_layer(L, G)
     step_tflops = step_flops / (ms_per_step / 1e3) / 1e12
 
     # per-kernel durations: the library's stage events on the launching stream,
@@ -681,7 +688,7 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
     stage_ms = sums / n_launch
     names = ext.PREFILL_STAGE_NAMES
     top = int(np.argmax(stage_ms))
-    sflops = stage_flops(L, T)
+    sflops = stage_flops(L, T, G)
     tname = names[top]
     if tname in sflops:
         ach = sflops[tname] / (stage_ms[top] / 1e3) / 1e12
@@ -697,7 +704,7 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
                 "kernel": tname, "note": "dominant stage is not a contraction"}
     roof["step"] = {"tflops": round(step_tflops, 1), "frac_burst": round(step_tflops / bf16, 4),
                     "frac_sustained": round(step_tflops / bf16_s, 4), "flops_per_step": step_flops,
-                    "flops_per_token_layer": flops_per_token_layer(L)}
+                    "flops_per_token_layer": flops_per_token_layer(L, G)}
     stages = {n: round(float(m), 4) for n, m in zip(names, stage_ms)}
     stages["timed_layer_ms_sum"] = round(float(stage_ms.sum()), 4)
 
@@ -713,8 +720,12 @@ def run_prefill(args, wl, rank, world, local, parity_tokens=8):
         stream.synchronize()
         idx = insts[l].routing(T)["idx"][sel]
         idx_layers.append(idx)
-        jobs.append(("layer", wl["seed"], l, L, wl["zipf"][l % len(wl["zipf"])],
-                     device.bf16_bits(cur)[sel], device.bf16_bits(yl)[sel], idx))
+        if G > 1:
+            jobs.append(("glayer", wl["seed"], l, L, wl["zipf"][l % len(wl["zipf"])], G, sg,
+                         device.bf16_bits(cur)[sel], device.bf16_bits(yl)[sel], idx))
+        else:
+            jobs.append(("layer", wl["seed"], l, L, wl["zipf"][l % len(wl["zipf"])],
+                         device.bf16_bits(cur)[sel], device.bf16_bits(yl)[sel], idx))
         if n_layers > 1:
             nx = torch.empty_like(cur)
             ext.edge0_residual_rmsnorm(cur, yl, nx, T, HIDDEN, 1e-6, stream)
@@ -983,9 +994,12 @@ def config_of(name, wl, world):
               f"(~{wl['instances'] * decode_algorithmic_bytes(wl['latent'], wl['T'], K * wl['T']) / 1e6:.0f} MB touched) > 126 MB L2")
     else:
         l2 = "48-layer stack, 47.6 GB of records > 126 MB L2"
-    return {"workload": name, "desc": wl["desc"], "hidden": HIDDEN, "latent": wl["latent"],
-            "experts": E, "top_k": K, "ffn": F, "T": wl["T"], "layers_per_step": wl["layers"],
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
+    out = {"workload": name, "desc": wl["desc"], "hidden": HIDDEN, "latent": wl["latent"],
+           "experts": E, "top_k": K, "ffn": F, "T": wl["T"], "layers_per_step": wl["layers"],
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
+    if wl.get("groups", 1) > 1:
+        out["latent_groups"] = wl["groups"]
+    return out
 
 
 def sub_line(name, r, world):

@@ -46,3 +46,13 @@ def test_gate_up_flops_per_launch_at_16k():
     # (T K + T) rows through the gate and up matrices [2F][l], 2 flops per multiply-add
     T, latent = 16384, 1792
     assert bench.stage_flops(latent, T)["gate_up_grouped"] == 2 * (T * 10 + T) * latent * 2 * 640 == 826_781_204_480
+
+
+def test_grouped_stage_flops_add_up_to_the_per_token_total():
+    T, L, G = 4096, 1792, 8
+    st = bench.stage_flops(L, T, G)
+    assert sum(st.values()) == T * bench.flops_per_token_layer(L, G)
+    # D and U of every group: G times the ungrouped projections, the experts unchanged
+    one = bench.stage_flops(L, T)
+    assert st["u_gemm"] == G * one["u_gemm"] and st["gate_up_grouped"] == one["gate_up_grouped"]
+    assert st["xz_gemm"] - 2 * T * L * bench.E == G * (one["xz_gemm"] - 2 * T * L * bench.E)

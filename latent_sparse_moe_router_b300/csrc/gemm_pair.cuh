@@ -21,6 +21,14 @@
 //     arrives on rank 0's `acc_empty` (eight arrivals).
 // Every wait is bounded; both CTAs run the same tile sequence and reach the
 // collective TMEM allocation and release.
+//
+// SWAP (few rows of A, M <= 64): the roles turn around so that the tensor cores do not
+// compute 256 padded rows.  The MMA's M side takes 256 rows of B (CTA r: rows
+// n0 + 128 r ..), its N side A's rows rounded up to NB, a multiple of 16 (CTA r: A rows
+// r NB/2 .. r NB/2 + NB/2 - 1, the A map's box NB/2 rows high), so the accumulator is
+// [B row][A row]: epilogue thread = one output column, and the epilogue's
+// swapped(row, col, v) takes one value of one output row at a time (all 32 lanes of a
+// warp call it together, for 32 consecutive columns).
 #pragma once
 
 #include "pair.cuh"
@@ -39,10 +47,11 @@ __device__ __forceinline__ bool gemm_named_and(int id, int n, bool pred) {
   return r != 0;
 }
 
-template <int STAGES>
+template <int STAGES, bool SWAP = false>
 struct GemmPairSmem {
-  static constexpr int kA = 128 * 64 * 2;   // one A stage (bytes)
-  static constexpr int kB = 128 * 64 * 2;   // one B stage (this CTA's half)
+  static constexpr int kA = 128 * 64 * 2;   // one A stage (bytes; with SWAP: B's 128 rows)
+  // one B stage (this CTA's half; with SWAP: A's NB/2 <= 32 rows)
+  static constexpr int kB = SWAP ? 32 * 64 * 2 : 128 * 64 * 2;
   static constexpr int kStage = kA + kB;
   // barriers and tmem slot, alignment, and 16 KB of slack past the last stage
   static constexpr int kBytes = STAGES * kStage + 1024 + 1024 + 16384;
@@ -53,12 +62,12 @@ struct GemmPairSmem {
 // launch); rows >= M are not passed.
 // Output columns [0, n_split) multiply B's rows, columns from n_split on multiply
 // B2's rows (n_split a multiple of 256; pass B2 = B for one matrix).
-template <int STAGES, class Epi>
+template <int STAGES, class Epi, bool SWAP>
 __global__ void __launch_bounds__(kGemmPairThreads, 1)
 gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmB2, int M, int N, int K, int n_split,
                          int k_splits, int* err, int* abort, Epi epi) {
-  using S = GemmPairSmem<STAGES>;
+  using S = GemmPairSmem<STAGES, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * S::kStage);   // rank 0: 2 arrivals + bytes
@@ -72,7 +81,9 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const uint32_t rank = cluster_ctarank();
   const int nk = K / 64;
   const int n_tiles = (N + 255) / 256;
-  const int total = ((M + 255) / 256) * n_tiles * k_splits;
+  const int m_tiles = SWAP ? 1 : (M + 255) / 256;
+  const int NB = SWAP ? (M + 15) & ~15 : 256;     // the MMA's N
+  const int total = m_tiles * n_tiles * k_splits;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (pair >= total) return;   // both CTAs of the pair leave together
 
@@ -109,17 +120,25 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           if (!mbar_wait_abort(&empty[s], ((it / STAGES) & 1) ^ 1, err, abort)) { ok = false; break; }
           uint8_t* sa = smem + s * S::kStage;
           const uint32_t fb = full0 + uint32_t(s) * 8u;
-          mbar_arrive_expect_tx_cl(fb, S::kStage);
-          tma_load_2d_pair(sa, &tmA, kb * 64, ya, fb);
-          // columns [0, n_split) come from B's rows, later columns from B2's rows
-          if (n0 < n_split) tma_load_2d_pair(sa + S::kA, &tmB, kb * 64, yb, fb);
-          else tma_load_2d_pair(sa + S::kA, &tmB2, kb * 64, yb - n_split, fb);
+          if constexpr (SWAP) {
+            // M side: B's (or B2's) 128 rows of this CTA; N side: A's NB / 2 rows
+            mbar_arrive_expect_tx_cl(fb, S::kA + uint32_t(NB / 2) * 128u);
+            if (n0 < n_split) tma_load_2d_pair(sa, &tmB, kb * 64, yb, fb);
+            else tma_load_2d_pair(sa, &tmB2, kb * 64, yb - n_split, fb);
+            tma_load_2d_pair(sa + S::kA, &tmA, kb * 64, (NB / 2) * int(rank), fb);
+          } else {
+            mbar_arrive_expect_tx_cl(fb, S::kStage);
+            tma_load_2d_pair(sa, &tmA, kb * 64, ya, fb);
+            // columns [0, n_split) come from B's rows, later columns from B2's rows
+            if (n0 < n_split) tma_load_2d_pair(sa + S::kA, &tmB, kb * 64, yb, fb);
+            else tma_load_2d_pair(sa + S::kA, &tmB2, kb * 64, yb - n_split, fb);
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(256, 256);
+      const uint32_t idesc = idesc_bf16_f32(256, NB);
       int it = 0, ti = 0;
       for (int tile = pair; ok && tile < total; tile += npairs, ++ti) {
         const int ab = ti & 1;
@@ -162,13 +181,26 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       ok = mbar_wait_abort(&acc_full[ab], (ti >> 1) & 1, err, abort);
       if (!gemm_named_and(1, 128, ok)) { ok = false; break; }
       tc_fence_after();
-      const int row = m0 + 128 * int(rank) + q * 32 + lane;
+      if constexpr (SWAP) {
+        // thread = output column n0 + 128 rank + 32 q + lane; accumulator column = A row
+        const int col = n0 + 128 * int(rank) + q * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + ab * 256 + c * 32, r);
-        tmem_ld_wait();
-        if (row < M) epi(row + ks * M, n0 + c * 32, reinterpret_cast<const float*>(r));
+        for (int c = 0; c * 32 < M; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + (uint32_t(q * 32) << 16) + ab * 256 + c * 32, r);
+          tmem_ld_wait();
+          const int nr = min(32, M - 32 * c);
+          for (int j = 0; j < nr; ++j) epi.swapped(32 * c + j + ks * M, col, __uint_as_float(r[j]));
+        }
+      } else {
+        const int row = m0 + 128 * int(rank) + q * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + (uint32_t(q * 32) << 16) + ab * 256 + c * 32, r);
+          tmem_ld_wait();
+          if (row < M) epi(row + ks * M, n0 + c * 32, reinterpret_cast<const float*>(r));
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -192,14 +224,15 @@ gemm_pair_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 }
 
 // Launch of one GEMM on CTA pairs: min(tiles, resident pairs) clusters of two.
-// A's, B's and B2's maps have 64 x 128 boxes (128-byte swizzle).  K a multiple of 64,
+// A's, B's and B2's maps have 64 x 128 boxes (128-byte swizzle); with SWAP, A's box is
+// 64 x NB/2 (NB = M rounded up to 16) and M <= 64.  K a multiple of 64,
 // 1 <= k_splits <= K / 64.
-template <int STAGES, class Epi>
+template <int STAGES, class Epi, bool SWAP = false>
 cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M, int N,
                              int K, int n_split, int* err, int* abort, const Epi& epi, cudaStream_t s,
                              int k_splits = 1) {
-  using Sm = GemmPairSmem<STAGES>;
-  auto kern = gemm_pair_bf16_tn_kernel<STAGES, Epi>;
+  using Sm = GemmPairSmem<STAGES, SWAP>;
+  auto kern = gemm_pair_bf16_tn_kernel<STAGES, Epi, SWAP>;
   static int max_pairs = 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -224,8 +257,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     max_pairs = clusters;
   }
-  if (k_splits < 1 || k_splits > K / 64) return cudaErrorInvalidValue;
-  const long tiles = long((M + 255) / 256) * ((N + 255) / 256) * k_splits;
+  if (k_splits < 1 || k_splits > K / 64 || (SWAP && M > 64)) return cudaErrorInvalidValue;
+  const long tiles = long(SWAP ? 1 : (M + 255) / 256) * ((N + 255) / 256) * k_splits;
   const int pairs = int(tiles < max_pairs ? tiles : max_pairs);
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);

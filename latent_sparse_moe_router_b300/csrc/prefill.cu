@@ -40,6 +40,10 @@ constexpr int kPfBox = 128, kPfStages = 6;   // CTA-pair GEMM: 128-row B halves,
 // U GEMM split along K when its output tiles would leave most SM pairs idle (few tokens):
 // at most kUSplits partial sums, for up to kUSplitTokens tokens
 constexpr int kUSplits = 8, kUSplitTokens = 768;
+// up to this many tokens the dense GEMMs put the weights on the MMA's M side and the
+// tokens on N (rounded up to 16) instead of padding the tokens to 256 rows
+constexpr int kSwapTokens = 64;
+constexpr int kSwapStages = 10;     // their stages are 20 KB (16 KB of weights + <= 4 KB of tokens)
 
 size_t pf_align(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -101,6 +105,18 @@ struct EpiXZ {
       }
     }
   }
+  // one value of output (row, col); the 32 lanes of a warp hold 32 consecutive columns
+  // (L is a multiple of 32, so a warp is on one side of it; router columns 2e, 2e + 1
+  // are lanes of the same warp)
+  __device__ __forceinline__ void swapped(int row, int col, float v) const {
+    if (col < L) {
+      zh[size_t(row) * L + col] = __float2half_rn(v * zsc[row]);
+    } else {
+      const float lo = __shfl_down_sync(0xFFFFFFFFu, v, 1);
+      const int e = (col - L) >> 1;
+      if (!(col & 1) && e < E) logits[size_t(row) * E + e] = (v + lo) + (bias ? bias[e] : 0.f);
+    }
+  }
 };
 
 // fp32 partial sums of a K-split GEMM: row r + s M of split s lands in part[s][r][..].
@@ -111,6 +127,9 @@ struct EpiStoreF32 {
     float4* dst = reinterpret_cast<float4*>(part + size_t(row) * ldc + col0);
 #pragma unroll
     for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+  __device__ __forceinline__ void swapped(int row, int col, float v) const {
+    if (col < ldc) part[size_t(row) * ldc + col] = v;
   }
 };
 
@@ -148,6 +167,9 @@ struct EpiStoreBF16 {
       for (int i = 0; i < 32; ++i)
         if (col0 + i < N) dst[i] = __float2bfloat16_rn(v[i]);
     }
+  }
+  __device__ __forceinline__ void swapped(int row, int col, float v) const {
+    if (col < N) C[size_t(row) * ldc + col] = __float2bfloat16_rn(v);
   }
 };
 
@@ -655,9 +677,21 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
     e = cudaGetLastError();
   }
   // 1. x -> z (f16, scaled), logits
-  if (e == cudaSuccess)
-    e = launch_gemm_pair<kPfStages>(mx, pf->m_D, pf->m_rdcat, T, GL + 2 * E, H, GL, pf->err, pf->abort,
-                                         EpiXZ{pf->zh, pf->zsc, pf->logits, d.router_bias, GL, E}, s);
+  const bool swap = T <= kSwapTokens;
+  const uint32_t nb2 = uint32_t(((T + 15) & ~15) / 2);   // token rows per CTA with swapped roles
+  if (e == cudaSuccess) {
+    const EpiXZ epi{pf->zh, pf->zsc, pf->logits, d.router_bias, GL, E};
+    if (swap) {
+      CUtensorMap mxs;
+      if (!make_tmap_2d(&mxs, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, uint64_t(H) * 2, 64, nb2,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return EDGE0_ERR_CUDA;
+      e = launch_gemm_pair<kSwapStages, EpiXZ, true>(mxs, pf->m_D, pf->m_rdcat, T, GL + 2 * E, H, GL, pf->err,
+                                                   pf->abort, epi, s);
+    } else {
+      e = launch_gemm_pair<kPfStages>(mx, pf->m_D, pf->m_rdcat, T, GL + 2 * E, H, GL, pf->err, pf->abort, epi, s);
+    }
+  }
   mark();
   // 2-4. routing and permutation
   if (e == cudaSuccess) {
@@ -722,14 +756,25 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   if (e == cudaSuccess) {
     const int pairs = num_sms / 2, tiles = ((T + 255) / 256) * ((H + 255) / 256);
     const int ksp = T <= kUSplitTokens && 2 * tiles <= pairs ? std::min({kUSplits, pairs / tiles, GL / 128}) : 1;
+    CUtensorMap mcs;                          // c rows, boxes of nb2 rows (swapped roles)
+    if (swap && !make_tmap_2d(&mcs, pf->cb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, GL, uint64_t(GL) * 2, 64, nb2,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+      return EDGE0_ERR_CUDA;
     if (ksp > 1) {
-      e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
-                                      EpiStoreF32{pf->upart, H}, s, ksp);
+      if (swap)
+        e = launch_gemm_pair<kSwapStages, EpiStoreF32, true>(mcs, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err,
+                                                           pf->abort, EpiStoreF32{pf->upart, H}, s, ksp);
+      else
+        e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
+                                        EpiStoreF32{pf->upart, H}, s, ksp);
       if (e == cudaSuccess) {
         splitk_reduce_bf16_kernel<<<std::min((T * H / 4 + 255) / 256, num_sms * 4), 256, 0, s>>>(pf->upart, ksp,
                                                                                                  T * H, y);
         e = cudaGetLastError();
       }
+    } else if (swap) {
+      e = launch_gemm_pair<kSwapStages, EpiStoreBF16, true>(mcs, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err,
+                                                          pf->abort, EpiStoreBF16{y, H, H}, s);
     } else {
       e = launch_gemm_pair<kPfStages>(pf->m_cb, pf->m_U, pf->m_U, T, H, GL, 1 << 30, pf->err, pf->abort,
                                       EpiStoreBF16{y, H, H}, s);

@@ -165,6 +165,9 @@ typedef struct {
  * Runs the router fold and the |z| bound on the device (legacy stream) and
  * synchronises before returning.
  * Returns INVALID_ARG, UNSUPPORTED, CUDA or OOM on failure (*handle_out = NULL).
+ * Source: the layer's parts and widths, "Edge0-145B hardware requirements",
+ * section "Edge0-145B latent MoE architecture: how 145B fits one GPU"; the D/U
+ * groups and expert labels, the same section.
  */
 edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);
 
@@ -176,6 +179,8 @@ edge0_status edge0_moe_create(const edge0_moe_desc *desc, void **handle_out);
  * layer (G > 1) runs the prefill path's kernels at every T.
  * Calls on one handle must be ordered (one stream, or synchronised): they
  * share the handle's workspace.
+ * Source: the layer's steps (D, router, 10 of 512 experts l -> 640 -> l with a
+ * shared expert, U), "Edge0-145B · Q3_K" model card, section "Architecture".
  */
 edge0_status edge0_moe_forward(void *handle, const void *x, void *y, int T,
                                edge0_stream_t stream);
@@ -243,6 +248,9 @@ edge0_status edge0_residual_rmsnorm(const void *x, const void *y, void *out, int
  * uploads it (stream-ordered).  A call captured into a CUDA graph must use the
  * list of the preceding uncaptured call on handles[0]; otherwise it returns
  * EDGE0_ERR_UNSUPPORTED (the graph would reference host memory).
+ * Source: 48 layers per model, model card "Edge0-145B · Q3_K", section
+ * "Architecture" (config block); the residual norm between layers is this
+ * library's reading (the pages give none).
  */
 edge0_status edge0_moe_stack_forward(void *const *handles, int n_layers, const void *x,
                                      void *y, int T, float eps, edge0_stream_t stream);
@@ -375,6 +383,9 @@ edge0_status edge0_moe_tier_detach(void *handle);
  * [n_slots], -1 empty) and still chosen keeps its slot; the other chosen experts fill
  * the remaining slots in rank order; a slot left over keeps its current expert.
  * Returns the number of slots whose expert changes, or -1 on bad arguments.
+ * Source: hot experts resident in VRAM, the rest in host RAM ("Edge0-145B en
+ * local", introduction; "Edge0-145B hardware requirements", flags table:
+ * --resident-budget-gib); the most-used policy is this library's reading.
  */
 int edge0_tier_plan(const unsigned int *use, int n_experts, int n_slots, const int *cur, int *next);
 

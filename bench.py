@@ -65,7 +65,7 @@ MIN_TIMED_S = 2.0
 # layer of the 16K workload (profiles/ncu_grouped_nvfp4_layer145b_t16384.md), the decode
 # kernel on one layer at T=1 (profiles/ncu_moe_decode_layer145b_t1_t16.md)
 TRAFFIC = {("prefill4x145b_t16384", "gate_up_grouped"): 1524064000,
-           ("layer145b_t1", "moe_decode_kernel"): 45104128}
+           ("layer145b_t1", "moe_decode_kernel"): 45092608}
 
 
 def flops_per_token_layer(latent, groups=1):

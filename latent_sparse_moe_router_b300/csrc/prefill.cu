@@ -124,9 +124,15 @@ struct EpiStoreF32 {
   float* part;
   int ldc;
   __device__ __forceinline__ void operator()(int row, int col0, const float* v) const {
-    float4* dst = reinterpret_cast<float4*>(part + size_t(row) * ldc + col0);
+    float* dst = part + size_t(row) * ldc + col0;
+    if (col0 + 32 <= ldc) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < ldc) dst[i] = v[i];
+    }
   }
   __device__ __forceinline__ void swapped(int row, int col, float v) const {
     if (col < ldc) part[size_t(row) * ldc + col] = v;

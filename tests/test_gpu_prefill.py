@@ -271,3 +271,23 @@ def test_prefill_t16384_bit_reproducible(dev, zipf):
         assert np.array_equal(y, ys[0])
     assert ext.edge0_moe_get_error(d.handle) == ext.EDGE0_OK
     d.close()
+
+
+@pytest.mark.parametrize("T", [17, 64, 65, 300, 800])
+def test_prefill_partial_output_tiles(dev, T):
+    """hidden = 576 is two 256-column output tiles and a partial third: the D GEMM's
+    latent and router columns and the U GEMM's columns end inside a tile, with the
+    tokens on the MMA's N side (T <= 64), the U GEMM split along K (T <= 768) and
+    neither (T = 800)."""
+    inp = synth.make_layer(small_spec(seed=29, hidden=576, zipf=0.4))
+    d = dev.DeviceLayer(inp, max_tokens=800)
+    lay = oracle_layer(inp)
+    x_bits = synth.tokens_bf16(70 + T, T, 576)
+    y = d.forward(dev_bf16(x_bits))
+    torch.cuda.synchronize()
+    assert ext.edge0_moe_get_error(d.handle) == ext.EDGE0_OK
+    sel = None if T <= 300 else np.arange(0, T, 7)
+    # outputs here reach 5x their rms, where half a bf16 ulp is already 1 % of it
+    m = check_layer(d, lay, x_bits, bits(y), d.routing(T), tokens=sel, out_ulp=True)
+    assert m["tokens"] == (T if sel is None else len(sel))
+    d.close()

@@ -215,3 +215,10 @@ def test_layer_matches_per_token_brute_force():
             Wg, Wu, Wd = mats(inp.expert(e))
             ct = ct + wt[j] * (Wd @ (torch.nn.functional.silu(Wg @ zt) * (Wu @ zt)))
         assert np.allclose(y[t], (U @ ct).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_bf16_ulp_of_the_parity_check():
+    import parity
+    v = np.array([1.0, 1.5, -0.065, 3.0e-3, 0.0])
+    # 8 significant bits: ulp = 2^(exponent - 7)
+    assert np.array_equal(parity.bf16_ulp(v), [2.0 ** -7, 2.0 ** -7, 2.0 ** -11, 2.0 ** -16, 0.0])

@@ -5,35 +5,38 @@
 // "Edge0-145B en local", introduction).  Tokens are grouped by expert (positions
 // p of the permutation); a work tile is (group g, token tile nt, weight tile mt),
 // and a cluster of two CTAs on two SMs (a pair) runs the weight tiles 2u, 2u + 1 of
-// one token tile as one M = 256 tcgen05.mma.cta_group::2:
-//   MODE 1 (gate/up): A = 64 gate rows + 64 up rows (f0 = 64 mt), B = BN token
-//     rows of the group (z * 2^-e_t in f16), K = l; f16 operands; epilogue
+// one token tile of up to 256 rows as tcgen05.mma.cta_group::2 with the tokens on
+// the MMA's M side (128 rows per CTA, so each TMEM lane is one token) and the
+// weights on its N side (256: the two CTAs' dequantised tiles of 128 rows):
+//   MODE 1 (gate/up): weight tile = 64 gate rows + 64 up rows (f0 = 64 mt), token
+//     rows = z * 2^-e_t in f16 of the group, K = l; f16 operands; epilogue
 //     h = silu(g_gate 2^e_t gate) * (g_up 2^e_t up), stored bf16 to H[p][f].
-//   MODE 2 (down):    A = 128 latent rows (r0 = 128 mt, 64 row pairs), B = BN rows
-//     of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
+//   MODE 2 (down):    weight tile = 128 latent rows (r0 = 128 mt, 64 row pairs),
+//     token rows = rows of H, K = F; epilogue o = g_down * acc, stored bf16 to O[p][r].
 // Persistent pairs (one CTA per SM) walk the pair tiles in index order with a
 // stride of the number of pairs, pair tile = (token tile, weight-tile pair u) with
 // u fastest, so the pairs working at one time share a few token tiles through L2.
-// CTA r of a pair owns weight tile 2u + r: it dequantises those 128 A rows, stages
-// half of the tile's B rows (columns r N/2 .. r N/2 + N/2 - 1 of the MMA) and holds
-// the accumulator rows of its A rows in its own TMEM.  Warp roles in both CTAs:
+// CTA r of a pair owns weight tile 2u + r (it dequantises those 128 rows: columns
+// 128 r .. 128 r + 127 of the MMA's N) and token rows 128 r .. 128 r + 127 of the
+// tile (its accumulator lanes).  Warp roles in both CTAs:
 //   warp 0 (one lane): TMA producer of the tile's E4M3 scales (double-buffered)
 //     and raw NVFP4 codes (4 KB per 64-wide k-step, 6-deep ring);
-//   warp 18 (one lane): TMA producer of this CTA's half of the B rows (64-row
-//     boxes, 128-byte swizzle), into the stages the MMA releases; completion on
-//     rank 0's barrier;
-//   warp 1 (one lane, rank 0 only): tcgen05.mma.cta_group::2, M=256, N = the
-//     tile's rows rounded to 16, K=16, into one of two TMEM accumulators of 256
-//     columns in each CTA; commits arrive in both CTAs;
-//   warps 2-9: dequantisation, two threads per A row, exact: mode 1 E2M1 -> f16
+//   warp 18 (one lane): TMA producer of this CTA's 128 token rows (64-row boxes,
+//     128-byte swizzle; boxes wholly past the tile's rows skipped), into the stages
+//     the MMA releases; completion on rank 0's barrier;
+//   warp 1 (one lane, rank 0 only): tcgen05.mma.cta_group::2, M=256 (tokens),
+//     N=256 (weights), K=16, into one of two TMEM accumulators of 256 columns in
+//     each CTA; commits arrive in both CTAs;
+//   warps 2-9: dequantisation, two threads per weight row, exact: mode 1 E2M1 -> f16
 //     by cvt times the E4M3 scale in one f16x2 multiply; mode 2 the same f16
 //     moved to the bf16 exponent range with shift/mask and multiplied by the
-//     block scale * 2^112 in bf16x2; into 128-byte-swizzled A tiles; each warp
+//     block scale * 2^112 in bf16x2; into 128-byte-swizzled tiles; each warp
 //     then arrives on rank 0's stage barrier;
-//   warps 10-17: epilogue of the previous accumulator (TMEM -> registers ->
-//     shared-memory transpose -> whole-row global stores; two warps per TMEM lane
-//     quarter, one per half of each 32-column chunk) while the next tile's main
-//     loop runs; each warp then arrives on rank 0's accumulator barrier.
+//   warps 10-17: epilogue of the previous accumulator (TMEM lane = token; two warps
+//     per TMEM lane quarter, one per half of the 256 weight columns; each warp's 32
+//     token rows staged in a padded buffer and stored as whole 16-byte pieces of
+//     their output rows) while the next tile's main loop runs; each warp then arrives
+//     on rank 0's accumulator barrier.
 #pragma once
 
 #include "pair.cuh"

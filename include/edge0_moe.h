@@ -260,8 +260,8 @@ edge0_status edge0_moe_stack_forward(void *const *handles, int n_layers, const v
  * routing (for layer-by-layer checks): trace_x, trace_y device bf16
  * [n_layers][T][hidden]; trace_idx device int32 [n_layers][T][top_k], the
  * experts each layer kept for each token in rank order (any may be NULL).
- * Decode sizes only (T <= 16, n_layers <= 64); other sizes return UNSUPPORTED
- * when a trace is requested.
+ * Decode sizes of one-group layers only (T <= 16, n_layers <= 64, n_groups <= 1);
+ * other calls return UNSUPPORTED when a trace is requested.
  */
 edge0_status edge0_moe_stack_forward_trace(void *const *handles, int n_layers, const void *x,
                                            void *y, int T, float eps, void *trace_x,

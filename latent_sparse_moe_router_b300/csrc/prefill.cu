@@ -497,8 +497,8 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ ob, const int* 
 
 // Grouped projections: c[t][g L + j] = [g = gs] O[TK + t][j] + sum over k with
 // labels[idx[t,k]] = g of w[t,k] O[pos[t,k]][j]  (fp32, k in rank order) -> bf16;
-// a group nobody used gets zeros.  Block = one token, thread = 8 columns of the
-// G L wide row at a time.
+// a group nobody used gets zeros.  Block (t, y) = token t, columns from 2048 y in
+// steps of 2048 gridDim.y; thread = 8 columns at a time.
 __global__ void __launch_bounds__(256) combine_grouped_kernel(const __nv_bfloat16* __restrict__ ob,
                                                               const int* __restrict__ pos,
                                                               const float* __restrict__ w,
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(256) combine_grouped_kernel(const __nv_bfloat1
                                                               __nv_bfloat16* __restrict__ cb) {
   const int t = blockIdx.x, GL = G * L;
   const size_t TK = size_t(T) * K;
-  for (int col = threadIdx.x * 8; col < GL; col += blockDim.x * 8) {
+  for (int col = (blockIdx.y * blockDim.x + threadIdx.x) * 8; col < GL; col += gridDim.y * blockDim.x * 8) {
     const int g = col / L, j = col - g * L;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (g == gs) {
@@ -749,11 +749,14 @@ edge0_status prefill_forward(const edge0_moe_desc& d, PrefillWorkspace* pf, int 
   mark();
   // 8. combine
   if (e == cudaSuccess) {
-    if (G == 1)
+    if (G == 1) {
       combine_kernel<<<T, (L / 8 + 31) / 32 * 32, 0, s>>>(pf->ob, pf->pos, pf->w, T, K, L, pf->cb);
-    else
-      combine_grouped_kernel<<<T, 256, 0, s>>>(pf->ob, pf->pos, pf->w, pf->idx, d.expert_group, d.shared_group, T,
-                                               K, L, G, pf->cb);
+    } else {
+      // enough blocks for the SMs when there are few tokens, one per token otherwise
+      const int gy = std::max(1, std::min((GL + 2047) / 2048, (8 * num_sms + T - 1) / T));
+      combine_grouped_kernel<<<dim3(T, gy), 256, 0, s>>>(pf->ob, pf->pos, pf->w, pf->idx, d.expert_group,
+                                                         d.shared_group, T, K, L, G, pf->cb);
+    }
     e = cudaGetLastError();
   }
   mark();
